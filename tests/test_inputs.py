@@ -1,0 +1,48 @@
+"""Checks of the seeded input recipe (CPU only)."""
+import numpy as np
+
+from weight_only_int4_moe_gb300 import inputs
+
+
+def test_bf16_rounding_is_rne():
+    vals = np.array([1.0, 1.00390625, 1.01171875, -3.5, 0.0, 1e-3], dtype=np.float32)
+    b = inputs.bf16_bits_from_f32(vals)
+    # 1 + 2^-8 is a tie between 1 and 1+2^-7: ties to even -> 1.0 (0x3F80)
+    assert b[0] == 0x3F80 and b[1] == 0x3F80
+    # 1 + 3*2^-8 is a tie between 1+2^-7 (odd) and 1+2^-6 (even) -> 0x3F82
+    assert b[2] == 0x3F82
+    assert inputs.f32_from_bf16_bits(b[3]) == -3.5
+    back = inputs.f32_from_bf16_bits(b)
+    assert np.all(np.abs(back - vals) <= np.abs(vals) * 2 ** -8)
+
+
+def test_weights_shapes_ranges_and_determinism():
+    w = inputs.make_weights(4, 64, 32, 3)
+    assert w["q13"].shape == (4, 64, 32) and w["s13"].shape == (4, 64, 2)
+    assert w["q2"].shape == (4, 64, 16) and w["s2"].shape == (4, 64, 1)
+    s = inputs.f32_from_bf16_bits(w["s13"])
+    assert s.min() >= 0.0049 and s.max() <= 0.0201
+    w2 = inputs.make_weights(4, 64, 32, 3)
+    for k in w:
+        np.testing.assert_array_equal(w[k], w2[k])
+    nib = np.concatenate([w["q13"].reshape(-1) & 15, w["q13"].reshape(-1) >> 4])
+    assert set(np.unique(nib).tolist()) == set(range(16))
+
+
+def test_routing_uniform():
+    cfg = inputs.CONFIGS[0]
+    t = inputs.make_tokens(cfg, 16)
+    ids, w = t["topk_ids"], t["topk_weights"]
+    assert ids.shape == (16, 2) and w.shape == (16, 2)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-6)
+    assert np.all(w[:, 0] >= w[:, 1])
+    assert all(len(set(r)) == 2 for r in ids.tolist())
+
+
+def test_routing_skewed_share():
+    cfg = inputs.CONFIGS[2]
+    small = inputs.MoEConfig("s", 384, 8, 64, 64, (256,), "skewed", 1, 2)
+    t = inputs.make_tokens(small, 256)
+    assert abs(t["hot_share"] - 0.5) <= 0.011
+    assert len(t["hot"]) == 77
+    assert cfg.routing == "skewed"
