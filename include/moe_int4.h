@@ -1,0 +1,243 @@
+/*
+ * moe_int4.h -- C ABI of the weight-only INT4 MoE expert-MLP library for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (pages: "The Throughput Lever: Quantifying the MoE GEMM and Mapping
+ * the Road to B300", sections "Phase 3: The INT4 Marlin MoE Throughput Lever",
+ * "Building the Benchmark" and "The Result: Two Regimes"):
+ *
+ *   for every token t and routing slot j with expert e = topk_ids[t, j]:
+ *     g = W_gate[e] x_t,  u = W_up[e] x_t          (gate/up grouped GEMM)
+ *     a = SiLU(g) * u                              (SwiGLU, fused in the epilogue)
+ *     y = W_down[e] a                              (down grouped GEMM)
+ *     out[t] = sum_j topk_weights[t, j] * y        (top-k weighted combine)
+ *
+ * with INT4 weights in groups of 32 along the reduction axis, each weight
+ * value = (q - 8) * scale, q in {0..15}, scale bf16 ("Building the Benchmark":
+ * INT4, group size 32).  Activations and outputs are bf16; the kernels multiply
+ * in bf16 on the tensor cores and accumulate in fp32.
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller, except those of
+ *    moe_int4_forward_host (host pointers, documented there).  The library never
+ *    frees or keeps caller memory past the call's stream work.
+ *  - Every call is stream-ordered and asynchronous on `stream` (a cudaStream_t;
+ *    NULL is the legacy default stream); none synchronises the host, except
+ *    moe_int4_get_errors, which reads back a few bytes, and moe_int4_forward_host,
+ *    which waits for its result.  No call allocates device memory.
+ *  - bf16 values are passed as their 16-bit patterns (uint16_t).
+ *  - Return value: MOE_OK (0) or a negative MOE_ERR_* code detected on the host
+ *    before anything is launched.  Bad data found on the device (an expert id
+ *    outside [0, E)) does not trap: the routing pair is dropped, and a flag and
+ *    a count are recorded in the workspace (moe_int4_get_errors).
+ */
+#ifndef MOE_INT4_H
+#define MOE_INT4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_NULL = -1,        /* a required pointer is NULL */
+    MOE_ERR_SHAPE = -2,       /* unsupported or inconsistent sizes */
+    MOE_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+    MOE_ERR_WORKSPACE = -4,   /* workspace too small */
+    MOE_ERR_CUDA = -5,        /* a CUDA runtime call failed (launch, copy) */
+    MOE_ERR_UNSUPPORTED = -6  /* current device is not compute capability 10.3 */
+};
+
+/* Device-side error flags (bit set), read with moe_int4_get_errors. */
+#define MOE_DEVERR_BAD_EXPERT_ID 0x1u /* a topk_ids entry outside [0, E) was dropped */
+#define MOE_DEVERR_TIMEOUT 0x2u       /* a pipeline wait gave up (kernel bug guard) */
+
+/* Output element types (moe_int4_shape.out_dtype). */
+#define MOE_OUT_BF16 0 /* bf16, rounded to nearest even from the fp32 combine */
+#define MOE_OUT_F32 1  /* the fp32 combine itself */
+
+/* Layer shape.  Supported: 1 <= E <= 1024, 1 <= top_k <= min(E, 32),
+ * hidden % 128 == 0, inter % 128 == 0, group == 32. */
+typedef struct {
+    int32_t E;         /* number of experts */
+    int32_t top_k;     /* routing slots per token */
+    int32_t hidden;    /* H: model width (K of the gate/up GEMM, N of the down GEMM) */
+    int32_t inter;     /* I: expert intermediate width */
+    int32_t group;     /* quantisation group along K; must be 32 */
+    int32_t out_dtype; /* MOE_OUT_BF16 or MOE_OUT_F32 */
+} moe_int4_shape;
+
+/* ------------------------------------------------------------------------- */
+/* Weight packing (offline, once per weight set; "Building the Benchmark":     */
+/* the pages repack GPTQ-format INT4 into the kernel's layout before timing)   */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of the packed INT4 buffer for E matrices of N rows x K columns:
+ * E*N*K/2 (same size as the canonical input). */
+size_t moe_int4_packed_bytes(int E, int N, int K);
+/* Bytes of the packed scale buffer: E*N*(K/32)*2. */
+size_t moe_int4_packed_scale_bytes(int E, int N, int K);
+
+/*
+ * moe_int4_pack: canonical INT4 weights -> device layout of the GEMM kernels.
+ *
+ * In:  q       uint8 [E][N][K/2]; element k of a row is in byte k/2, low nibble
+ *              for even k, high nibble for odd k; value = (q - 8) * scale.
+ *      scales  bf16 bits [E][N][K/32]; one scale per 32 consecutive k.
+ *      is_w13  1: the gate/up matrix, N = 2*inter (rows [0,inter) gate,
+ *              [inter, 2*inter) up), K = hidden.  0: the down matrix, N = hidden,
+ *              K = inter.
+ * Out: packed (moe_int4_packed_bytes) and packed_scales
+ *      (moe_int4_packed_scale_bytes), caller-allocated, 16-byte aligned.
+ *
+ * Packed layout (a "slab" is 128 rows x 64 k; a "stage" is two slabs):
+ *   w13: stage (e, r, kb) for row tile r in [0, inter/128) and k block kb in
+ *        [0, hidden/64): slab 0 = gate rows 128r..128r+127, slab 1 = up rows
+ *        inter+128r.., both for k in [64kb, 64kb+64).
+ *   w2:  stage (e, r, ks) for r in [0, hidden/128), ks in [0, inter/128):
+ *        slab 0 = rows 128r.. for k block 2ks, slab 1 = same rows, k block 2ks+1.
+ *   Stages are stored in order e, r, then k (8192 bytes each).  Inside a slab,
+ *   byte offset h*2048 + row*16 + w*4 holds word v = 4h + w of the row; bits
+ *   4s..4s+3 of word v hold q at k = 8v + 2s and bits 16+4s..16+4s+3 hold q at
+ *   k = 8v + 2s + 1 (s = 0..3), k relative to the slab's k block.
+ *   Scales: per stage 1024 bytes, [slab][row][2] bf16, groups 2kb and 2kb+1 of
+ *   the slab's k block.
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE (N or K not multiples as above),
+ *   MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ */
+int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
+                  int is_w13, void *packed, void *packed_scales, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Align: bucket routing pairs by expert and pad each bucket to block_m       */
+/* ("The Result: Two Regimes": each token's top-8 experts are gathered into    */
+/* per-expert groups for the grouped GEMM)                                     */
+/* ------------------------------------------------------------------------- */
+
+/* Capacity (entries) that sorted_ids needs: M*top_k + min(E, M*top_k)*(block_m-1).
+ * expert_ids needs capacity/block_m entries. */
+size_t moe_align_capacity(int M, int top_k, int E, int block_m);
+/* Device scratch bytes moe_align needs (0 when M*top_k <= 4096). */
+size_t moe_align_scratch_bytes(int M, int top_k, int E);
+
+/*
+ * moe_align: stable counting sort of the P = M*top_k routing pairs by expert.
+ * In:  topk_ids int32 [M][top_k].
+ * Out: sorted_ids int32: for each expert e = 0..E-1 in order, the flat pair
+ *        indices t*top_k+j routed to e in ascending order, then pad entries equal
+ *        to P up to the next multiple of block_m (experts with no pair take no
+ *        space).  Entries past num_post_pad are not written.
+ *      expert_ids int32: the expert of each block of block_m entries.
+ *      num_post_pad int32 [1]: total entries written.
+ *      Pairs whose id is outside [0, E) are dropped and flagged (needs
+ *      err_flags, may be NULL to skip the flag: uint32 [2] = flags, count).
+ * block_m: 1..256.  scratch: moe_align_scratch_bytes bytes (NULL if 0).
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ */
+int moe_align(const int32_t *topk_ids, int M, int top_k, int E, int block_m,
+              int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+              uint32_t *err_flags, void *scratch, size_t scratch_bytes,
+              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Forward                                                                    */
+/* ------------------------------------------------------------------------- */
+
+/* Workspace flag: also reserve room for the host-IO staging of
+ * moe_int4_forward_host. */
+#define MOE_WS_HOST_IO 0x1
+
+/* Workspace bytes for a forward of M tokens (0 < M <= 1<<20). */
+size_t moe_int4_workspace_bytes(int M, const moe_int4_shape *shape, int flags);
+
+/* The routing block height the forward uses for M tokens (16..192). */
+int moe_int4_block_m(int M, const moe_int4_shape *shape);
+
+/*
+ * moe_int4_workspace_layout: byte offsets inside the workspace of a forward of
+ * M tokens, for inspecting a finished call: offsets[0] error words (uint32 flags,
+ * uint32 dropped count), [1] num_post_pad (int32), [2] sorted_ids (int32,
+ * moe_align contract with block_m = moe_int4_block_m), [3] expert_ids (int32),
+ * [4] the bf16 SwiGLU intermediate [row][inter] indexed by position in
+ * sorted_ids (rows of pad entries are undefined), [5] the fp32 [M][hidden]
+ * combine accumulator of a bf16-output forward (unused for fp32 output).
+ * Returns MOE_OK or MOE_ERR_SHAPE / MOE_ERR_NULL.
+ */
+int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offsets);
+
+/*
+ * moe_int4_forward: out = the MoE expert MLP of x (see the top of this file).
+ * In:  x             bf16 [M][hidden]
+ *      w13_packed    moe_int4_pack(is_w13=1) output, w13_scales its scales
+ *      w2_packed     moe_int4_pack(is_w13=0) output, w2_scales its scales
+ *      topk_ids      int32 [M][top_k]
+ *      topk_weights  fp32 [M][top_k], used as given
+ * Out: out           [M][hidden] of shape->out_dtype (bf16 bits or fp32),
+ *                    overwritten (tokens whose pairs were all dropped get 0).
+ * workspace: >= moe_int4_workspace_bytes(M, shape, 0) bytes of device memory,
+ *   16-byte aligned; no initial contents are required.  It holds the align
+ *   buffers, the bf16 intermediate, fp32 accumulators and the error words; two
+ *   calls in flight at once must not share it.
+ * M == 0 returns MOE_OK without touching out.  Every pointer must be 16-byte
+ * aligned.  The call launches only kernels (no host sync, no allocation).
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,
+ *   MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ */
+int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_scales,
+                     const void *w2_packed, const void *w2_scales,
+                     const int32_t *topk_ids, const float *topk_weights,
+                     void *out, int M, const moe_int4_shape *shape,
+                     void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_int4_forward_host: the same layer with x, topk_ids, topk_weights and out
+ * in HOST memory (pinned memory makes the copies asynchronous).  The inputs are
+ * copied into the workspace's staging area, the forward runs on `stream`, the
+ * output is copied back, and the call waits for the stream before returning.
+ * Weights and workspace are device memory as for moe_int4_forward; the
+ * workspace must be >= moe_int4_workspace_bytes(M, shape, MOE_WS_HOST_IO).
+ */
+int moe_int4_forward_host(const uint16_t *x_host, const void *w13_packed,
+                          const void *w13_scales, const void *w2_packed,
+                          const void *w2_scales, const int32_t *topk_ids_host,
+                          const float *topk_weights_host, void *out_host, int M,
+                          const moe_int4_shape *shape, void *workspace,
+                          size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_int4_get_errors: read (synchronously on `stream`) the device error flags
+ * (MOE_DEVERR_*) and the count of dropped routing pairs accumulated in the
+ * workspace since the last moe_int4_clear_errors.  Either output may be NULL.
+ */
+int moe_int4_get_errors(const void *workspace, uint32_t *flags, uint32_t *count,
+                        moe_stream_t stream);
+/* moe_int4_clear_errors: zero the error words (stream-ordered). */
+int moe_int4_clear_errors(void *workspace, moe_stream_t stream);
+
+/* Human-readable text for a MOE_ERR_* code (static storage). */
+const char *moe_int4_strerror(int code);
+
+/*
+ * Stage timing for measurement: while enabled (on != 0), every forward records
+ * CUDA events around its align, gate/up GEMM, down GEMM and finalize launches on
+ * its stream.  moe_int4_profile_read waits for the last forward's events and
+ * writes the four stage durations in milliseconds to ms[0..3]; returns
+ * MOE_ERR_CUDA if no profiled forward has run.  Not for use during stream
+ * capture.
+ */
+int moe_int4_profile_enable(int on);
+int moe_int4_profile_read(float *ms);
+
+/* Number of kernel launches the last moe_int4_forward made on this thread. */
+int moe_int4_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_INT4_H */

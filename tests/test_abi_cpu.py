@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every declared entry point; host
+logic that needs no GPU (sizes, policy, argument checks) behaves as declared."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from weight_only_int4_moe_gb300 import ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_int4.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(moe_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("moe_int4_pack", "moe_align", "moe_int4_forward"):
+        assert required in names
+    assert set(names) == set(ops.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ops.load_library()
+    assert os.path.exists(ops.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_sizes_and_policy():
+    assert ops.moe_int4_packed_bytes(384, 4096, 7168) == 384 * 4096 * 3584
+    assert ops.moe_int4_packed_scale_bytes(384, 4096, 7168) == 384 * 4096 * 224 * 2
+    # the pages' ~8.5 GB per layer for 384 experts (int4 bytes only)
+    gb = (ops.moe_int4_packed_bytes(384, 4096, 7168) + ops.moe_int4_packed_bytes(384, 7168, 2048)) / 1e9
+    assert abs(gb - 8.456) < 0.01
+    assert ops.moe_align_capacity(1, 8, 384, 16) == 8 + 8 * 15
+    assert ops.moe_align_capacity(10, 8, 4, 16) == 80 + 4 * 15
+    sh = ops.Shape.of(384, 8, 7168, 2048)
+    assert ops.moe_int4_block_m(1, sh) == 16
+    assert ops.moe_int4_block_m(8192, sh) == 192
+    for M in (1, 9, 90, 256, 1024, 8192):
+        bm = ops.moe_int4_block_m(M, sh)
+        assert 16 <= bm <= 192 and bm % 16 == 0
+        assert ops.moe_int4_workspace_bytes(M, sh, 0) > M * 7168 * 4
+        assert ops.moe_int4_workspace_bytes(M, sh, ops.MOE_WS_HOST_IO) > ops.moe_int4_workspace_bytes(M, sh, 0)
+    assert ops.moe_align_scratch_bytes(512, 8, 384) == 0
+    assert ops.moe_align_scratch_bytes(8192, 8, 384) == 64 * 384 * 4
+
+
+def test_bad_out_dtype_rejected():
+    lib = ops.load_library()
+    sh = ops.Shape(8, 2, 256, 128, 32, 7)
+    assert lib.moe_int4_workspace_bytes(4, ctypes.byref(sh), 0) == 0
+
+
+def test_fp32_output_needs_no_accumulator_workspace():
+    f = ops.moe_int4_workspace_bytes(4096, ops.Shape.of(64, 6, 4096, 1408, ops.MOE_OUT_F32))
+    b = ops.moe_int4_workspace_bytes(4096, ops.Shape.of(64, 6, 4096, 1408, ops.MOE_OUT_BF16))
+    assert b - f >= 4096 * 4096 * 4
+
+
+@pytest.mark.parametrize("E,k,H,I,grp", [(0, 1, 128, 128, 32), (8, 9, 128, 128, 32),
+                                         (8, 2, 192, 128, 32), (8, 2, 128, 64, 32),
+                                         (8, 2, 128, 128, 64), (2000, 2, 128, 128, 32)])
+def test_bad_shapes_rejected_on_host(E, k, H, I, grp):
+    lib = ops.load_library()
+    sh = ops.Shape(E, k, H, I, grp, 0)
+    assert lib.moe_int4_workspace_bytes(4, ctypes.byref(sh), 0) == 0
+    one = ctypes.c_void_p(16)
+    rc = lib.moe_int4_forward(one, one, one, one, one, one, one, one, 4, ctypes.byref(sh), one,
+                              1 << 30, None)
+    assert rc == -2  # MOE_ERR_SHAPE
+
+
+def test_null_and_alignment_rejected_on_host():
+    lib = ops.load_library()
+    sh = ops.Shape.of(8, 2, 256, 128)
+    good = ctypes.c_void_p(1 << 20)
+    rc = lib.moe_int4_forward(None, good, good, good, good, good, good, good, 4, ctypes.byref(sh),
+                              good, 1 << 30, None)
+    assert rc == -1
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    rc = lib.moe_int4_forward(good, good, good, good, good, good, good, bad, 4, ctypes.byref(sh),
+                              good, 1 << 30, None)
+    assert rc == -3
+    rc = lib.moe_int4_forward(good, good, good, good, good, good, good, good, 4, ctypes.byref(sh),
+                              good, 16, None)
+    assert rc == -4
+    # M == 0 is a no-op that touches nothing
+    rc = lib.moe_int4_forward(None, None, None, None, None, None, None, None, 0, ctypes.byref(sh),
+                              None, 0, None)
+    assert rc == 0
+    assert lib.moe_int4_pack(None, good, 1, 256, 64, 1, good, good, None) == -1
+    assert lib.moe_int4_pack(good, good, 1, 128, 64, 1, good, good, None) == -2
+    assert lib.moe_int4_pack(good, good, 1, 128, 64, 0, good, good, None) == -2
+    assert ops.moe_int4_strerror(-4) == "workspace too small"

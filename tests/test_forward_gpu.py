@@ -1,0 +1,252 @@
+"""moe_int4_forward on the GPU against the oracle, element by element, at sizes
+the oracle finishes in seconds (several tiles, ragged tails, every block-height
+regime), plus the invariants and edge cases of the layer."""
+import numpy as np
+import pytest
+
+import oracle
+from weight_only_int4_moe_gb300 import inputs
+from helpers import assert_parity, gpu_forward, parity, to_device_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def _ops():
+    from weight_only_int4_moe_gb300 import ops
+    return ops
+
+
+_cache = {}
+
+
+def setup(E, k, H, I, M, seed, routing="uniform"):
+    key = (E, H, I, seed)
+    ops = _ops()
+    if key not in _cache:
+        w = inputs.make_weights(E, H, I, 500 + seed)
+        _cache[key] = (w, ops.PackedWeights(w, E, H, I, k))
+    w, pw = _cache[key]
+    pw.shape.top_k = k
+    cfg = inputs.MoEConfig("t", E, k, H, I, (M,), routing, 0, 700 + seed)
+    t = inputs.make_tokens(cfg, M)
+    return w, pw, t
+
+
+def oracle_out(w, t, tokens=None):
+    out, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
+                                t["topk_weights"], tokens=tokens)
+    return out
+
+
+SMALL = [
+    # E, k, H, I, M, seed  (block heights 16..192, single- and multi-block align)
+    (8, 2, 256, 128, 16, 0),      # the tiny workload's shape
+    (8, 2, 256, 128, 1, 1),
+    (16, 4, 384, 256, 37, 2),     # ragged M, 2 gate/up tiles, 3 down tiles
+    (4, 1, 256, 128, 300, 3),     # ~75 tokens per expert
+    (8, 2, 512, 256, 1000, 4),    # ~250 tokens per expert -> block 192, 2 blocks
+    (64, 6, 512, 256, 700, 5),    # P = 4200 -> multi-block align
+    (32, 8, 1024, 384, 5, 6),     # many k stages per tile, stream-K splits
+]
+
+
+@pytest.mark.parametrize("E,k,H,I,M,seed", SMALL)
+def test_forward_matches_oracle(E, k, H, I, M, seed):
+    w, pw, t = setup(E, k, H, I, M, seed)
+    got = gpu_forward(pw, t)
+    ref = oracle_out(w, t)
+    m = assert_parity(got, ref, f"E{E} k{k} H{H} I{I} M{M}")
+    print(m)
+
+
+def test_tiny_workload_seed():
+    cfg = inputs.CONFIGS[0]
+    w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
+    pw = _ops().PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k)
+    t = inputs.make_tokens(cfg, 16)
+    assert_parity(gpu_forward(pw, t), oracle_out(w, t), "tiny")
+
+
+def test_skewed_routing_small():
+    w, pw, t = setup(64, 8, 512, 256, 256, 7, routing="skewed")
+    assert_parity(gpu_forward(pw, t), oracle_out(w, t), "skewed")
+
+
+def test_all_tokens_one_expert():
+    w, pw, t = setup(8, 2, 256, 128, 200, 8)
+    t = dict(t)
+    t["topk_ids"] = np.tile(np.array([[3, 5]], dtype=np.int32), (200, 1))
+    assert_parity(gpu_forward(pw, t), oracle_out(w, t), "one expert")
+
+
+def test_duplicate_expert_in_slots():
+    w, pw, t = setup(8, 2, 256, 128, 16, 9)
+    t = dict(t)
+    ids = t["topk_ids"].copy()
+    ids[:, 1] = ids[:, 0]
+    t["topk_ids"] = ids
+    assert_parity(gpu_forward(pw, t), oracle_out(w, t), "duplicates")
+
+
+def test_top1_weight1():
+    w, pw, t = setup(8, 1, 256, 128, 33, 10)
+    t = dict(t, topk_weights=np.ones((33, 1), dtype=np.float32))
+    assert_parity(gpu_forward(pw, t), oracle_out(w, t), "top1")
+
+
+def test_invalid_ids_dropped_and_reported():
+    import torch
+    ops = _ops()
+    w, pw, t = setup(8, 2, 256, 128, 16, 11)
+    t = dict(t)
+    ids = t["topk_ids"].copy()
+    ids[2, 0] = 8
+    ids[7, 1] = -3
+    t["topk_ids"] = ids
+    ws = ops.alloc_workspace(16, pw.shape)
+    got = gpu_forward(pw, t, workspace=ws)
+    assert_parity(got, oracle_out(w, t), "invalid ids")
+    flags, count = ops.moe_int4_get_errors(ws)
+    assert flags == ops.MOE_DEVERR_BAD_EXPERT_ID and count == 2
+    # a clean call clears the report
+    t2 = dict(t, topk_ids=np.abs(t["topk_ids"]) % 8)
+    gpu_forward(pw, t2, workspace=ws)
+    assert ops.moe_int4_get_errors(ws) == (0, 0)
+
+
+def test_unrouted_experts_cannot_change_output():
+    import torch
+    ops = _ops()
+    E, k, H, I, M = 16, 2, 256, 128, 24
+    w, pw, t = setup(E, k, H, I, M, 12)
+    base = gpu_forward(pw, t)
+    used = set(np.unique(t["topk_ids"]).tolist())
+    rng = np.random.default_rng(3)
+    w2 = {kk: v.copy() for kk, v in w.items()}
+    for e in range(E):
+        if e not in used:
+            for kk in w2:
+                w2[kk][e] = rng.integers(0, 1 << (8 if kk[0] == "q" else 16), w2[kk][e].shape)
+    pw2 = ops.PackedWeights(w2, E, H, I, k)
+    again = gpu_forward(pw2, t)
+    # identical up to the order of fp32 atomic additions (at most one bf16 ulp)
+    ulp = np.abs(base) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(again - base) <= ulp)
+    assert np.mean(again == base) > 0.99
+
+
+def test_zero_input_gives_zero():
+    w, pw, t = setup(8, 2, 256, 128, 16, 13)
+    t = dict(t, x=np.zeros_like(t["x"]))
+    assert not gpu_forward(pw, t).any()
+
+
+def test_m_zero_is_noop():
+    import torch
+    ops = _ops()
+    w, pw, t = setup(8, 2, 256, 128, 16, 14)
+    x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((0, 2), dtype=torch.int32, device="cuda")
+    tw = torch.zeros((0, 2), dtype=torch.float32, device="cuda")
+    out = torch.full((1, 256), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    lib = ops.load_library()
+    import ctypes
+    rc = lib.moe_int4_forward(x.data_ptr(), pw.w13.data_ptr(), pw.w13_scales.data_ptr(),
+                              pw.w2.data_ptr(), pw.w2_scales.data_ptr(), ids.data_ptr(),
+                              tw.data_ptr(), out.data_ptr(), 0, ctypes.byref(pw.shape),
+                              ws.data_ptr(), 256, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert (out.float() == 7.0).all()
+
+
+def test_repeated_calls_and_workspace_reuse():
+    ops = _ops()
+    w, pw, t = setup(16, 4, 384, 256, 37, 15)
+    ws = ops.alloc_workspace(37, pw.shape)
+    ref = oracle_out(w, t)
+    for _ in range(3):
+        assert_parity(gpu_forward(pw, t, workspace=ws), ref, "reuse")
+
+
+def test_forward_host_buffers():
+    import torch
+    ops = _ops()
+    w, pw, t = setup(16, 4, 384, 256, 37, 16)
+    ws = ops.alloc_workspace(37, pw.shape, flags=ops.MOE_WS_HOST_IO)
+    x = torch.from_numpy(t["x"].view(np.int16)).pin_memory()
+    ids = torch.from_numpy(t["topk_ids"]).pin_memory()
+    tw = torch.from_numpy(t["topk_weights"]).pin_memory()
+    out = torch.empty((37, 384), dtype=torch.float32).pin_memory()
+    ops.moe_int4_forward_host(x, pw.w13, pw.w13_scales, pw.w2, pw.w2_scales, ids, tw, out,
+                              pw.shape, ws)
+    got = out.numpy()
+    assert_parity(got, oracle_out(w, t), "host io")
+
+
+def test_no_timeout_flag_on_normal_runs():
+    ops = _ops()
+    w, pw, t = setup(32, 8, 1024, 384, 5, 6)
+    ws = ops.alloc_workspace(5, pw.shape)
+    gpu_forward(pw, t, workspace=ws)
+    flags, _ = ops.moe_int4_get_errors(ws)
+    assert not (flags & ops.MOE_DEVERR_TIMEOUT)
+
+
+@pytest.mark.parametrize("E,k,H,I,M,seed", [(16, 4, 384, 256, 37, 2), (64, 6, 512, 256, 700, 5),
+                                            (8, 2, 512, 256, 1000, 4)])
+def test_internal_align_and_intermediate(E, k, H, I, M, seed):
+    """The forward's own align buffers are bit-exact, and the gate/up GEMM's
+    SwiGLU output matches the oracle's intermediate before the down GEMM."""
+    import torch
+    ops = _ops()
+    w, pw, t = setup(E, k, H, I, M, seed)
+    ws = ops.alloc_workspace(M, pw.shape)
+    gpu_forward(pw, t, workspace=ws)
+    lay = ops.moe_int4_workspace_layout(M, pw.shape)
+    BM = ops.moe_int4_block_m(M, pw.shape)
+    raw = ws.cpu().numpy()
+    npp = int(raw[lay["num_post_pad"]:lay["num_post_pad"] + 4].view(np.int32)[0])
+    rs, re_, rn, _ = oracle.align(t["topk_ids"], E, BM)
+    assert npp == rn
+    got_sorted = raw[lay["sorted_ids"]:lay["sorted_ids"] + 4 * npp].view(np.int32)
+    np.testing.assert_array_equal(got_sorted, rs)
+    got_exp = raw[lay["expert_ids"]:lay["expert_ids"] + 4 * (npp // BM)].view(np.int32)
+    np.testing.assert_array_equal(got_exp, re_)
+    a_bits = raw[lay["intermediate"]:lay["intermediate"] + 2 * npp * I].view(np.uint16)
+    a = inputs.f32_from_bf16_bits(a_bits).reshape(npp, I)
+    real = np.nonzero(rs < M * k)[0]
+    pick = real[:: max(1, len(real) // 64)]
+    ref = oracle.moe_intermediate(t["x"], w["q13"], w["s13"], t["topk_ids"], rs[pick])
+    # the intermediate is stored in bf16: allow its own rounding (half an ulp)
+    # on top of the accumulated error
+    m = parity(a[pick], ref)
+    assert m["rel_l1"] <= 5e-3, m
+    slack = np.abs(a[pick] - ref) - 2.0 ** -8 * np.abs(ref)
+    assert slack.max() <= 2e-2 * m["rms"], (slack.max(), m)
+
+
+def test_bf16_output_is_rounded_fp32_output():
+    """The bf16 output is the fp32 combine rounded to nearest even (up to the
+    order of fp32 atomic additions)."""
+    import torch
+    ops = _ops()
+    w, pw, t = setup(16, 4, 384, 256, 37, 17)
+    f32 = gpu_forward(pw, t)
+    pw_b = ops.PackedWeights(w, 16, 384, 256, 4, out_dtype=ops.MOE_OUT_BF16)
+    x, ids, tw = to_device_tokens(t)
+    ws = ops.alloc_workspace(37, pw_b.shape)
+    ob = pw_b.forward(x, ids, tw, workspace=ws)
+    torch.cuda.synchronize()
+    assert ob.dtype == torch.bfloat16
+    got = ob.float().cpu().numpy()
+    want = inputs.f32_from_bf16_bits(inputs.bf16_bits_from_f32(f32))
+    ulp = np.abs(want) * 2.0 ** -7
+    assert np.all(np.abs(got - want) <= ulp)
+    assert np.mean(got == want) > 0.98
+    ref = oracle_out(w, t)
+    m = parity(got, ref)
+    assert m["rel_l1"] <= 5e-3
+    # beyond the fp32 result's error, only the final rounding (half an ulp)
+    assert np.all(np.abs(got - ref) <= 2e-2 * m["rms"] + 2.0 ** -8 * np.abs(ref))

@@ -1,0 +1,475 @@
+// Host side of the C ABI declared in include/moe_int4.h: argument checks,
+// workspace planning, the launch sequence of a forward (align -> gate/up GEMM ->
+// down GEMM -> finalize), tensor-map encoding, error read-back and stage timing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_int4.h"
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxGrid = 160;          // persistent GEMM grid cap (GB300: 152 SMs)
+constexpr int kSingleBlockAlignMax = 4096;
+constexpr int kAlignChunk = 1024;
+
+thread_local int g_last_launches = 0;
+
+inline size_t rup(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_shape(const moe_int4_shape *sh) {
+    if (!sh) return MOE_ERR_NULL;
+    if (sh->E < 1 || sh->E > 1024) return MOE_ERR_SHAPE;
+    if (sh->top_k < 1 || sh->top_k > sh->E || sh->top_k > 32) return MOE_ERR_SHAPE;
+    if (sh->hidden < 128 || sh->hidden % 128) return MOE_ERR_SHAPE;
+    if (sh->inter < 128 || sh->inter % 128) return MOE_ERR_SHAPE;
+    if (sh->group != 32) return MOE_ERR_SHAPE;
+    if (sh->out_dtype != MOE_OUT_BF16 && sh->out_dtype != MOE_OUT_F32) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
+int choose_block_m(long long P, int E) {
+    const long long touched = P < E ? P : E;
+    const double avg = touched > 0 ? (double)P / (double)touched : 1.0;
+    int bm = (int)(avg * 1.25 + 8.0);
+    bm = (bm + 15) / 16 * 16;
+    if (bm < 16) bm = 16;
+    if (bm > 192) bm = 192;
+    return bm;
+}
+
+struct Plan {
+    int M, E, k, H, I, P, BM, RT1, RT2, n_chunks, out_f32;
+    size_t cap, blocks_cap, tiles1_cap;
+    size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_cnt, off_partial, off_a,
+        off_acc, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
+};
+
+Plan make_plan(int M, const moe_int4_shape *sh) {
+    Plan p{};
+    p.M = M;
+    p.E = sh->E;
+    p.k = sh->top_k;
+    p.H = sh->hidden;
+    p.I = sh->inter;
+    p.P = M * sh->top_k;
+    p.out_f32 = sh->out_dtype == MOE_OUT_F32;
+    p.BM = choose_block_m(p.P, p.E);
+    p.RT1 = p.I / 128;
+    p.RT2 = p.H / 128;
+    p.n_chunks = p.P > kSingleBlockAlignMax ? (p.P + kAlignChunk - 1) / kAlignChunk : 0;
+    const size_t touched = (size_t)(p.P < p.E ? p.P : p.E);
+    p.cap = (size_t)p.P + touched * (size_t)(p.BM - 1);
+    p.blocks_cap = p.cap / p.BM + 1;
+    p.tiles1_cap = p.blocks_cap * p.RT1;
+    size_t o = 0;
+    p.off_err = o; o += 256;
+    p.off_npp = o; o += 256;
+    p.off_sorted = o; o = rup(o + p.cap * 4, 256);
+    p.off_expert = o; o = rup(o + p.blocks_cap * 4, 256);
+    p.off_chunk = o; o = rup(o + (size_t)p.n_chunks * p.E * 4, 256);
+    p.off_cnt = o; o = rup(o + p.tiles1_cap * 4, 256);
+    p.off_partial = o; o = rup(o + (size_t)kMaxGrid * 4 * p.BM * 128 * 4, 256);
+    p.off_a = o; o = rup(o + p.cap * (size_t)p.I * 2, 256);
+    p.off_acc = o; o = rup(o + (p.out_f32 ? 0 : (size_t)p.M * p.H * 4), 256);
+    p.total = o;
+    p.off_io_x = o; o = rup(o + (size_t)p.M * p.H * 2, 256);
+    p.off_io_ids = o; o = rup(o + (size_t)p.P * 4, 256);
+    p.off_io_w = o; o = rup(o + (size_t)p.P * 4, 256);
+    p.off_io_out = o; o = rup(o + (size_t)p.M * p.H * (p.out_f32 ? 4 : 2), 256);
+    p.total_io = o;
+    return p;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int ok = -1;  // -1 unknown, 0 unsupported, 1 sm_103
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+int device_info(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (d.ok < 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        d.ok = (major == 10 && minor == 3) ? 1 : 0;
+    }
+    if (!d.ok) return MOE_ERR_UNSUPPORTED;
+    *sms = d.sms;
+    return MOE_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map over the bf16 intermediate [rows][I], box = 64 columns x BM rows,
+// 128-byte swizzle (the MMA's K-major B layout).
+bool encode_intermediate_map(CUtensorMap *m, void *a, size_t rows, int I, int BM) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)I * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)BM};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- profiling --
+struct Profiler {
+    bool on = false;
+    bool recorded = false;
+    int dev = -1;
+    cudaEvent_t ev[5] = {};
+};
+Profiler g_prof;
+
+void prof_record(int i, cudaStream_t s) {
+    if (g_prof.on && g_prof.ev[i]) cudaEventRecord(g_prof.ev[i], s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_int4_packed_bytes(int E, int N, int K) {
+    if (E <= 0 || N <= 0 || K <= 0) return 0;
+    return (size_t)E * N * (size_t)(K / 2);
+}
+
+size_t moe_int4_packed_scale_bytes(int E, int N, int K) {
+    if (E <= 0 || N <= 0 || K <= 0) return 0;
+    return (size_t)E * N * (size_t)(K / 32) * 2;
+}
+
+int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K, int is_w13,
+                  void *packed, void *packed_scales, moe_stream_t stream) {
+    if (!q || !scales || !packed || !packed_scales) return MOE_ERR_NULL;
+    if (E < 1 || N < 1 || K < 1) return MOE_ERR_SHAPE;
+    if (is_w13) {
+        if (N % 256 || K % 64) return MOE_ERR_SHAPE;
+    } else {
+        if (N % 128 || K % 128) return MOE_ERR_SHAPE;
+    }
+    if (!aligned16(q) || !aligned16(scales) || !aligned16(packed) || !aligned16(packed_scales))
+        return MOE_ERR_ALIGN;
+    cudaError_t e = launch_pack(q, scales, E, N, K, is_w13, packed, packed_scales,
+                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_align_capacity(int M, int top_k, int E, int block_m) {
+    if (M < 0 || top_k < 1 || E < 1 || block_m < 1) return 0;
+    const long long P = (long long)M * top_k;
+    const long long touched = P < E ? P : E;
+    return (size_t)(P + touched * (block_m - 1));
+}
+
+size_t moe_align_scratch_bytes(int M, int top_k, int E) {
+    if (M < 0 || top_k < 1 || E < 1) return 0;
+    const long long P = (long long)M * top_k;
+    if (P <= kSingleBlockAlignMax) return 0;
+    return (size_t)((P + kAlignChunk - 1) / kAlignChunk) * E * 4;
+}
+
+int moe_align(const int32_t *topk_ids, int M, int top_k, int E, int block_m,
+              int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+              uint32_t *err_flags, void *scratch, size_t scratch_bytes, moe_stream_t stream) {
+    if (M < 0 || top_k < 1 || top_k > 32 || E < 1 || E > 1024 || block_m < 1 || block_m > 256)
+        return MOE_ERR_SHAPE;
+    if ((long long)M * top_k > (1LL << 30)) return MOE_ERR_SHAPE;
+    if (!num_post_pad || (M > 0 && (!topk_ids || !sorted_ids || !expert_ids)))
+        return MOE_ERR_NULL;
+    const size_t need = moe_align_scratch_bytes(M, top_k, E);
+    if (need && (!scratch || scratch_bytes < need)) return MOE_ERR_WORKSPACE;
+    AlignArgs a{};
+    a.ids = topk_ids;
+    a.P = M * top_k;
+    a.E = E;
+    a.block_m = block_m;
+    a.sorted_ids = sorted_ids;
+    a.expert_ids = expert_ids;
+    a.num_post_pad = num_post_pad;
+    a.err = err_flags;
+    a.chunk_tab = reinterpret_cast<int32_t *>(scratch);
+    a.n_chunks = need ? (a.P + kAlignChunk - 1) / kAlignChunk : 0;
+    ZeroArgs z{};
+    cudaError_t e = launch_align(a, z, 0, reinterpret_cast<cudaStream_t>(stream), nullptr);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_int4_workspace_bytes(int M, const moe_int4_shape *shape, int flags) {
+    if (check_shape(shape) != MOE_OK || M < 0 || M > (1 << 20)) return 0;
+    if (M == 0) return 256;
+    Plan p = make_plan(M, shape);
+    return (flags & MOE_WS_HOST_IO) ? p.total_io : p.total;
+}
+
+int moe_int4_block_m(int M, const moe_int4_shape *shape) {
+    if (check_shape(shape) != MOE_OK || M < 0) return 0;
+    return choose_block_m((long long)M * shape->top_k, shape->E);
+}
+
+int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offsets) {
+    if (!offsets) return MOE_ERR_NULL;
+    const int rc = check_shape(shape);
+    if (rc != MOE_OK) return rc;
+    if (M < 1 || M > (1 << 20)) return MOE_ERR_SHAPE;
+    const Plan p = make_plan(M, shape);
+    offsets[0] = p.off_err;
+    offsets[1] = p.off_npp;
+    offsets[2] = p.off_sorted;
+    offsets[3] = p.off_expert;
+    offsets[4] = p.off_a;
+    offsets[5] = p.off_acc;
+    return MOE_OK;
+}
+
+int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_scales,
+                     const void *w2_packed, const void *w2_scales, const int32_t *topk_ids,
+                     const float *topk_weights, void *out, int M,
+                     const moe_int4_shape *shape, void *workspace, size_t workspace_bytes,
+                     moe_stream_t stream) {
+    g_last_launches = 0;
+    int rc = check_shape(shape);
+    if (rc != MOE_OK) return rc;
+    if (M < 0 || M > (1 << 20)) return MOE_ERR_SHAPE;
+    if (M == 0) return MOE_OK;
+    if (!x || !w13_packed || !w13_scales || !w2_packed || !w2_scales || !topk_ids ||
+        !topk_weights || !out || !workspace)
+        return MOE_ERR_NULL;
+    const void *ptrs[] = {x, w13_packed, w13_scales, w2_packed, w2_scales, topk_ids,
+                          topk_weights, out, workspace};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return MOE_ERR_ALIGN;
+    const Plan pl = make_plan(M, shape);
+    if (workspace_bytes < pl.total) return MOE_ERR_WORKSPACE;
+    int sms = 0;
+    rc = device_info(&sms);
+    if (rc != MOE_OK) return rc;
+    const int grid = sms < kMaxGrid ? sms : kMaxGrid;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    int launches = 0;
+
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + pl.off_err);
+    int32_t *npp = reinterpret_cast<int32_t *>(ws + pl.off_npp);
+    int32_t *sorted = reinterpret_cast<int32_t *>(ws + pl.off_sorted);
+    int32_t *expert = reinterpret_cast<int32_t *>(ws + pl.off_expert);
+    uint16_t *a_buf = reinterpret_cast<uint16_t *>(ws + pl.off_a);
+    // fp32 output: the down GEMM accumulates straight into `out`
+    float *acc = pl.out_f32 ? reinterpret_cast<float *>(out)
+                            : reinterpret_cast<float *>(ws + pl.off_acc);
+
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_prof.on) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            if (g_prof.dev != dev) {
+                for (auto &e : g_prof.ev)
+                    if (e) cudaEventDestroy(e), e = nullptr;
+                for (auto &e : g_prof.ev) cudaEventCreate(&e);
+                g_prof.dev = dev;
+            }
+            g_prof.recorded = true;
+        }
+    }
+    prof_record(0, s);
+
+    AlignArgs al{};
+    al.ids = topk_ids;
+    al.P = pl.P;
+    al.E = pl.E;
+    al.block_m = pl.BM;
+    al.sorted_ids = sorted;
+    al.expert_ids = expert;
+    al.num_post_pad = npp;
+    al.err = err;
+    al.chunk_tab = reinterpret_cast<int32_t *>(ws + pl.off_chunk);
+    al.n_chunks = pl.n_chunks;
+    ZeroArgs z{};
+    z.ptr[0] = ws + pl.off_cnt;
+    z.n16[0] = (pl.tiles1_cap * 4 + 15) / 16;
+    z.ptr[1] = acc;
+    z.n16[1] = (size_t)pl.M * pl.H * 4 / 16;
+    const size_t zero_bytes = (z.n16[0] + z.n16[1]) * 16;
+    int zero_ctas = (int)(zero_bytes / (64 * 1024));
+    if (zero_ctas < 1) zero_ctas = 1;
+    if (zero_ctas > 2 * sms) zero_ctas = 2 * sms;
+    if (launch_align(al, z, zero_ctas, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+    prof_record(1, s);
+
+    GemmParams g{};
+    g.sorted_ids = sorted;
+    g.expert_ids = expert;
+    g.num_post_pad = npp;
+    g.topk_weights = topk_weights;
+    g.err = err;
+    g.M = pl.M;
+    g.top_k = pl.k;
+    g.H = pl.H;
+    g.I = pl.I;
+    g.P = pl.P;
+    g.block_m = pl.BM;
+    g.split = 1;
+
+    GemmParams g1 = g;
+    g1.wq = reinterpret_cast<const uint8_t *>(w13_packed);
+    g1.wsc = reinterpret_cast<const uint8_t *>(w13_scales);
+    g1.x = x;
+    g1.a_out = a_buf;
+    g1.partial = reinterpret_cast<float *>(ws + pl.off_partial);
+    g1.tile_cnt = reinterpret_cast<int32_t *>(ws + pl.off_cnt);
+    g1.RT = pl.RT1;
+    g1.KS = pl.H / 64;
+    if (!plan_gemm_smem(1, g1)) return MOE_ERR_SHAPE;
+    CUtensorMap dummy;
+    memset(&dummy, 0, sizeof dummy);
+    if (launch_gemm(1, g1, &dummy, grid, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+    prof_record(2, s);
+
+    GemmParams g2 = g;
+    g2.wq = reinterpret_cast<const uint8_t *>(w2_packed);
+    g2.wsc = reinterpret_cast<const uint8_t *>(w2_scales);
+    g2.out_acc = acc;
+    g2.RT = pl.RT2;
+    g2.KS = pl.I / 128;
+    if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
+    CUtensorMap tmap;
+    if (!encode_intermediate_map(&tmap, a_buf, pl.cap, pl.I, pl.BM)) return MOE_ERR_CUDA;
+    if (launch_gemm(2, g2, &tmap, grid, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+    prof_record(3, s);
+
+    if (!pl.out_f32 && launch_finalize(acc, reinterpret_cast<uint16_t *>(out),
+                                       (size_t)pl.M * pl.H, sms, s, &launches) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    prof_record(4, s);
+    g_last_launches = launches;
+    return MOE_OK;
+}
+
+int moe_int4_forward_host(const uint16_t *x_host, const void *w13_packed,
+                          const void *w13_scales, const void *w2_packed, const void *w2_scales,
+                          const int32_t *topk_ids_host, const float *topk_weights_host,
+                          void *out_host, int M, const moe_int4_shape *shape,
+                          void *workspace, size_t workspace_bytes, moe_stream_t stream) {
+    int rc = check_shape(shape);
+    if (rc != MOE_OK) return rc;
+    if (M < 0 || M > (1 << 20)) return MOE_ERR_SHAPE;
+    if (M == 0) return MOE_OK;
+    if (!x_host || !topk_ids_host || !topk_weights_host || !out_host || !workspace)
+        return MOE_ERR_NULL;
+    const Plan pl = make_plan(M, shape);
+    if (workspace_bytes < pl.total_io) return MOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MOE_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    uint16_t *dx = reinterpret_cast<uint16_t *>(ws + pl.off_io_x);
+    int32_t *dids = reinterpret_cast<int32_t *>(ws + pl.off_io_ids);
+    float *dw = reinterpret_cast<float *>(ws + pl.off_io_w);
+    void *dout = ws + pl.off_io_out;
+    const size_t out_bytes = (size_t)M * pl.H * (pl.out_f32 ? 4 : 2);
+    if (cudaMemcpyAsync(dx, x_host, (size_t)M * pl.H * 2, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(dids, topk_ids_host, (size_t)pl.P * 4, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(dw, topk_weights_host, (size_t)pl.P * 4, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    rc = moe_int4_forward(dx, w13_packed, w13_scales, w2_packed, w2_scales, dids, dw, dout, M,
+                          shape, workspace, pl.total, stream);
+    if (rc != MOE_OK) return rc;
+    if (cudaMemcpyAsync(out_host, dout, out_bytes, cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_int4_get_errors(const void *workspace, uint32_t *flags, uint32_t *count,
+                        moe_stream_t stream) {
+    if (!workspace) return MOE_ERR_NULL;
+    uint32_t h[2] = {0, 0};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(h, workspace, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (flags) *flags = h[0];
+    if (count) *count = h[1];
+    return MOE_OK;
+}
+
+int moe_int4_clear_errors(void *workspace, moe_stream_t stream) {
+    if (!workspace) return MOE_ERR_NULL;
+    return cudaMemsetAsync(workspace, 0, 8, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
+
+const char *moe_int4_strerror(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULL: return "a required pointer is NULL";
+        case MOE_ERR_SHAPE: return "unsupported or inconsistent sizes";
+        case MOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "a CUDA runtime call failed";
+        case MOE_ERR_UNSUPPORTED: return "device is not compute capability 10.3 (sm_103a)";
+        default: return "unknown error code";
+    }
+}
+
+int moe_int4_profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_prof.on = on != 0;
+    g_prof.recorded = false;
+    return MOE_OK;
+}
+
+int moe_int4_profile_read(float *ms) {
+    if (!ms) return MOE_ERR_NULL;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_prof.recorded || !g_prof.ev[4]) return MOE_ERR_CUDA;
+    if (cudaEventSynchronize(g_prof.ev[4]) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int i = 0; i < 4; ++i)
+        if (cudaEventElapsedTime(&ms[i], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_int4_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

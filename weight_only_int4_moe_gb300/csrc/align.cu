@@ -1,0 +1,254 @@
+// Align (bucket routing pairs by expert, pad buckets to the block height), the
+// per-call zeroing of accumulators, and the final fp32 -> bf16 conversion.
+//
+// The align step turns the routed token batch into per-expert groups for the
+// grouped GEMMs ("The Throughput Lever", section "The Result: Two Regimes": each
+// token activates top-8 of the experts and the kernel works expert by expert).
+// Output contract: for each expert in ascending order, the flat pair indices
+// t*top_k+j routed to it in ascending order, then pad entries (value P) up to a
+// multiple of block_m; one expert id per block; the total count.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+// Exclusive prefix sum over one value per thread of a 1024-thread block.
+// `warp_tot` is shared scratch of 32 ints.  Returns the exclusive prefix and
+// writes the block total to *total (all threads).
+__device__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += n;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int t = warp_tot[lane];
+        int ti = t;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, ti, d);
+            if (lane >= d) ti += n;
+        }
+        warp_tot[lane] = ti - t;  // exclusive prefix of warp totals
+        if (lane == 31) warp_tot[32] = ti;
+    }
+    __syncthreads();
+    int res = warp_tot[wid] + incl - v;
+    *total = warp_tot[32];
+    __syncthreads();
+    return res;
+}
+
+// Given per-expert counts cnt[0..E) (shared), compute padded bucket offsets
+// into off[0..E) (shared), write expert_ids, pad entries, num_post_pad and the
+// error words.  One 1024-thread block; E <= 1024.
+__device__ void align_layout(const AlignArgs &a, const int *cnt, int *off, int *scan_tmp) {
+    const int e = threadIdx.x;
+    const int c = (e < a.E) ? cnt[e] : 0;
+    const int pc = ((c + a.block_m - 1) / a.block_m) * a.block_m;
+    int total = 0;
+    const int o = block_exclusive_scan(pc, scan_tmp, &total);
+    int valid_total = 0;
+    block_exclusive_scan(c, scan_tmp, &valid_total);
+    if (e < a.E) {
+        off[e] = o;
+        for (int b = o / a.block_m; b < (o + pc) / a.block_m; ++b) a.expert_ids[b] = e;
+        for (int p = o + c; p < o + pc; ++p) a.sorted_ids[p] = a.P;
+    }
+    if (threadIdx.x == 0) {
+        *a.num_post_pad = total;
+        if (a.err) {
+            const uint32_t dropped = (uint32_t)(a.P - valid_total);
+            a.err[0] = dropped ? kErrBadExpert : 0u;
+            a.err[1] = dropped;
+        }
+    }
+}
+
+// Place the pairs of items [i0, i0 + 1024) using per-expert running bases
+// base[e] (shared, advanced on return).  wtab: shared [32][E] ints.
+__device__ void align_place_round(const AlignArgs &a, int i0, int *base, int *wtab) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int idx = threadIdx.x; idx < kAlignWarps * a.E; idx += kAlignThreads) wtab[idx] = 0;
+    __syncthreads();
+    const int i = i0 + threadIdx.x;
+    const int e = (i < a.P) ? a.ids[i] : -1;
+    const bool valid = (e >= 0) && (e < a.E);
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) wtab[wid * a.E + e] = __popc(peers);
+    __syncthreads();
+    for (int ee = threadIdx.x; ee < a.E; ee += kAlignThreads) {
+        int acc = base[ee];
+        for (int w = 0; w < kAlignWarps; ++w) {
+            const int t = wtab[w * a.E + ee];
+            wtab[w * a.E + ee] = acc;
+            acc += t;
+        }
+        base[ee] = acc;
+    }
+    __syncthreads();
+    if (valid) a.sorted_ids[wtab[wid * a.E + e] + rank] = i;
+    __syncthreads();
+}
+
+__device__ void zero_regions(const ZeroArgs &z, int cta, int nctas) {
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < 2; ++r) {
+        float4 *p = reinterpret_cast<float4 *>(z.ptr[r]);
+        const size_t n = z.n16[r];
+        for (size_t idx = (size_t)cta * blockDim.x + threadIdx.x; idx < n;
+             idx += (size_t)nctas * blockDim.x)
+            p[idx] = zero;
+    }
+}
+
+// Whole align in one block (P small); blocks 1.. zero the accumulators.
+__global__ void __launch_bounds__(kAlignThreads)
+    align_fused_kernel(const AlignArgs a, const ZeroArgs z) {
+    extern __shared__ int sm[];
+    if (blockIdx.x > 0) {
+        zero_regions(z, blockIdx.x - 1, gridDim.x - 1);
+        return;
+    }
+    int *cnt = sm;                    // [E]
+    int *base = cnt + a.E;            // [E]
+    int *scan_tmp = base + a.E;       // [33]
+    int *wtab = scan_tmp + 64;        // [32][E]
+    for (int e = threadIdx.x; e < a.E; e += kAlignThreads) cnt[e] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.P; i += kAlignThreads) {
+        const int e = a.ids[i];
+        if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    align_layout(a, cnt, base, scan_tmp);
+    __syncthreads();
+    for (int i0 = 0; i0 < a.P; i0 += kAlignThreads) align_place_round(a, i0, base, wtab);
+}
+
+// Multi-block align, step 1: per-chunk histograms; extra blocks zero.
+__global__ void __launch_bounds__(kAlignThreads)
+    align_hist_kernel(const AlignArgs a, const ZeroArgs z) {
+    extern __shared__ int sm[];
+    if ((int)blockIdx.x < a.n_chunks) {
+        int *cnt = sm;
+        for (int e = threadIdx.x; e < a.E; e += kAlignThreads) cnt[e] = 0;
+        __syncthreads();
+        const int i = blockIdx.x * kAlignThreads + threadIdx.x;
+        if (i < a.P) {
+            const int e = a.ids[i];
+            if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < a.E; e += kAlignThreads)
+            a.chunk_tab[(size_t)blockIdx.x * a.E + e] = cnt[e];
+    }
+    zero_regions(z, blockIdx.x, gridDim.x);
+}
+
+// Step 2 (one block): bucket offsets, expert ids, pads; turns chunk_tab into
+// per-chunk starting positions.
+__global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(const AlignArgs a) {
+    extern __shared__ int sm[];
+    int *cnt = sm;
+    int *off = cnt + a.E;
+    int *scan_tmp = off + a.E;
+    for (int e = threadIdx.x; e < a.E; e += kAlignThreads) {
+        int s = 0;
+        for (int c = 0; c < a.n_chunks; ++c) s += a.chunk_tab[(size_t)c * a.E + e];
+        cnt[e] = s;
+    }
+    __syncthreads();
+    align_layout(a, cnt, off, scan_tmp);
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += kAlignThreads) {
+        int run = off[e];
+        for (int c = 0; c < a.n_chunks; ++c) {
+            const int t = a.chunk_tab[(size_t)c * a.E + e];
+            a.chunk_tab[(size_t)c * a.E + e] = run;
+            run += t;
+        }
+    }
+}
+
+// Step 3: each block places its chunk.
+__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const AlignArgs a) {
+    extern __shared__ int sm[];
+    int *base = sm;            // [E]
+    int *wtab = base + a.E;    // [32][E]
+    for (int e = threadIdx.x; e < a.E; e += kAlignThreads)
+        base[e] = a.chunk_tab[(size_t)blockIdx.x * a.E + e];
+    __syncthreads();
+    align_place_round(a, blockIdx.x * kAlignThreads, base, wtab);
+}
+
+// out[i] = bf16(acc[i]) (round to nearest even), 8 elements per step.
+__global__ void finalize_kernel(const float *__restrict__ acc, uint16_t *__restrict__ out,
+                                size_t n8) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a0 = reinterpret_cast<const float4 *>(acc)[2 * i];
+        const float4 a1 = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(a0.x, a0.y);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(a0.z, a0.w);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(a1.x, a1.y);
+        __nv_bfloat162 b3 = __floats2bfloat162_rn(a1.z, a1.w);
+        uint4 v;
+        v.x = *reinterpret_cast<uint32_t *>(&b0);
+        v.y = *reinterpret_cast<uint32_t *>(&b1);
+        v.z = *reinterpret_cast<uint32_t *>(&b2);
+        v.w = *reinterpret_cast<uint32_t *>(&b3);
+        reinterpret_cast<uint4 *>(out)[i] = v;
+    }
+}
+
+size_t align_smem_fused(int E) { return (size_t)(2 * E + 64 + kAlignWarps * E) * sizeof(int); }
+size_t align_smem_scan(int E) { return (size_t)(2 * E + 64) * sizeof(int); }
+size_t align_smem_scatter(int E) { return (size_t)(E + kAlignWarps * E) * sizeof(int); }
+
+cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas,
+                         cudaStream_t s, int *launches) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        const int maxs = (int)align_smem_fused(1024);
+        cudaFuncSetAttribute(align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+        cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+        cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+        cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+        attr_done[dev] = true;
+    }
+    if (a.n_chunks <= 0) {
+        align_fused_kernel<<<1 + zero_ctas, kAlignThreads, align_smem_fused(a.E), s>>>(a, z);
+        if (launches) *launches += 1;
+    } else {
+        align_hist_kernel<<<a.n_chunks + zero_ctas, kAlignThreads, (size_t)a.E * sizeof(int), s>>>(a, z);
+        align_scan_kernel<<<1, kAlignThreads, align_smem_scan(a.E), s>>>(a);
+        align_scatter_kernel<<<a.n_chunks, kAlignThreads, align_smem_scatter(a.E), s>>>(a);
+        if (launches) *launches += 3;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, cudaStream_t s,
+                            int *launches) {
+    const size_t n8 = n / 8;
+    size_t blocks = (n8 + 255) / 256;
+    if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
+    if (blocks < 1) blocks = 1;
+    finalize_kernel<<<(unsigned)blocks, 256, 0, s>>>(acc, out, n8);
+    if (launches) *launches += 1;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,71 @@
+// Internal interface between the kernel translation units and the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct AlignArgs {
+    const int32_t *ids;    // [P]
+    int P, E, block_m;
+    int32_t *sorted_ids;   // [capacity]
+    int32_t *expert_ids;   // [capacity / block_m]
+    int32_t *num_post_pad; // [1]
+    uint32_t *err;         // [2] or null
+    int32_t *chunk_tab;    // [n_chunks][E] (multi-block path)
+    int n_chunks;          // 0: single-block path
+};
+
+struct ZeroArgs {
+    void *ptr[2];
+    size_t n16[2];  // 16-byte units
+};
+
+cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas, cudaStream_t s,
+                         int *launches);
+cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, cudaStream_t s,
+                            int *launches);
+cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
+                        int is_w13, void *packed, void *packed_scales, cudaStream_t s);
+
+// Packed weight geometry shared by the pack kernel and the GEMMs.
+constexpr int kSlabRows = 128;
+constexpr int kSlabK = 64;
+constexpr int kSlabBytes = kSlabRows * kSlabK / 2;      // 4096
+constexpr int kStageWBytes = 2 * kSlabBytes;            // 8192
+constexpr int kStageSBytes = 2 * kSlabRows * 2 * 2;     // 1024
+constexpr int kStageBytes = kStageWBytes + kStageSBytes;  // 9216
+
+struct GemmParams {
+    const uint8_t *wq;         // packed INT4 stages
+    const uint8_t *wsc;        // packed scales
+    const uint16_t *x;         // gate/up: activations [M][H]
+    const int32_t *sorted_ids; // align output
+    const int32_t *expert_ids;
+    const int32_t *num_post_pad;
+    const float *topk_weights; // down: [P]
+    uint16_t *a_out;           // gate/up output, intermediate [rows][I]
+    float *partial;            // gate/up split slots [G][2][2][BM][128]
+    int32_t *tile_cnt;         // gate/up split counters [tiles]
+    float *out_acc;            // down: fp32 accumulator [M][H]
+    uint32_t *err;             // [2]
+    int M, top_k, H, I, P;
+    int block_m;               // BM: routing block height (multiple of 16, <= 192)
+    int RT, KS;                // row tiles per expert, k stages per tile
+    int n_w, n_b, n_a;         // ring depths: weight stages, B stages, A (TMEM) stages
+    int split;                 // 1: partition k iterations evenly over CTAs
+    uint32_t b_stage_bytes;
+    uint32_t smem_b_off, smem_misc_off, smem_bytes;
+};
+
+// kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine.
+cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_a, int grid,
+                        cudaStream_t s, int *launches);
+// Fills the ring depths and shared-memory layout of p for the given kind.
+bool plan_gemm_smem(int kind, GemmParams &p);
+
+}  // namespace moe

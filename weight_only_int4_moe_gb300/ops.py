@@ -1,0 +1,288 @@
+"""Thin Python binding of the C ABI in ``include/moe_int4.h``.
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+PyTorch provides device memory and the current CUDA stream.  If the library is
+missing and cannot be built, or the device is not an sm_103 GPU, calls raise --
+there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_WS_HOST_IO = 0x1
+MOE_OUT_BF16 = 0
+MOE_OUT_F32 = 1
+MOE_DEVERR_BAD_EXPERT_ID = 0x1
+MOE_DEVERR_TIMEOUT = 0x2
+
+EXPORTED = [
+    "moe_int4_packed_bytes", "moe_int4_packed_scale_bytes", "moe_int4_pack",
+    "moe_align_capacity", "moe_align_scratch_bytes", "moe_align",
+    "moe_int4_workspace_bytes", "moe_int4_block_m", "moe_int4_workspace_layout",
+    "moe_int4_forward",
+    "moe_int4_forward_host", "moe_int4_get_errors", "moe_int4_clear_errors",
+    "moe_int4_strerror", "moe_int4_profile_enable", "moe_int4_profile_read",
+    "moe_int4_last_launch_count",
+]
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("inter", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32)]
+
+    @classmethod
+    def of(cls, E, top_k, hidden, inter, out_dtype=MOE_OUT_F32):
+        return cls(E, top_k, hidden, inter, 32, out_dtype)
+
+    @property
+    def torch_out_dtype(self):
+        return torch.float32 if self.out_dtype == MOE_OUT_F32 else torch.bfloat16
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Load (building first if needed) the CUDA library and declare signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB
+        lib = ctypes.CDLL(path)
+        p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sp = ctypes.POINTER(Shape)
+        sig = {
+            "moe_int4_packed_bytes": ([i, i, i], sz),
+            "moe_int4_packed_scale_bytes": ([i, i, i], sz),
+            "moe_int4_pack": ([p, p, i, i, i, i, p, p, p], i),
+            "moe_align_capacity": ([i, i, i, i], sz),
+            "moe_align_scratch_bytes": ([i, i, i], sz),
+            "moe_align": ([p, i, i, i, i, p, p, p, p, p, sz, p], i),
+            "moe_int4_workspace_bytes": ([i, sp, i], sz),
+            "moe_int4_block_m": ([i, sp], i),
+            "moe_int4_workspace_layout": ([i, sp, p], i),
+            "moe_int4_forward": ([p] * 8 + [i, sp, p, sz, p], i),
+            "moe_int4_forward_host": ([p] * 8 + [i, sp, p, sz, p], i),
+            "moe_int4_get_errors": ([p, p, p, p], i),
+            "moe_int4_clear_errors": ([p, p], i),
+            "moe_int4_strerror": ([i], ctypes.c_char_p),
+            "moe_int4_profile_enable": ([i], i),
+            "moe_int4_profile_read": ([p], i),
+            "moe_int4_last_launch_count": ([], i),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        msg = load_library().moe_int4_strerror(rc).decode()
+        raise RuntimeError(f"{what} failed ({rc}): {msg}")
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dptr(t: torch.Tensor) -> int:
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _u16(t: torch.Tensor) -> torch.Tensor:
+    """bf16 tensors are passed by bit pattern."""
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16)
+    if t.dtype in (torch.int16, torch.uint16):
+        return t
+    raise TypeError(f"expected bf16 (or its int16 bits), got {t.dtype}")
+
+
+# ----------------------------------------------------------------- packing --
+def moe_int4_packed_bytes(E: int, N: int, K: int) -> int:
+    return load_library().moe_int4_packed_bytes(E, N, K)
+
+
+def moe_int4_packed_scale_bytes(E: int, N: int, K: int) -> int:
+    return load_library().moe_int4_packed_scale_bytes(E, N, K)
+
+
+def moe_int4_pack(q: torch.Tensor, scales: torch.Tensor, is_w13: bool, stream=None):
+    """Canonical INT4 (uint8 [E, N, K/2]) + bf16 scales [E, N, K/32] -> packed
+    (uint8) and packed scales (uint8) device tensors."""
+    lib = load_library()
+    E, N, K2 = q.shape
+    K = 2 * K2
+    packed = torch.empty(lib.moe_int4_packed_bytes(E, N, K), dtype=torch.uint8, device=q.device)
+    pscales = torch.empty(lib.moe_int4_packed_scale_bytes(E, N, K), dtype=torch.uint8,
+                          device=q.device)
+    rc = lib.moe_int4_pack(_dptr(q), _dptr(_u16(scales)), E, N, K, int(bool(is_w13)),
+                           _dptr(packed), _dptr(pscales), _stream(stream))
+    _check(rc, "moe_int4_pack")
+    return packed, pscales
+
+
+# ------------------------------------------------------------------- align --
+def moe_align_capacity(M: int, top_k: int, E: int, block_m: int) -> int:
+    return load_library().moe_align_capacity(M, top_k, E, block_m)
+
+
+def moe_align_scratch_bytes(M: int, top_k: int, E: int) -> int:
+    return load_library().moe_align_scratch_bytes(M, top_k, E)
+
+
+def moe_align(topk_ids: torch.Tensor, E: int, block_m: int, stream=None):
+    """Returns (sorted_ids, expert_ids, num_post_pad, err) device tensors; only
+    the first num_post_pad entries of sorted_ids are defined."""
+    lib = load_library()
+    M, k = topk_ids.shape
+    cap = max(lib.moe_align_capacity(M, k, E, block_m), 1)
+    dev = topk_ids.device
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(cap // block_m + 1, dtype=torch.int32, device=dev)
+    npp = torch.zeros(1, dtype=torch.int32, device=dev)
+    err = torch.zeros(2, dtype=torch.int32, device=dev)
+    scratch_bytes = lib.moe_align_scratch_bytes(M, k, E)
+    scratch = torch.empty(max(scratch_bytes, 16), dtype=torch.uint8, device=dev)
+    rc = lib.moe_align(_dptr(topk_ids), M, k, E, block_m, _dptr(sorted_ids), _dptr(expert_ids),
+                       _dptr(npp), _dptr(err), _dptr(scratch), scratch_bytes, _stream(stream))
+    _check(rc, "moe_align")
+    return sorted_ids, expert_ids, npp, err
+
+
+# ----------------------------------------------------------------- forward --
+def moe_int4_workspace_bytes(M: int, shape: Shape, flags: int = 0) -> int:
+    return load_library().moe_int4_workspace_bytes(M, ctypes.byref(shape), flags)
+
+
+def moe_int4_block_m(M: int, shape: Shape) -> int:
+    return load_library().moe_int4_block_m(M, ctypes.byref(shape))
+
+
+def moe_int4_workspace_layout(M: int, shape: Shape) -> dict:
+    off = (ctypes.c_size_t * 6)()
+    _check(load_library().moe_int4_workspace_layout(M, ctypes.byref(shape), off),
+           "moe_int4_workspace_layout")
+    keys = ["err", "num_post_pad", "sorted_ids", "expert_ids", "intermediate", "acc"]
+    return dict(zip(keys, list(off)))
+
+
+def alloc_workspace(M: int, shape: Shape, flags: int = 0, device="cuda") -> torch.Tensor:
+    n = moe_int4_workspace_bytes(M, shape, flags)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def moe_int4_forward(x, w13_packed, w13_scales, w2_packed, w2_scales, topk_ids, topk_weights,
+                     shape: Shape, out=None, workspace=None, stream=None):
+    """out [M, H] (fp32 or bf16 per shape.out_dtype) = the MoE expert MLP."""
+    lib = load_library()
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, shape.hidden), dtype=shape.torch_out_dtype, device=x.device)
+    if out.dtype != shape.torch_out_dtype:
+        raise TypeError(f"out must be {shape.torch_out_dtype}")
+    if workspace is None:
+        workspace = alloc_workspace(M, shape, device=x.device)
+    rc = lib.moe_int4_forward(
+        _dptr(_u16(x)), _dptr(w13_packed), _dptr(w13_scales), _dptr(w2_packed),
+        _dptr(w2_scales), _dptr(topk_ids), _dptr(topk_weights), _dptr(out), M,
+        ctypes.byref(shape), _dptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "moe_int4_forward")
+    return out
+
+
+def moe_int4_forward_host(x_host, w13_packed, w13_scales, w2_packed, w2_scales, ids_host,
+                          weights_host, out_host, shape: Shape, workspace, stream=None):
+    """Host-buffer variant: x/ids/weights/out are CPU tensors (pinned for async
+    copies); the call returns once out_host holds the result."""
+    lib = load_library()
+    for t in (x_host, ids_host, weights_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+    M = x_host.shape[0]
+    rc = lib.moe_int4_forward_host(
+        _u16(x_host).data_ptr(), _dptr(w13_packed), _dptr(w13_scales), _dptr(w2_packed),
+        _dptr(w2_scales), ids_host.data_ptr(), weights_host.data_ptr(),
+        out_host.data_ptr(), M, ctypes.byref(shape), _dptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check(rc, "moe_int4_forward_host")
+    return out_host
+
+
+def moe_int4_get_errors(workspace, stream=None):
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    count = ctypes.c_uint32(0)
+    rc = lib.moe_int4_get_errors(_dptr(workspace), ctypes.byref(flags), ctypes.byref(count),
+                                 _stream(stream))
+    _check(rc, "moe_int4_get_errors")
+    return flags.value, count.value
+
+
+def moe_int4_clear_errors(workspace, stream=None):
+    _check(load_library().moe_int4_clear_errors(_dptr(workspace), _stream(stream)),
+           "moe_int4_clear_errors")
+
+
+def moe_int4_strerror(code: int) -> str:
+    return load_library().moe_int4_strerror(code).decode()
+
+
+def moe_int4_profile_enable(on: bool):
+    _check(load_library().moe_int4_profile_enable(int(bool(on))), "moe_int4_profile_enable")
+
+
+def moe_int4_profile_read():
+    ms = (ctypes.c_float * 4)()
+    _check(load_library().moe_int4_profile_read(ms), "moe_int4_profile_read")
+    return list(ms)
+
+
+def moe_int4_last_launch_count() -> int:
+    return load_library().moe_int4_last_launch_count()
+
+
+# --------------------------------------------------------------- helpers --
+class PackedWeights:
+    """Device copies of one weight set in the kernels' packed layout."""
+
+    def __init__(self, w: dict, E: int, H: int, I: int, top_k: int, device="cuda",
+                 keep_canonical: bool = False, out_dtype: int = MOE_OUT_F32):
+        self.shape = Shape.of(E, top_k, H, I, out_dtype)
+        q13 = torch.from_numpy(np.ascontiguousarray(w["q13"])).to(device)
+        s13 = torch.from_numpy(np.ascontiguousarray(w["s13"]).view(np.int16)).to(device)
+        self.w13, self.w13_scales = moe_int4_pack(q13, s13, True)
+        if not keep_canonical:
+            del q13, s13
+        q2 = torch.from_numpy(np.ascontiguousarray(w["q2"])).to(device)
+        s2 = torch.from_numpy(np.ascontiguousarray(w["s2"]).view(np.int16)).to(device)
+        self.w2, self.w2_scales = moe_int4_pack(q2, s2, False)
+        torch.cuda.synchronize()
+
+    def forward(self, x, topk_ids, topk_weights, out=None, workspace=None, stream=None):
+        return moe_int4_forward(x, self.w13, self.w13_scales, self.w2, self.w2_scales, topk_ids,
+                                topk_weights, self.shape, out=out, workspace=workspace,
+                                stream=stream)
