@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of the weight-only INT4 MoE expert MLP on GB300.
+
+One step = one moe_int4_forward per token count M of the workload's sweep
+(default: the K2.6-shaped decode workload, 384 experts, top-8, hidden 7168,
+intermediate 2048, M in {1, 9, 90}).  Weights are resident in HBM; every call
+gets a routing from a rotating pool and an L2 flush (a 512 MB device write)
+runs before it, outside its timed interval.  Times are CUDA events on the
+launching stream.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle on
+the host cores instead (bounded samples of the same workload).  Under torchrun
+each rank runs an independent replica on its own GPU (the layer does not shard).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from weight_only_int4_moe_gb300 import inputs  # noqa: E402
+
+METRIC = ("fused INT4 MoE µs/call & tokens/s vs M; HBM GB/s and tensor-pipe % of "
+          "roofline")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--ms", type=str, default=None, help="comma-separated token counts")
+    ap.add_argument("--pool", type=int, default=8, help="routings per M")
+    ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def expert_bytes(H, I):
+    w13 = 2 * I * H // 2 + 2 * I * (H // 32) * 2
+    w2 = H * I // 2 + H * (I // 32) * 2
+    return w13, w2
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled=True):
+        self.index = index
+        self.proc = None
+        self.path = None
+        self.enabled = enabled
+
+    def start(self):
+        if not self.enabled:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[1]) for r in rows]
+        smax = max(num(r[2]) for r in rows)
+        power = [num(r[3]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "sm_mhz_min": min(sm), "power_w_max": max(power), "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------- distributed --
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, local, use_gpu):
+    if world <= 1:
+        return None
+    import torch
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    if use_gpu:
+        torch.cuda.set_device(local)
+    dist.init_process_group("nccl" if use_gpu else "gloo")
+    return dist
+
+
+def barrier(dist, use_gpu):
+    if dist is None:
+        return
+    if use_gpu:
+        import torch
+        dist.barrier(device_ids=[torch.cuda.current_device()])
+    else:
+        dist.barrier()
+
+
+def allreduce_max(dist, value, use_gpu):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if use_gpu else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle --
+def time_oracle(w, cfg, Ms, target_s, threads, state=None):
+    """Times the oracle on a bounded sample: rounds of `threads` tokens (one per
+    thread) taken in turn from the largest call of the sweep, until about
+    target_s seconds have passed.  Returns (tokens, seconds, M sampled)."""
+    import oracle
+    oracle.build()
+    M = max(Ms)
+    t = inputs.make_tokens(cfg, M)
+    state = state if state is not None else {"next": 0}
+    toks_done, t_total, rounds = 0, 0.0, 0
+    while rounds == 0 or (t_total < target_s and rounds < 100):
+        n = min(threads, M)
+        tk = np.array(sorted({(state["next"] + j) % M for j in range(n)}))
+        state["next"] = (state["next"] + n) % M
+        t0 = time.perf_counter()
+        oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
+                           t["topk_weights"], tokens=tk, threads=threads)
+        t_total += time.perf_counter() - t0
+        toks_done += len(tk)
+        rounds += 1
+    return toks_done, t_total, M
+
+
+def run_reference(args, cfg, Ms, world, rank):
+    if rank != 0:
+        return
+    threads = host_threads()
+    w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
+    per_step_s = max(0.5, args.cpu_seconds / max(1, args.steps))
+    state = {"next": 0}
+    for _ in range(args.warmup):
+        time_oracle(w, cfg, Ms, 0.0, threads, state)
+    toks, secs = 0, 0.0
+    step_ms = []
+    for _ in range(args.steps):
+        n, s, Msamp = time_oracle(w, cfg, Ms, per_step_s, threads, state)
+        toks += n
+        secs += s
+        step_ms.append(s * 1e3)
+    value = toks / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(step_ms), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "E": cfg.E, "top_k": cfg.top_k, "hidden": cfg.H,
+                   "inter": cfg.I, "Ms": list(Ms)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{toks} tokens of the M={Msamp} call ({args.steps} "
+                                   f"steps of rounds of {threads} tokens), fp64 oracle, "
+                                   f"{threads} threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm --
+def run_ours(args, cfg, Ms, world, rank, local):
+    import torch
+    from weight_only_int4_moe_gb300 import ops
+
+    dist = dist_init(world, local, True)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    out_dtype = ops.MOE_OUT_F32 if args.out_dtype == "f32" else ops.MOE_OUT_BF16
+
+    w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
+    pw = ops.PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k, device=dev, out_dtype=out_dtype)
+    shape = pw.shape
+    Mmax = max(Ms)
+    ws = ops.alloc_workspace(Mmax, shape, device=dev)
+    ws_bytes_max = max(ops.moe_int4_workspace_bytes(M, shape) for M in Ms)
+    if ws.numel() < ws_bytes_max:
+        ws = torch.empty(ws_bytes_max, dtype=torch.uint8, device=dev)
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+    w13_b, w2_b = expert_bytes(cfg.H, cfg.I)
+
+    data = {}
+    for M in Ms:
+        t = inputs.make_tokens(cfg, M)
+        pool = [(t["topk_ids"], t["topk_weights"])] + inputs.routing_pool(cfg, M, args.pool - 1)
+        x = torch.from_numpy(t["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+        routes = []
+        for ids, tw in pool:
+            n = len(inputs.touched_experts(ids, cfg.E))
+            routes.append((torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev), n))
+        out = torch.empty((M, cfg.H), dtype=shape.torch_out_dtype, device=dev)
+        data[M] = {"x": x, "routes": routes, "out": out, "host": t, "pool": pool}
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def one_call(M, r, rec):
+        d = data[M]
+        ids, tw, n_touched = d["routes"][r % len(d["routes"])]
+        flush.zero_()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        ops.moe_int4_forward(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales, ids, tw,
+                             shape, out=d["out"], workspace=ws, stream=stream)
+        ev1.record(stream)
+        launches = ops.moe_int4_last_launch_count()
+        if rec is not None:
+            stages = ops.moe_int4_profile_read()  # waits for this call's events
+            ev1.synchronize()
+            rec.append({"M": M, "ms": ev0.elapsed_time(ev1), "stages": stages,
+                        "touched": n_touched, "launches": launches})
+
+    # warm-up
+    for s in range(args.warmup):
+        for M in Ms:
+            one_call(M, s, None)
+    torch.cuda.synchronize()
+
+    # timed region
+    ops.moe_int4_profile_enable(True)
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    barrier(dist, True)
+    torch.cuda.synchronize()
+    clocks.start()
+    rec = []
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        for M in Ms:
+            one_call(M, args.warmup + s, rec)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(dist, True)
+    clk = clocks.stop()
+    ops.moe_int4_profile_enable(False)
+
+    ms_per_step = sum(r["ms"] for r in rec) / args.steps
+    ms_per_step_max = allreduce_max(dist, ms_per_step, True)
+    tokens_per_step = sum(Ms)
+    value = world * tokens_per_step / (ms_per_step_max / 1e3)
+
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    per_m = {}
+    for M in Ms:
+        rs = [r for r in rec if r["M"] == M]
+        us = [r["ms"] * 1e3 for r in rs]
+        touched = statistics.mean(r["touched"] for r in rs)
+        bytes_w = touched * (w13_b + w2_b)
+        flops = 2.0 * M * cfg.top_k * 3 * cfg.H * cfg.I
+        t_med = statistics.median(us)
+        t_hbm = bytes_w / (hbm_peak * 1e9) * 1e6
+        t_tc = flops / (tc_peak * 1e12) * 1e6
+        st = np.mean([r["stages"] for r in rs], axis=0)
+        per_m[str(M)] = {
+            "us_per_call": t_med, "us_mean": statistics.mean(us),
+            "tokens_per_s": M / (t_med / 1e6),
+            "touched_experts": touched,
+            "weight_bytes": bytes_w,
+            "hbm_gbs": bytes_w / (t_med / 1e6) / 1e9,
+            "frac_hbm": bytes_w / (t_med / 1e6) / 1e9 / hbm_peak,
+            "tflops": flops / (t_med / 1e6) / 1e12,
+            "frac_tensor": flops / (t_med / 1e6) / 1e12 / tc_peak,
+            "ideal_us": {"hbm": t_hbm, "tensor": t_tc},
+            "roofline_frac": max(t_hbm, t_tc) / t_med,
+            "stage_us": {"align": st[0] * 1e3, "gate_up": st[1] * 1e3, "down": st[2] * 1e3,
+                         "finalize": st[3] * 1e3},
+        }
+
+    # dominant kernel: the gate/up GEMM (largest stage share); algorithmic bytes
+    # = touched experts x (w13 int4 + scales) per launch
+    g1_ms = [r["stages"][1] for r in rec]
+    g1_bytes = [r["touched"] * w13_b for r in rec]
+    g2_ms = [r["stages"][2] for r in rec]
+    dominant = "gate_up" if sum(g1_ms) >= sum(g2_ms) else "down"
+    if dominant == "gate_up":
+        ach = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
+    else:
+        ach = sum(r["touched"] * w2_b for r in rec) / (sum(g2_ms) / 1e3) / 1e9
+    traffic = None
+    prof_json = os.path.join(ROOT, "profiles", f"{dominant}_{cfg.name}_traffic.json")
+    if os.path.exists(prof_json):
+        with open(prof_json) as f:
+            traffic = json.load(f).get("traffic_bytes_per_launch")
+    roofline = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                "frac": ach / hbm_peak, "traffic": traffic, "kernel": dominant,
+                "peak_source": f"{peak_src} (hbm_gbs)",
+                "bytes_per_launch_mean": statistics.mean(
+                    g1_bytes if dominant == "gate_up" else [r["touched"] * w2_b for r in rec]),
+                "launch_ms_mean": statistics.mean(g1_ms if dominant == "gate_up" else g2_ms)}
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        ws_io = ops.alloc_workspace(Mmax, shape, flags=ops.MOE_WS_HOST_IO, device=dev)
+        hosts = {}
+        h2d = d2h = 0
+        for M in Ms:
+            t = data[M]["host"]
+            hx = torch.from_numpy(t["x"].view(np.int16)).pin_memory()
+            hids = torch.from_numpy(t["topk_ids"]).pin_memory()
+            htw = torch.from_numpy(t["topk_weights"]).pin_memory()
+            hout = torch.empty((M, cfg.H), dtype=shape.torch_out_dtype).pin_memory()
+            hosts[M] = (hx, hids, htw, hout)
+            h2d += hx.numel() * 2 + hids.numel() * 4 + htw.numel() * 4
+            d2h += hout.numel() * hout.element_size()
+        for _ in range(max(1, args.warmup)):
+            for M in Ms:
+                ops.moe_int4_forward_host(hosts[M][0], pw.w13, pw.w13_scales, pw.w2,
+                                          pw.w2_scales, hosts[M][1], hosts[M][2], hosts[M][3],
+                                          shape, ws_io)
+        torch.cuda.synchronize()
+        e2e_s = 0.0
+        for _ in range(args.steps):
+            for M in Ms:
+                flush.zero_()
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                ops.moe_int4_forward_host(hosts[M][0], pw.w13, pw.w13_scales, pw.w2,
+                                          pw.w2_scales, hosts[M][1], hosts[M][2], hosts[M][3],
+                                          shape, ws_io)
+                e2e_s += time.perf_counter() - t0
+        e2e_step = allreduce_max(dist, e2e_s / args.steps, True)
+        e2e = {"value": world * tokens_per_step / e2e_step, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_step * 1e3}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = host_threads()
+        n, secs, Msamp = time_oracle(w, cfg, Ms, args.cpu_seconds, threads)
+        cpu = {"value": n / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} tokens of the M={Msamp} call, fp64 oracle, {threads} threads, "
+                         f"{secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "E": cfg.E, "top_k": cfg.top_k, "hidden": cfg.H,
+                       "inter": cfg.I, "group": 32, "Ms": list(Ms),
+                       "step": "one moe_int4_forward per M",
+                       "l2": f"flushed by a {args.flush_mb} MB device write before every call; "
+                             f"routing rotates over {args.pool} seeded routings per M",
+                       "out_dtype": args.out_dtype, "parallelism": f"replicas x{world}",
+                       "block_m": {str(M): ops.moe_int4_block_m(M, shape) for M in Ms}},
+            "per_m": per_m, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(sum(r["launches"] for r in rec)),
+            "clocks": clk, "wall_s_timed": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    cfg = inputs.CONFIGS[args.config]
+    Ms = tuple(int(m) for m in args.ms.split(",")) if args.ms else cfg.Ms
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, cfg, Ms, world, rank)
+        return
+    run_ours(args, cfg, Ms, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -14,8 +14,13 @@
  *
  * with INT4 weights in groups of 32 along the reduction axis, each weight
  * value = (q - 8) * scale, q in {0..15}, scale bf16 ("Building the Benchmark":
- * INT4, group size 32).  Activations and outputs are bf16; the kernels multiply
- * in bf16 on the tensor cores and accumulate in fp32.
+ * INT4, group size 32).  Activations are bf16 and the output bf16 or fp32.  The
+ * tensor cores multiply fp16 operands with fp32 accumulation: each dequantised
+ * weight (q - 8) * scale is rounded once to fp16 (11 significant bits, where
+ * bf16 would keep 8), x is converted to fp16 (exact for |x| in [2^-14, 65504];
+ * larger magnitudes saturate to +-65504, smaller ones lose precision as fp16
+ * subnormals), and the SwiGLU intermediate is stored as fp16 saturated to
+ * +-65504.
  *
  * Conventions for every entry point:
  *  - All array pointers are DEVICE pointers owned by the caller, except those of
@@ -105,8 +110,9 @@ size_t moe_int4_packed_scale_bytes(int E, int N, int K);
  *   byte offset h*2048 + row*16 + w*4 holds word v = 4h + w of the row; bits
  *   4s..4s+3 of word v hold q at k = 8v + 2s and bits 16+4s..16+4s+3 hold q at
  *   k = 8v + 2s + 1 (s = 0..3), k relative to the slab's k block.
- *   Scales: per stage 1024 bytes, [slab][row][2] bf16, groups 2kb and 2kb+1 of
- *   the slab's k block.
+ *   Scales: per stage 1024 bytes, [slab][row][2] fp16, groups 2kb and 2kb+1 of
+ *   the slab's k block; each bf16 scale is converted to fp16 (exact for
+ *   magnitudes in [2^-14, 65504], saturating above, fp16 subnormal below).
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE (N or K not multiples as above),
  *   MOE_ERR_ALIGN, MOE_ERR_CUDA.
  */
@@ -155,7 +161,7 @@ int moe_align(const int32_t *topk_ids, int M, int top_k, int E, int block_m,
 /* Workspace bytes for a forward of M tokens (0 < M <= 1<<20). */
 size_t moe_int4_workspace_bytes(int M, const moe_int4_shape *shape, int flags);
 
-/* The routing block height the forward uses for M tokens (16..192). */
+/* The routing block height the forward uses for M tokens (16..128). */
 int moe_int4_block_m(int M, const moe_int4_shape *shape);
 
 /*
@@ -163,7 +169,7 @@ int moe_int4_block_m(int M, const moe_int4_shape *shape);
  * M tokens, for inspecting a finished call: offsets[0] error words (uint32 flags,
  * uint32 dropped count), [1] num_post_pad (int32), [2] sorted_ids (int32,
  * moe_align contract with block_m = moe_int4_block_m), [3] expert_ids (int32),
- * [4] the bf16 SwiGLU intermediate [row][inter] indexed by position in
+ * [4] the fp16 SwiGLU intermediate [row][inter] indexed by position in
  * sorted_ids (rows of pad entries are undefined), [5] the fp32 [M][hidden]
  * combine accumulator of a bf16-output forward (unused for fp32 output).
  * Returns MOE_OK or MOE_ERR_SHAPE / MOE_ERR_NULL.

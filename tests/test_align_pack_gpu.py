@@ -3,6 +3,7 @@ import numpy as np
 import pytest
 
 import oracle
+from weight_only_int4_moe_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -74,7 +75,9 @@ def np_pack_reference(q, s, is_w13):
         rows0 = rows1 = lambda r: slice(128 * r, 128 * r + 128)
         ks0 = lambda kk: slice(128 * kk, 128 * kk + 64)
         ks1 = lambda kk: slice(128 * kk + 64, 128 * kk + 128)
-    sv = s.astype(np.uint32)
+    # scales are stored as fp16 (saturated to +-65504), two per 32-bit word
+    sf = np.clip(s.astype(np.uint32).__lshift__(16).view(np.float32), -65504, 65504)
+    sv = sf.astype(np.float16).view(np.uint16).astype(np.uint32)
     out_w, out_s = [], []
     for e in range(E):
         for r in range(RT):
@@ -102,7 +105,10 @@ def test_pack_matches_layout_spec(is_w13, E, N, K):
     ops = _ops()
     rng = np.random.default_rng(E * N + K + is_w13)
     q = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
-    s = rng.integers(0, 1 << 16, (E, N, K // 32), dtype=np.uint16)
+    # finite bf16 scales over a wide range, signs included, plus fp16 edge cases
+    mag = np.exp2(rng.uniform(-20, 18, (E, N, K // 32))).astype(np.float32)
+    sgn = np.where(rng.random(mag.shape) < 0.5, -1.0, 1.0).astype(np.float32)
+    s = inputs.bf16_bits_from_f32(mag * sgn)
     pw, ps = ops.moe_int4_pack(torch.from_numpy(q).cuda(),
                                torch.from_numpy(s.view(np.int16)).cuda(), bool(is_w13))
     torch.cuda.synchronize()

@@ -1,0 +1,64 @@
+"""Full-size parity: the five workloads at their real sizes, in the launch
+configuration the benchmark times (moe_int4_forward with its own plan), checked
+against the oracle on sampled tokens (the oracle computes each token's output
+one by one), plus checks that hold for every output at any size."""
+import numpy as np
+import pytest
+
+import oracle
+from weight_only_int4_moe_gb300 import inputs
+from helpers import assert_parity, gpu_forward
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+SAMPLES = 6
+
+
+def _ops():
+    from weight_only_int4_moe_gb300 import ops
+    return ops
+
+
+@pytest.fixture(scope="module")
+def k26():
+    cfg = inputs.CONFIGS[1]
+    w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
+    pw = _ops().PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k)
+    yield w, pw
+    del pw
+
+
+@pytest.fixture(scope="module")
+def mid():
+    cfg = inputs.CONFIGS[4]
+    w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
+    pw = _ops().PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k)
+    yield w, pw
+    del pw
+
+
+def _check(w, pw, cfg, M, n_samples=SAMPLES):
+    t = inputs.make_tokens(cfg, M)
+    got = gpu_forward(pw, t)
+    assert np.all(np.isfinite(got))
+    # tokens whose every slot went to experts... all tokens have k valid slots here,
+    # so no output row may be identically zero
+    assert np.all(np.abs(got).max(axis=1) > 0)
+    rng = np.random.default_rng([M, 99])
+    toks = np.sort(rng.choice(M, size=min(n_samples, M), replace=False))
+    ref, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
+                                t["topk_weights"], tokens=toks)
+    return assert_parity(got[toks], ref, f"{cfg.name} M={M}")
+
+
+@pytest.mark.parametrize("cfg_idx,M", [(1, 1), (1, 9), (1, 90), (2, 256), (2, 512), (2, 1024),
+                                       (3, 8192)])
+def test_k26_workloads(k26, cfg_idx, M):
+    w, pw = k26
+    print(_check(w, pw, inputs.CONFIGS[cfg_idx], M))
+
+
+@pytest.mark.parametrize("M", [1, 32, 128, 2048, 8192])
+def test_mid_workload(mid, M):
+    w, pw = mid
+    print(_check(w, pw, inputs.CONFIGS[4], M, n_samples=M if M <= 32 else SAMPLES))

@@ -8,7 +8,7 @@
 
 #include <mutex>
 
-#include "../../include/moe_int4.h"
+#include "moe_int4.h"
 #include "kernels.cuh"
 
 using namespace moe;
@@ -41,7 +41,7 @@ int choose_block_m(long long P, int E) {
     int bm = (int)(avg * 1.25 + 8.0);
     bm = (bm + 15) / 16 * 16;
     if (bm < 16) bm = 16;
-    if (bm > 192) bm = 192;
+    if (bm > 128) bm = 128;
     return bm;
 }
 
@@ -49,7 +49,7 @@ struct Plan {
     int M, E, k, H, I, P, BM, RT1, RT2, n_chunks, out_f32;
     size_t cap, blocks_cap, tiles1_cap;
     size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_cnt, off_partial, off_a,
-        off_acc, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
+        off_x16, off_acc, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
 };
 
 Plan make_plan(int M, const moe_int4_shape *sh) {
@@ -78,6 +78,7 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.off_cnt = o; o = rup(o + p.tiles1_cap * 4, 256);
     p.off_partial = o; o = rup(o + (size_t)kMaxGrid * 4 * p.BM * 128 * 4, 256);
     p.off_a = o; o = rup(o + p.cap * (size_t)p.I * 2, 256);
+    p.off_x16 = o; o = rup(o + (size_t)p.M * p.H * 2, 256);
     p.off_acc = o; o = rup(o + (p.out_f32 ? 0 : (size_t)p.M * p.H * 4), 256);
     p.total = o;
     p.off_io_x = o; o = rup(o + (size_t)p.M * p.H * 2, 256);
@@ -132,7 +133,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map over the bf16 intermediate [rows][I], box = 64 columns x BM rows,
+// Tensor map over the fp16 intermediate [rows][I], box = 64 columns x BM rows,
 // 128-byte swizzle (the MMA's K-major B layout).
 bool encode_intermediate_map(CUtensorMap *m, void *a, size_t rows, int I, int BM) {
     EncodeTiledFn fn = encode_fn();
@@ -141,7 +142,7 @@ bool encode_intermediate_map(CUtensorMap *m, void *a, size_t rows, int I, int BM
     cuuint64_t strides[1] = {(cuuint64_t)I * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)BM};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box, estr,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
@@ -325,7 +326,11 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     z.n16[0] = (pl.tiles1_cap * 4 + 15) / 16;
     z.ptr[1] = acc;
     z.n16[1] = (size_t)pl.M * pl.H * 4 / 16;
-    const size_t zero_bytes = (z.n16[0] + z.n16[1]) * 16;
+    uint16_t *x16 = reinterpret_cast<uint16_t *>(ws + pl.off_x16);
+    z.x_bf16 = x;
+    z.x_f16 = x16;
+    z.x_n8 = (size_t)pl.M * pl.H / 8;
+    const size_t zero_bytes = (z.n16[0] + z.n16[1]) * 16 + z.x_n8 * 32;
     int zero_ctas = (int)(zero_bytes / (64 * 1024));
     if (zero_ctas < 1) zero_ctas = 1;
     if (zero_ctas > 2 * sms) zero_ctas = 2 * sms;
@@ -349,12 +354,13 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     GemmParams g1 = g;
     g1.wq = reinterpret_cast<const uint8_t *>(w13_packed);
     g1.wsc = reinterpret_cast<const uint8_t *>(w13_scales);
-    g1.x = x;
+    g1.x = x16;
     g1.a_out = a_buf;
     g1.partial = reinterpret_cast<float *>(ws + pl.off_partial);
     g1.tile_cnt = reinterpret_cast<int32_t *>(ws + pl.off_cnt);
     g1.RT = pl.RT1;
-    g1.KS = pl.H / 64;
+    g1.KSS = pl.H / 64;
+    g1.KS = (g1.KSS + 1) / 2;
     if (!plan_gemm_smem(1, g1)) return MOE_ERR_SHAPE;
     CUtensorMap dummy;
     memset(&dummy, 0, sizeof dummy);
@@ -366,7 +372,8 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     g2.wsc = reinterpret_cast<const uint8_t *>(w2_scales);
     g2.out_acc = acc;
     g2.RT = pl.RT2;
-    g2.KS = pl.I / 128;
+    g2.KSS = pl.I / 128;
+    g2.KS = (g2.KSS + 1) / 2;
     if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
     CUtensorMap tmap;
     if (!encode_intermediate_map(&tmap, a_buf, pl.cap, pl.I, pl.BM)) return MOE_ERR_CUDA;

@@ -8,6 +8,7 @@
 // t*top_k+j routed to it in ascending order, then pad entries (value P) up to a
 // multiple of block_m; one expert id per block; the total count.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 
@@ -100,14 +101,32 @@ __device__ void align_place_round(const AlignArgs &a, int i0, int *base, int *wt
     __syncthreads();
 }
 
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
+    float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
+    lo = fminf(fmaxf(lo, -65504.0f), 65504.0f);
+    hi = fminf(fmaxf(hi, -65504.0f), 65504.0f);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 __device__ void zero_regions(const ZeroArgs &z, int cta, int nctas) {
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t stride = (size_t)nctas * blockDim.x;
+    const size_t first = (size_t)cta * blockDim.x + threadIdx.x;
     for (int r = 0; r < 2; ++r) {
         float4 *p = reinterpret_cast<float4 *>(z.ptr[r]);
         const size_t n = z.n16[r];
-        for (size_t idx = (size_t)cta * blockDim.x + threadIdx.x; idx < n;
-             idx += (size_t)nctas * blockDim.x)
-            p[idx] = zero;
+        for (size_t idx = first; idx < n; idx += stride) p[idx] = zero;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(z.x_bf16);
+    uint4 *dst = reinterpret_cast<uint4 *>(z.x_f16);
+    for (size_t idx = first; idx < z.x_n8; idx += stride) {
+        uint4 v = src[idx];
+        v.x = bf16x2_to_f16x2_sat(v.x);
+        v.y = bf16x2_to_f16x2_sat(v.y);
+        v.z = bf16x2_to_f16x2_sat(v.z);
+        v.w = bf16x2_to_f16x2_sat(v.w);
+        dst[idx] = v;
     }
 }
 

@@ -15,9 +15,10 @@ namespace moe {
 constexpr uint32_t kErrBadExpert = 0x1u;
 constexpr uint32_t kErrTimeout = 0x2u;
 
-// A pipeline wait that takes longer than this is treated as a kernel bug: the
-// waiting role records kErrTimeout and the CTA winds down.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
+// A pipeline wait that takes longer than this many SM cycles (about 2 s at the
+// GB300's 2.07 GHz maximum clock) is treated as a kernel bug: the waiting role
+// records kErrTimeout and the CTA winds down.
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 MOE_DEV uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -44,14 +45,18 @@ MOE_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
                  "r"(bytes)
                  : "memory");
 }
+// try_wait suspends the thread until the phase completes or kSuspendHintNs
+// passes, so a waiting warp does not spin on the issue slots.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -61,18 +66,29 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                        uint32_t *err) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1; it < (1u << 30); ++it) {
+    const long long t0 = clock64();
+#pragma unroll 1
+    for (uint32_t round = 0; round < (1u << 24); ++round) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) break;
-        }
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitTimeoutCycles) break;
     }
     *abort_flag = 1;
     if (err) atomicOr(err, kErrTimeout);
     return false;
 }
+
+// Position in a ring of n stages: index and the parity of the current lap.
+struct Ring {
+    uint32_t idx, ph, n;
+    MOE_DEV explicit Ring(uint32_t n_) : idx(0), ph(0), n(n_) {}
+    MOE_DEV void next() {
+        if (++idx == n) {
+            idx = 0;
+            ph ^= 1u;
+        }
+    }
+};
 
 // ------------------------------------------------------------- async copies --
 MOE_DEV uint64_t l2_policy_evict_first() {
@@ -108,6 +124,19 @@ MOE_DEV void cp_async_16(uint32_t dst, const void *src) {
 MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 MOE_DEV void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 MOE_DEV void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Wait until at most `depth` (1..7) of this thread's cp.async groups are pending.
+MOE_DEV void cp_async_wait_depth(uint32_t depth) {
+    switch (depth) {
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    }
+}
 
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (TMA, tensor-core operand reads).
@@ -164,8 +193,30 @@ MOE_DEV void tc_commit(uint32_t bar) {
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
-MOE_DEV void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// Warp-collective forms: every lane of the warp executes them with the same
+// operands and elect.sync picks the one lane that issues.  (Issuing from
+// warp-uniform code keeps the operands in uniform registers.)
+MOE_DEV void mma_ts_f16_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+MOE_DEV void tc_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            bar)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (fp16 in, fp32 accumulate).
+MOE_DEV void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -175,12 +226,12 @@ MOE_DEV void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
         : "memory");
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major,
-// M = 128, N = n (multiple of 16, 16..256).
-MOE_DEV uint32_t idesc_bf16_m128(uint32_t n) {
+// Instruction descriptor of kind::f16: fp16 A and B (format code 0), fp32 D,
+// both K-major, M = 128, N = n (multiple of 16, 16..256).
+MOE_DEV uint32_t idesc_f16_m128(uint32_t n) {
     return (1u << 4)            // D format: f32
-           | (1u << 7)          // A format: bf16
-           | (1u << 10)         // B format: bf16
+           | (0u << 7)          // A format: f16
+           | (0u << 10)         // B format: f16
            | ((n >> 3) << 17)   // N / 8
            | ((128u >> 4) << 24);  // M / 16
 }

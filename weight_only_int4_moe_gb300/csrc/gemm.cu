@@ -4,37 +4,42 @@
 // Lever" and "The Result: Two Regimes") measures the grouped INT4 MoE GEMM: below
 // a few hundred tokens per call it streams the touched experts' weights from
 // memory and its time grows with the number of active experts; above, every
-// expert is streamed once and extra tokens ride along.  The kernel here is built
-// for both regimes on one design:
+// expert is streamed once and extra tokens ride along.  One kernel design serves
+// both regimes:
 //
 //  * Swap-AB: the MMA's M side (128 lanes of tensor memory) is 128 weight rows,
-//    its N side is the tokens routed to one expert block (16..192, the block's
+//    its N side is the tokens routed to one expert block (16..128, the block's
 //    real row count rounded up to 16), so a decode call with one token per expert
-//    wastes no weight traffic.
-//  * One 8 KB stage = two 128x64 INT4 slabs (+1 KB of bf16 scales), stored
-//    contiguously by the pack step and fetched with one bulk TMA copy into a deep
-//    shared-memory ring (the weight stream is the HBM-bound part).
-//  * Eight dequant warps turn a slab row into 64 bf16 weights with the scale
-//    applied ((q-8)*s: mask/OR into a bf16 with exponent 2^7, subtract 136,
-//    multiply by the scale; two weights per instruction) and store them straight
-//    into tensor memory, which tcgen05.mma reads as its A operand.  Shared-memory
-//    bandwidth is left to the TMA writes.
-//  * The B operand (activations) sits in shared memory in the 128-byte-swizzled
-//    K-major layout: gathered rows of x via cp.async for gate/up, contiguous rows
-//    of the intermediate via a 2-D TMA tensor copy for down.
-//  * Accumulators live in tensor memory.  gate/up keeps gate and up rows of the
-//    same intermediate features in the same lanes (two accumulators), so the
-//    epilogue forms SiLU(g)*u in registers and writes the bf16 intermediate.  The
-//    down epilogue scales by the routing weight and adds into an fp32 [M][H]
-//    accumulator (the top-k combine).
-//  * Work = (expert block, 128-row tile) x k iterations, split evenly over a
-//    persistent grid of one CTA per SM (a k range may cut a tile).  A gate/up tile
-//    cut between CTAs is finished by whichever piece arrives last (partial sums
-//    in per-CTA slots + a counter; nothing spins on another CTA).
+//    streams each touched weight once and wastes no weight traffic.
+//  * A pipeline stage is two k sub-stages of two 128x64 INT4 slabs each (16 KB,
+//    plus 2 KB of bf16 scales), stored contiguously by the pack step.  Two
+//    producer threads fetch a stage with one bulk TMA copy each (weights and
+//    scales), so the weight stream reaches HBM speed with few, large requests.
+//  * Sixteen dequant warps (four per scheduler) each turn one slab row of one
+//    sub-stage into 64 fp16 weights (q-8)*s -- a mask/OR into an fp16 with
+//    exponent 2^10, an exact subtraction (or 1/16-scaled FMA for the high
+//    nibble), one multiply by the scale; two weights per instruction -- and
+//    store them into tensor memory, which tcgen05.mma reads as its A operand.
+//  * The B operand (fp16 activations) sits in shared memory in the 128-byte-
+//    swizzled K-major layout: rows of x gathered with cp.async for gate/up,
+//    contiguous rows of the intermediate by 2-D TMA tensor copies for down.
+//  * Accumulators live in tensor memory.  gate/up keeps the gate and up rows of
+//    the same 128 intermediate features in the same lanes (two accumulators), so
+//    the epilogue forms SiLU(g)*u in registers and writes the fp16 intermediate.
+//    The down epilogue scales by the routing weight and adds into the fp32
+//    [M][H] output (the top-k combine).
+//  * Work = (expert block, 128-row tile) x stages, split evenly over a persistent
+//    grid of one CTA per SM (a CTA's range may cut a tile).  A gate/up tile cut
+//    between CTAs is finished by whichever piece arrives last (partial sums in
+//    per-CTA slots + a counter); no CTA ever waits for another.
 //
-// Warp roles (512 threads): 0 weight producer (TMA), 1 MMA issuer + TMEM owner,
-// 2 B loader, 3 idle, 4-11 dequant (4-7 slab 0, 8-11 slab 1), 12-15 epilogue.
-#include <cuda_bf16.h>
+// Warp roles (768 threads): 0 weight producer, 1 TMEM owner, 2 B loader,
+// 3 scale producer, 4-19 dequant in four groups (slab x sub-stage), 20-23 MMA
+// issue + epilogue.  A thread issuing tcgen05.mma waits ~90 cycles per
+// instruction while MMAs from several warps overlap, so each dequant group has
+// its own issuing warp and accumulator (the epilogue sums them).  Every wait is
+// bounded (MOE_DEVERR_TIMEOUT).
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 
@@ -42,11 +47,18 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 768;
 constexpr int kTmemCols = 512;
+constexpr int kDequantWarps = 16;
+constexpr int kFirstDequantWarp = 4;
+constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
+constexpr uint32_t kStageW = 2 * kStageWBytes;  // 16 KB of INT4 per stage
+constexpr uint32_t kStageS = 2 * kStageSBytes;  // 2 KB of scales per stage
+constexpr uint32_t kStage = kStageW + kStageS;  // 18 KB
+constexpr uint32_t kACols = 128;                // TMEM columns per A stage
 
 struct Sched {
-    long long start, end;  // k-iteration range of this CTA (split mode)
+    long long start, end;  // stage range of this CTA (split mode)
     int tiles, KS, G, cta, split;
 };
 
@@ -90,7 +102,7 @@ struct PieceIter {
     }
 };
 
-// First iteration index of CTA c and the CTA owning iteration `it` (split mode).
+// First stage index of CTA c and the CTA owning stage `it` (split mode).
 __device__ __forceinline__ long long range_start(long long T, int G, int c) {
     return (T * c) / G;
 }
@@ -112,28 +124,54 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w, __nv_bfloat162 s2) {
-    const uint32_t v = (w & 0x000F000Fu) | 0x43004300u;  // bf16 pair 128+q
-    const __nv_bfloat162 c136 = __halves2bfloat162(__ushort_as_bfloat16(0x4308),
-                                                   __ushort_as_bfloat16(0x4308));
-    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v);
-    b = __hmul2(__hsub2(b, c136), s2);
-    return *reinterpret_cast<uint32_t *>(&b);
+// Sub-stages of stage j of a tile with `kss` sub-stages (the last may hold one).
+__device__ __forceinline__ int stage_subs(int j, int kss) {
+    return (2 * j + 2 <= kss) ? 2 : 1;
 }
 
+// fp16 pair (1024 + q_lo, 1024 + q_hi) from the nibbles at bits 0..3 and 16..19.
+__device__ __forceinline__ uint32_t magic_lo(uint32_t w) {
+    return (w & 0x000F000Fu) | 0x64006400u;
+}
+// fp16 pair (1024 + 16 q_lo, 1024 + 16 q_hi) from the nibbles at bits 4..7 and 20..23.
+__device__ __forceinline__ uint32_t magic_hi(uint32_t w) {
+    return (w & 0x00F000F0u) | 0x64006400u;
+}
+__device__ __forceinline__ __half2 as_h2(uint32_t v) {
+    return *reinterpret_cast<const __half2 *>(&v);
+}
+__device__ __forceinline__ uint32_t as_u32(__half2 h) {
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// One slab row of a sub-stage: 64 weights (k = 0..63 of the slab's k block) as
+// 32 fp16 pairs (q - 8) * s, out[c] holding k = 2c (low half) and 2c + 1 (high).
+// Word v holds k = 8v..8v+7: bits 4s and 16+4s are k = 8v+2s and 8v+2s+1.
+// The subtraction of 1032 (or the 1/16-scaled FMA with -72) is exact; the one
+// rounding is the final product with the fp16 scale (two per word `sc`).
 __device__ __forceinline__ void dequant_row(const uint4 lo, const uint4 hi, uint32_t sc,
                                             uint32_t (&out)[32]) {
-    const __nv_bfloat16 s_lo = __ushort_as_bfloat16((unsigned short)(sc & 0xFFFFu));
-    const __nv_bfloat16 s_hi = __ushort_as_bfloat16((unsigned short)(sc >> 16));
-    const __nv_bfloat162 s0 = __halves2bfloat162(s_lo, s_lo);
-    const __nv_bfloat162 s1 = __halves2bfloat162(s_hi, s_hi);
+    const __half2 s0 = as_h2(__byte_perm(sc, 0, 0x1010));  // group 0 scale, both halves
+    const __half2 s1 = as_h2(__byte_perm(sc, 0, 0x3232));  // group 1 scale
+    const __half2 c1032 = as_h2(0x64086408u);  // 1032
+    const __half2 c16th = as_h2(0x2C002C00u);  // 1/16
+    const __half2 cm72 = as_h2(0xD480D480u);   // -72
     const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
     for (int v = 0; v < 8; ++v) {
-        const __nv_bfloat162 s2 = (v < 4) ? s0 : s1;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) out[4 * v + s] = dq_pair(w[v] >> (4 * s), s2);
+        const __half2 s2 = (v < 4) ? s0 : s1;
+        const uint32_t w8 = w[v] >> 8;
+        out[4 * v + 0] = as_u32(__hmul2(__hsub2(as_h2(magic_lo(w[v])), c1032), s2));
+        out[4 * v + 1] = as_u32(__hmul2(__hfma2(as_h2(magic_hi(w[v])), c16th, cm72), s2));
+        out[4 * v + 2] = as_u32(__hmul2(__hsub2(as_h2(magic_lo(w8)), c1032), s2));
+        out[4 * v + 3] = as_u32(__hmul2(__hfma2(as_h2(magic_hi(w8)), c16th, cm72), s2));
     }
+}
+
+// fp32 -> fp16, saturating at the largest finite fp16 value.
+__device__ __forceinline__ uint16_t f16_sat(float v) {
+    v = fminf(fmaxf(v, -65504.0f), 65504.0f);
+    return __half_as_ushort(__float2half_rn(v));
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
@@ -153,6 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BM = p.block_m;
     const int n_w = p.n_w, n_b = p.n_b, n_a = p.n_a;
+    const int ni = p.ni;    // MMA issuers (4: one per dequant group, 2: one per slab)
+    const int kss = p.KSS;  // sub-stages per tile
 
     // shared-memory map
     const uint32_t w_ring = base;
@@ -162,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_w_empty = bar_w_full + 8 * n_w;
     const uint32_t bar_b_full = bar_w_empty + 8 * n_w;
     const uint32_t bar_b_empty = bar_b_full + 8 * n_b;
-    const uint32_t bar_a_full = bar_b_empty + 8 * n_b;
-    const uint32_t bar_a_empty = bar_a_full + 8 * n_a;
+    const uint32_t bar_a_full = bar_b_empty + 8 * n_b;  // [4 groups][n_a]
+    const uint32_t bar_a_empty = bar_a_full + 8 * 4 * n_a;
     const uint32_t bar_acc_full = bar_a_empty + 8 * n_a;
     const uint32_t bar_acc_empty = bar_acc_full + 8;
     const uint32_t bar_drain = bar_acc_empty + 8;
@@ -176,20 +216,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_w; ++i) {
-            mbar_init(bar_w_full + 8 * i, 1);
-            mbar_init(bar_w_empty + 8 * i, 8);
+            mbar_init(bar_w_full + 8 * i, 2);  // weight + scale producers
+            mbar_init(bar_w_empty + 8 * i, kDequantWarps);
         }
         for (int i = 0; i < n_b; ++i) {
             mbar_init(bar_b_full + 8 * i, 1);
-            mbar_init(bar_b_empty + 8 * i, 1);
+            mbar_init(bar_b_empty + 8 * i, ni);
         }
-        for (int i = 0; i < n_a; ++i) {
-            mbar_init(bar_a_full + 8 * i, 8);
-            mbar_init(bar_a_empty + 8 * i, 1);
-        }
-        mbar_init(bar_acc_full, 1);
+        for (int i = 0; i < n_a; ++i) mbar_init(bar_a_empty + 8 * i, ni);
+        for (int i = 0; i < 4 * n_a; ++i) mbar_init(bar_a_full + 8 * i, 4);  // a group's 4 warps
+        mbar_init(bar_acc_full, ni);
         mbar_init(bar_acc_empty, 4);
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, ni);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -202,38 +240,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // tensor-memory column map
-    const uint32_t col_d0 = 0;                          // gate acc (kind 1) / acc (kind 2)
-    const uint32_t col_d1 = (KIND == 1) ? BM : 0;       // up acc (kind 1)
-    const uint32_t col_a = (KIND == 1) ? 2 * BM : BM;   // A ring: n_a stages x 64 columns
+    // Tensor-memory column map: accumulators first, then the A ring.
+    // Accumulator of dequant group (slab g, sub-stage u): (ni == 4 ? 2g + u : g) * BM.
+    // gate/up: slab 0 feeds the gate accumulator(s), slab 1 the up accumulator(s).
+    // accumulators: one per issuer, but a single gate/up issuer keeps two
+    const int n_acc = (ni == 1 && KIND == 1) ? 2 : ni;
+    const uint32_t col_a = (uint32_t)(n_acc * BM);  // A ring: n_a stages x 128 columns
 
     const Sched sched = make_sched(p);
     PieceIter pi;
     pi.init(sched);
     int tile, kb0, kb1;
 
-    if (wid == 0) {
-        // ------------------------------------------------ weight producer --
+    if (wid == 0 || wid == 3) {
+        // --------------------------- weight (warp 0) / scale (warp 3) producer --
         if (lane == 0) {
+            const bool scales = (wid == 3);
+            const uint8_t *src = scales ? p.wsc : p.wq;
+            const uint32_t sub_bytes = scales ? kStageSBytes : kStageWBytes;
+            const uint32_t dst_off = scales ? kStageW : 0u;
             const uint64_t pol = l2_policy_evict_first();
             uint32_t i = 0;
+            Ring w(n_w);
             bool ok = true;
             while (ok && pi.next(sched, tile, kb0, kb1)) {
                 const int b = tile / p.RT, r = tile % p.RT;
                 const int e = p.expert_ids[b];
-                const size_t st0 = ((size_t)e * p.RT + r) * p.KS;
-                for (int kb = kb0; kb < kb1; ++kb, ++i) {
-                    const uint32_t s = i % n_w;
-                    if (!mbar_wait(bar_w_empty + 8 * s, ((i / n_w) & 1) ^ 1, abort_flag, p.err)) {
+                const size_t sub0 = ((size_t)e * p.RT + r) * kss;  // first sub-stage of the tile
+                for (int j = kb0; j < kb1; ++j, ++i, w.next()) {
+                    if (!mbar_wait(bar_w_empty + 8 * w.idx, w.ph ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = w_ring + s * kStageBytes;
-                    mbar_arrive_expect_tx(bar_w_full + 8 * s, kStageBytes);
-                    bulk_g2s(dst, p.wq + (st0 + kb) * kStageWBytes, kStageWBytes,
-                             bar_w_full + 8 * s, pol);
-                    bulk_g2s(dst + kStageWBytes, p.wsc + (st0 + kb) * kStageSBytes,
-                             kStageSBytes, bar_w_full + 8 * s, pol);
+                    const uint32_t bytes = stage_subs(j, kss) * sub_bytes;
+                    mbar_arrive_expect_tx(bar_w_full + 8 * w.idx, bytes);
+                    bulk_g2s(w_ring + w.idx * kStage + dst_off, src + (sub0 + 2 * j) * sub_bytes,
+                             bytes, bar_w_full + 8 * w.idx, pol);
                 }
             }
             if (!ok) {  // let copies in flight land before the CTA exits
@@ -243,123 +285,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(bar_w_full + 8 * (j % n_w), (j / n_w) & 1, &never, nullptr);
             }
         }
-    } else if (wid == 1) {
-        // ---------------------------------------------------- MMA issuer --
-        uint32_t i = 0, c = 0;
-        bool ok = true;
-        while (ok && pi.next(sched, tile, kb0, kb1)) {
-            const int b = tile / p.RT;
-            const int nr = block_rows(p.sorted_ids, b * BM, BM, p.P);
-            const uint32_t n_mma = nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15);
-            const uint32_t idesc = idesc_bf16_m128(n_mma);
-            if (!warp_wait(bar_acc_empty, (c & 1) ^ 1, abort_flag, p.err)) { ok = false; break; }
-            tc_fence_after();
-            for (int kb = kb0; kb < kb1; ++kb, ++i) {
-                const uint32_t as = i % n_a, bs = i % n_b;
-                if (!warp_wait(bar_a_full + 8 * as, (i / n_a) & 1, abort_flag, p.err) ||
-                    !warp_wait(bar_b_full + 8 * bs, (i / n_b) & 1, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a0 = tmem + col_a + as * 64;
-                    const uint32_t bsm = b_ring + bs * p.b_stage_bytes;
-                    const uint64_t bd0 = smem_desc_sw128(bsm);
-                    const uint32_t first = (kb == kb0) ? 0u : 1u;
-                    if (KIND == 1) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_ts_bf16(tmem + col_d0, a0 + 8 * k, bd0 + 2 * k, idesc,
-                                        (k > 0) | first);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_ts_bf16(tmem + col_d1, a0 + 32 + 8 * k, bd0 + 2 * k, idesc,
-                                        (k > 0) | first);
-                    } else {
-                        const uint64_t bd1 = smem_desc_sw128(bsm + (uint32_t)BM * 128u);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_ts_bf16(tmem + col_d0, a0 + 8 * k, bd0 + 2 * k, idesc,
-                                        (k > 0) | first);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_ts_bf16(tmem + col_d0, a0 + 32 + 8 * k, bd1 + 2 * k, idesc, 1u);
-                    }
-                    tc_commit(bar_a_empty + 8 * as);
-                    tc_commit(bar_b_empty + 8 * bs);
-                }
-                __syncwarp();
-            }
-            if (!ok) break;
-            if (lane == 0) tc_commit(bar_acc_full);
-            __syncwarp();
-            ++c;
-        }
-        // wait for every MMA issued by this warp before the CTA releases TMEM
-        if (lane == 0) {
-            volatile int never = 0;
-            tc_commit(bar_drain);
-            mbar_wait(bar_drain, 0, &never, nullptr);
-        }
-        __syncwarp();
     } else if (wid == 2) {
         // ------------------------------------------------------ B loader --
         uint32_t i = 0;
         bool ok = true;
         if (KIND == 1) {
-            const uint32_t tile_bytes = p.b_stage_bytes;
+            // x rows gathered by cp.async; stage i is published once stage
+            // i + depth has been issued (depth <= n_b / 2 keeps n_b - depth
+            // stages of slack between this loader and the MMAs).
+            const uint32_t depth = (uint32_t)(n_b / 2);
+            Ring bq(n_b), pub(n_b);
             while (ok && pi.next(sched, tile, kb0, kb1)) {
                 const int b = tile / p.RT;
                 const int pos0 = b * BM;
                 const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
                 __syncwarp();
-                for (int j = lane; j < nr; j += 32)
-                    tok_off[j] = (p.sorted_ids[pos0 + j] / p.top_k) * p.H;
+                for (int jr = lane; jr < nr; jr += 32)
+                    tok_off[jr] = (p.sorted_ids[pos0 + jr] / p.top_k) * p.H;
                 __syncwarp();
-                for (int kb = kb0; kb < kb1; ++kb, ++i) {
-                    const uint32_t s = i % n_b;
-                    if (!warp_wait(bar_b_empty + 8 * s, ((i / n_b) & 1) ^ 1, abort_flag, p.err)) {
+                for (int j = kb0; j < kb1; ++j, ++i, bq.next()) {
+                    if (!warp_wait(bar_b_empty + 8 * bq.idx, bq.ph ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst0 = b_ring + s * tile_bytes;
-                    const uint16_t *src0 = p.x + kb * 64;
-                    for (int idx = lane; idx < nr * 8; idx += 32) {
-                        const int j = idx >> 3, ch = idx & 7;
-                        cp_async_16(dst0 + j * 128 + ((ch ^ (j & 7)) << 4),
-                                    src0 + tok_off[j] + ch * 8);
+                    const int nsub = stage_subs(j, kss);
+                    for (int u = 0; u < nsub; ++u) {
+                        const uint32_t dst0 = b_ring + bq.idx * p.b_stage_bytes + u * BM * 128;
+                        const uint16_t *src0 = p.x + (2 * j + u) * 64;
+                        for (int idx = lane; idx < nr * 8; idx += 32) {
+                            const int jr = idx >> 3, ch = idx & 7;
+                            cp_async_16(dst0 + jr * 128 + ((ch ^ (jr & 7)) << 4),
+                                        src0 + tok_off[jr] + ch * 8);
+                        }
                     }
                     cp_async_commit();
-                    if (i > 0) {
-                        cp_async_wait_1();
+                    if (i >= depth) {
+                        cp_async_wait_depth(depth);
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_b_full + 8 * ((i - 1) % n_b));
+                        if (lane == 0) mbar_arrive(bar_b_full + 8 * pub.idx);
+                        pub.next();
                     }
                 }
             }
             cp_async_wait_0();
             fence_proxy_async_smem();
             __syncwarp();
-            if (ok && i > 0 && lane == 0) mbar_arrive(bar_b_full + 8 * ((i - 1) % n_b));
+            if (ok && lane == 0) {
+                const uint32_t pending = (i > depth) ? depth : i;
+                for (uint32_t j = 0; j < pending; ++j, pub.next())
+                    mbar_arrive(bar_b_full + 8 * pub.idx);
+            }
         } else {
             if (lane == 0) {
-                const uint32_t bytes = 2u * BM * 128u;
+                Ring bq(n_b);
                 while (ok && pi.next(sched, tile, kb0, kb1)) {
                     const int b = tile / p.RT;
-                    for (int kb = kb0; kb < kb1; ++kb, ++i) {
-                        const uint32_t s = i % n_b;
-                        if (!mbar_wait(bar_b_empty + 8 * s, ((i / n_b) & 1) ^ 1, abort_flag,
-                                       p.err)) {
+                    for (int j = kb0; j < kb1; ++j, ++i, bq.next()) {
+                        const uint32_t s = bq.idx;
+                        if (!mbar_wait(bar_b_empty + 8 * s, bq.ph ^ 1, abort_flag, p.err)) {
                             ok = false;
                             break;
                         }
+                        const int nsub = stage_subs(j, kss);
                         const uint32_t dst = b_ring + s * p.b_stage_bytes;
-                        mbar_arrive_expect_tx(bar_b_full + 8 * s, bytes);
-                        tma_load_2d(dst, &tmap_a, (2 * kb) * 64, b * BM, bar_b_full + 8 * s);
-                        tma_load_2d(dst + BM * 128, &tmap_a, (2 * kb + 1) * 64, b * BM,
-                                    bar_b_full + 8 * s);
+                        mbar_arrive_expect_tx(bar_b_full + 8 * s,
+                                              (uint32_t)nsub * 2u * BM * 128u);
+                        for (int q = 0; q < 2 * nsub; ++q)  // k blocks 4j .. 4j + 2 nsub - 1
+                            tma_load_2d(dst + q * BM * 128, &tmap_a, (4 * j + q) * 64, b * BM,
+                                        bar_b_full + 8 * s);
                     }
                 }
                 if (!ok) {
@@ -370,98 +364,159 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (wid >= 4 && wid < 12) {
+    } else if (wid >= kFirstDequantWarp && wid < kFirstEpilogueWarp) {
         // ------------------------------------------------------- dequant --
-        const int g = (wid - 4) >> 2;
+        const int d = (wid - kFirstDequantWarp) >> 2;  // group: slab g, sub-stage u
+        const int g = d & 1;
+        const int u = d >> 1;
         const int q = wid & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        uint32_t i = 0;
+        const uint8_t *my_w = smem + u * kStageWBytes + g * kSlabBytes + row * 16;
+        const uint8_t *my_s = smem + kStageW + u * kStageSBytes + g * 512 + row * 4;
+        const uint32_t my_t = tmem + lane_off + col_a + u * 64 + g * 32;
+        Ring w(n_w), a(n_a);
         bool ok = true;
         while (ok && pi.next(sched, tile, kb0, kb1)) {
-            for (int kb = kb0; kb < kb1; ++kb, ++i) {
-                const uint32_t ws = i % n_w;
-                if (!warp_wait(bar_w_full + 8 * ws, (i / n_w) & 1, abort_flag, p.err)) {
+            for (int j = kb0; j < kb1; ++j, w.next(), a.next()) {
+                if (!warp_wait(bar_w_full + 8 * w.idx, w.ph, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *st = smem + (size_t)ws * kStageBytes;
-                const uint4 lo = *reinterpret_cast<const uint4 *>(st + g * kSlabBytes + row * 16);
-                const uint4 hi =
-                    *reinterpret_cast<const uint4 *>(st + g * kSlabBytes + 2048 + row * 16);
-                const uint32_t sc =
-                    *reinterpret_cast<const uint32_t *>(st + kStageWBytes + g * 512 + row * 4);
+                const bool active = u < stage_subs(j, kss);
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                uint32_t sc = 0;
+                if (active) {
+                    const size_t so = (size_t)w.idx * kStage;
+                    lo = *reinterpret_cast<const uint4 *>(my_w + so);
+                    hi = *reinterpret_cast<const uint4 *>(my_w + so + 2048);
+                    sc = *reinterpret_cast<const uint32_t *>(my_s + so);
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_w_empty + 8 * ws);
-                uint32_t v[32];
-                dequant_row(lo, hi, sc, v);
-                const uint32_t as = i % n_a;
-                if (!warp_wait(bar_a_empty + 8 * as, ((i / n_a) & 1) ^ 1, abort_flag, p.err)) {
+                if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
+                if (!warp_wait(bar_a_empty + 8 * a.idx, a.ph ^ 1, abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                tmem_st_32x32b_x32_wait(tmem + lane_off + col_a + as * 64 + g * 32, v);
+                if (active) {
+                    uint32_t v[32];
+                    dequant_row(lo, hi, sc, v);
+                    tc_fence_after();
+                    tmem_st_32x32b_x32_wait(my_t + a.idx * kACols, v);
+                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_a_full + 8 * as);
+                if (lane == 0) mbar_arrive(bar_a_full + 8 * (d * n_a + a.idx));
             }
         }
-    } else if (wid >= 12) {
-        // ------------------------------------------------------ epilogue --
-        const int q = wid & 3;
-        const int row = q * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    } else if (wid >= kFirstEpilogueWarp) {
+        // -------------------------------------------- MMA issue + epilogue --
+        // Warp 20 + qe issues the MMAs of dequant group qe (slab qe & 1,
+        // sub-stage qe >> 1) into its own accumulator; with two issuers, warps
+        // 20 and 21 each cover both sub-stages of slab 0 / 1.  At the end of a
+        // piece all four warps read the accumulators for their 32 TMEM lanes.
+        const int qe = wid & 3;
+        const int row = qe * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(qe * 32) << 16;
+        const bool issuer = (ni == 4) || (qe < 2);
+        const int ig = qe & 1;                        // slab of this issuer
+        const int iu_lo = (ni == 4) ? (qe >> 1) : 0;  // sub-stages of this issuer
+        const int iu_hi = (ni == 4) ? (qe >> 1) + 1 : 2;
+        const uint32_t acc_col = tmem + (uint32_t)(((ni == 4) ? 2 * ig + (qe >> 1) : ig) * BM);
         const long long T = (long long)sched.tiles * sched.KS;
+        Ring a(n_a), bq(n_b);
         uint32_t c = 0;
         bool ok = true;
         while (ok && pi.next(sched, tile, kb0, kb1)) {
             const int b = tile / p.RT, r = tile % p.RT;
             const int pos0 = b * BM;
             const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
-            const bool got = warp_wait(bar_acc_full, c & 1, abort_flag, p.err);
-            // the four epilogue warps leave together (they share named barrier 1)
-            if (named_bar_or(1, 128, !got)) { ok = false; break; }
-            tc_fence_after();
-            if (KIND == 1) {
-                const bool full = (kb0 == 0 && kb1 == p.KS);
-                const int feat = r * kSlabRows + row;
-                if (full) {
-                    for (int j0 = 0; j0 < nr; j0 += 16) {
-                        float gv[16], uv[16];
-                        tmem_ld2_32x32b_x16_wait(tmem + lane_off + col_d0 + j0,
-                                                 tmem + lane_off + col_d1 + j0, gv, uv);
+            // ---- issue
+            bool iok = true;
+            if (issuer) {
+                const uint32_t idesc = idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
+                bool fresh = true;
+                iok = warp_wait(bar_acc_empty, (c & 1) ^ 1, abort_flag, p.err);
+                for (int j = kb0; iok && j < kb1; ++j, a.next(), bq.next()) {
+                    const int nsub = stage_subs(j, kss);
+                    const int uhi = iu_hi < nsub ? iu_hi : nsub;
+                    for (int uu = iu_lo; iok && uu < iu_hi; ++uu)
+                        iok = warp_wait(bar_a_full + 8 * ((2 * uu + ig) * n_a + a.idx), a.ph,
+                                        abort_flag, p.err);
+                    if (iok) iok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
+                    if (!iok) break;
+                    tc_fence_after();
+                    const uint32_t a_st = tmem + col_a + a.idx * kACols;
+                    const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
+                    for (int uu = iu_lo; uu < uhi; ++uu) {
+                        const uint32_t sub = (KIND == 1) ? (uint32_t)uu : (uint32_t)(2 * uu + ig);
+                        const uint64_t bd = smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int j = j0 + jj;
-                            if (j < nr)
-                                p.a_out[(size_t)(pos0 + j) * p.I + feat] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul(gv[jj], uv[jj])));
+                        for (int k = 0; k < 4; ++k) {
+                            mma_ts_f16_elect(acc_col, a_st + uu * 64 + ig * 32 + 8 * k, bd + 2 * k,
+                                             idesc, fresh ? 0u : 1u);
+                            fresh = false;
                         }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty);
-                } else {
+                    tc_commit_elect(bar_a_empty + 8 * a.idx);
+                    tc_commit_elect(bar_b_empty + 8 * bq.idx);
+                }
+                if (iok) tc_commit_elect(bar_acc_full);
+            }
+            // ---- epilogue (all four warps)
+            const bool u1 = !(kb1 - kb0 == 1 && stage_subs(kb0, p.KSS) == 1);
+            const bool got = iok && warp_wait(bar_acc_full, c & 1, abort_flag, p.err);
+            // the four warps leave together (they share named barrier 1)
+            if (named_bar_or(1, 128, !got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int feat = r * kSlabRows + row;
+            const uint32_t tl = tmem + lane_off;
+            if (KIND == 1) {
+                const bool full = (kb0 == 0 && kb1 == p.KS);
+                float *sl = nullptr;
+                if (!full) {
                     const long long piece_start = (long long)tile * p.KS + kb0;
                     const int slot = (piece_start == sched.start) ? 0 : 1;
-                    float *sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
-                    for (int j0 = 0; j0 < nr; j0 += 16) {
-                        float gv[16], uv[16];
-                        tmem_ld2_32x32b_x16_wait(tmem + lane_off + col_d0 + j0,
-                                                 tmem + lane_off + col_d1 + j0, gv, uv);
+                    sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
+                }
+                for (int j0 = 0; j0 < nr; j0 += 16) {
+                    float gv[16], uv[16];
+                    if (ni == 4) {
+                        // accumulator of (slab g, sub-stage u) is column (2g + u) * BM
+                        tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, gv, uv);
+                        if (u1) {
+                            float g1[16], u1v[16];
+                            tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, g1, u1v);
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int j = j0 + jj;
-                            if (j < nr) {
-                                sl[(size_t)j * 128 + row] = gv[jj];
-                                sl[(size_t)(BM + j) * 128 + row] = uv[jj];
+                            for (int jj = 0; jj < 16; ++jj) {
+                                gv[jj] += g1[jj];
+                                uv[jj] += u1v[jj];
+                            }
+                        }
+                    } else {
+                        tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int jr = j0 + jj;
+                        if (jr < nr) {
+                            if (full) {
+                                p.a_out[(size_t)(pos0 + jr) * p.I + feat] =
+                                    f16_sat(silu_mul(gv[jj], uv[jj]));
+                            } else {
+                                sl[(size_t)jr * 128 + row] = gv[jj];
+                                sl[(size_t)(BM + jr) * 128 + row] = uv[jj];
                             }
                         }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acc_empty);
+                if (!full) {
                     __threadfence();
                     named_bar_sync(1, 128);
                     if (row == 0) {
@@ -477,32 +532,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const long long ts = (long long)tile * p.KS, te = ts + p.KS;
                         const int c_first = range_owner(T, sched.G, ts);
                         const int c_last = range_owner(T, sched.G, te - 1);
-                        for (int j = 0; j < nr; ++j) {
+                        for (int jr = 0; jr < nr; ++jr) {
                             float gs = 0.f, us = 0.f;
                             for (int cc = c_first; cc <= c_last; ++cc) {
                                 const long long cs = range_start(T, sched.G, cc);
-                                if (range_start(T, sched.G, cc + 1) == cs) continue;  // empty range
+                                if (range_start(T, sched.G, cc + 1) == cs) continue;  // empty
                                 const int sslot = (cs >= ts) ? 0 : 1;
                                 const float *ps =
                                     p.partial + ((size_t)(cc * 2 + sslot) * 2) * BM * 128;
-                                gs += __ldcg(ps + (size_t)j * 128 + row);
-                                us += __ldcg(ps + (size_t)(BM + j) * 128 + row);
+                                gs += __ldcg(ps + (size_t)jr * 128 + row);
+                                us += __ldcg(ps + (size_t)(BM + jr) * 128 + row);
                             }
-                            p.a_out[(size_t)(pos0 + j) * p.I + feat] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul(gs, us)));
+                            p.a_out[(size_t)(pos0 + jr) * p.I + feat] = f16_sat(silu_mul(gs, us));
                         }
                     }
                 }
             } else {
-                const int feat = r * kSlabRows + row;
                 for (int j0 = 0; j0 < nr; j0 += 16) {
                     float dv[16];
-                    tmem_ld_32x32b_x16_wait(tmem + lane_off + col_d0 + j0, dv);
+                    if (ni == 4) {
+                        float d1[16];
+                        tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, dv, d1);
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
+                        if (u1) {
+                            float d2[16], d3[16];
+                            tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, d2, d3);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) dv[jj] += d2[jj] + d3[jj];
+                        }
+                    } else {
+                        float d1[16];
+                        tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, dv, d1);
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
+                    }
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const int j = j0 + jj;
-                        if (j < nr) {
-                            const int pair = p.sorted_ids[pos0 + j];
+                        const int jr = j0 + jj;
+                        if (jr < nr) {
+                            const int pair = p.sorted_ids[pos0 + jr];
                             const int t = pair / p.top_k;
                             atomicAdd(p.out_acc + (size_t)t * p.H + feat,
                                       p.topk_weights[pair] * dv[jj]);
@@ -515,6 +584,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++c;
         }
+        if (issuer) {  // every MMA of this CTA must finish before TMEM is released
+            volatile int never = 0;
+            tc_commit_elect(bar_drain);
+            warp_wait(bar_drain, 0, &never, nullptr);
+        }
     }
 
     __syncthreads();
@@ -526,23 +600,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool plan_gemm_smem(int kind, GemmParams &p) {
     const int BM = p.block_m;
-    if (BM < 16 || BM % 16 != 0 || BM > 192) return false;
-    p.b_stage_bytes = (uint32_t)((kind == 1 ? 1 : 2) * BM * 128);
-    const int a_cols = (kind == 1) ? 2 * BM : BM;
-    p.n_a = (kTmemCols - a_cols) / 64;
-    if (p.n_a > 4) p.n_a = 4;
+    if (BM < 16 || BM % 16 != 0 || BM > 128) return false;
+    // k blocks per B stage: gate/up two 64-wide blocks, down four
+    p.b_stage_bytes = (uint32_t)((kind == 1 ? 2 : 4) * BM * 128);
+    // four MMA issuers (one accumulator each) while tensor memory allows two A
+    // stages next to them; else two
+    p.ni = (4 * BM + 2 * (int)kACols <= kTmemCols) ? 4 : 2;
+    const int n_acc = (p.ni == 1 && kind == 1) ? 2 : p.ni;
+    p.n_a = (kTmemCols - n_acc * BM) / (int)kACols;
+    if (p.n_a > 3) p.n_a = 3;
     if (p.n_a < 2) return false;
     const uint32_t limit = 227 * 1024 - 1024;  // opt-in maximum minus alignment slack
-    const uint32_t misc = 1024 + 16 + 4 * 192;  // barriers + words + loader table
-    int n_b = (BM <= 64) ? 4 : 3;
-    if (kind == 2 && BM > 128) n_b = 2;
+    const uint32_t misc = 1024 + 16 + 4 * 128;  // barriers + words + loader table
+    int n_b = (BM <= 32) ? 8 : (BM <= 64) ? 4 : 3;
+    if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;
     p.n_b = n_b;
     const uint32_t b_bytes = (uint32_t)n_b * p.b_stage_bytes;
-    int n_w = (int)((limit - b_bytes - misc) / kStageBytes);
-    if (n_w > 16) n_w = 16;
-    if (n_w < 4) return false;
+    int n_w = (int)((limit - b_bytes - misc) / kStage);
+    if (n_w > 10) n_w = 10;
+    if (n_w < 3) return false;
     p.n_w = n_w;
-    const uint32_t w_bytes = (uint32_t)n_w * kStageBytes;
+    const uint32_t w_bytes = (uint32_t)n_w * kStage;
     p.smem_b_off = (w_bytes + 1023u) & ~1023u;
     p.smem_misc_off = p.smem_b_off + b_bytes;
     p.smem_bytes = p.smem_misc_off + misc + 1024;  // + slack for the 1 KB alignment

@@ -20,9 +20,14 @@ struct AlignArgs {
     int n_chunks;          // 0: single-block path
 };
 
+// Per-call preparation done by the align launch's spare blocks: zero two
+// regions and convert the bf16 activations to the fp16 tensor-core operand.
 struct ZeroArgs {
     void *ptr[2];
-    size_t n16[2];  // 16-byte units
+    size_t n16[2];         // 16-byte units
+    const uint16_t *x_bf16;  // [n8 * 8] or null
+    uint16_t *x_f16;
+    size_t x_n8;           // 8-element units
 };
 
 cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas, cudaStream_t s,
@@ -43,20 +48,23 @@ constexpr int kStageBytes = kStageWBytes + kStageSBytes;  // 9216
 struct GemmParams {
     const uint8_t *wq;         // packed INT4 stages
     const uint8_t *wsc;        // packed scales
-    const uint16_t *x;         // gate/up: activations [M][H]
+    const uint16_t *x;         // gate/up: fp16 activations [M][H]
     const int32_t *sorted_ids; // align output
     const int32_t *expert_ids;
     const int32_t *num_post_pad;
     const float *topk_weights; // down: [P]
-    uint16_t *a_out;           // gate/up output, intermediate [rows][I]
+    uint16_t *a_out;           // gate/up output, fp16 intermediate [rows][I]
     float *partial;            // gate/up split slots [G][2][2][BM][128]
     int32_t *tile_cnt;         // gate/up split counters [tiles]
     float *out_acc;            // down: fp32 accumulator [M][H]
     uint32_t *err;             // [2]
     int M, top_k, H, I, P;
-    int block_m;               // BM: routing block height (multiple of 16, <= 192)
-    int RT, KS;                // row tiles per expert, k stages per tile
+    int block_m;               // BM: routing block height (multiple of 16, <= 128)
+    int RT;                    // row tiles per expert
+    int KSS, KS;               // k sub-stages per tile (one 8 KB packed stage each) and
+                               // pipeline stages per tile (two sub-stages, the last maybe one)
     int n_w, n_b, n_a;         // ring depths: weight stages, B stages, A (TMEM) stages
+    int ni;                    // MMA-issuing warps (= accumulators): 4 or 2
     int split;                 // 1: partition k iterations evenly over CTAs
     uint32_t b_stage_bytes;
     uint32_t smem_b_off, smem_misc_off, smem_bytes;

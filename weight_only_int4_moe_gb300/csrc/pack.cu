@@ -6,6 +6,8 @@
 // each stage is contiguous, each dequantising thread reads its row's 32 bytes
 // as two conflict-free 16-byte shared-memory loads, and the nibble order lets
 // one mask/OR produce two bf16 values at once.
+#include <cuda_fp16.h>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -48,6 +50,14 @@ __global__ void pack_weights_kernel(const uint8_t *__restrict__ q, uint32_t *__r
     }
 }
 
+// bf16 scale -> fp16 (exact for magnitudes in [2^-14, 65504]; saturating above,
+// fp16 subnormals below).
+__device__ __forceinline__ uint16_t bf16_bits_to_f16_sat(uint16_t b) {
+    float v = __uint_as_float((uint32_t)b << 16);
+    v = fminf(fmaxf(v, -65504.0f), 65504.0f);
+    return __half_as_ushort(__float2half_rn(v));
+}
+
 __global__ void pack_scales_kernel(const uint16_t *__restrict__ s, uint32_t *__restrict__ out,
                                    int N, int K, int is_w13, size_t n_words) {
     const int KS = is_w13 ? K / kSlabK : K / (2 * kSlabK);
@@ -71,7 +81,8 @@ __global__ void pack_scales_kernel(const uint16_t *__restrict__ s, uint32_t *__r
             kb = 2 * kk + slab;
         }
         const uint16_t *src = s + (e * N + n) * (size_t)G + 2 * kb;
-        out[idx] = (uint32_t)src[0] | ((uint32_t)src[1] << 16);
+        out[idx] = (uint32_t)bf16_bits_to_f16_sat(src[0]) |
+                   ((uint32_t)bf16_bits_to_f16_sat(src[1]) << 16);
     }
 }
 
