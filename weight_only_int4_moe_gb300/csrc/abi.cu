@@ -78,7 +78,7 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.off_cnt = o; o = rup(o + p.tiles1_cap * 4, 256);
     p.off_partial = o; o = rup(o + (size_t)kMaxGrid * 4 * p.BM * 128 * 4, 256);
     p.off_a = o; o = rup(o + p.cap * (size_t)p.I * 2, 256);
-    p.off_x16 = o; o = rup(o + (size_t)p.M * p.H * 2, 256);
+    p.off_x16 = o; o = rup(o + p.cap * (size_t)p.H * 2, 256);  // x rows, bucketed, fp16
     p.off_acc = o; o = rup(o + (p.out_f32 ? 0 : (size_t)p.M * p.H * 4), 256);
     p.total = o;
     p.off_io_x = o; o = rup(o + (size_t)p.M * p.H * 2, 256);
@@ -133,9 +133,9 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map over the fp16 intermediate [rows][I], box = 64 columns x BM rows,
-// 128-byte swizzle (the MMA's K-major B layout).
-bool encode_intermediate_map(CUtensorMap *m, void *a, size_t rows, int I, int BM) {
+// Tensor map over fp16 rows [rows][cols] (bucketed x or the intermediate), box
+// = 64 columns x BM rows, 128-byte swizzle (the MMA's K-major B layout).
+bool encode_rows_map(CUtensorMap *m, void *a, size_t rows, int I, int BM) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)rows};
@@ -327,14 +327,14 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     z.ptr[1] = acc;
     z.n16[1] = (size_t)pl.M * pl.H * 4 / 16;
     uint16_t *x16 = reinterpret_cast<uint16_t *>(ws + pl.off_x16);
-    z.x_bf16 = x;
-    z.x_f16 = x16;
-    z.x_n8 = (size_t)pl.M * pl.H / 8;
-    const size_t zero_bytes = (z.n16[0] + z.n16[1]) * 16 + z.x_n8 * 32;
+    const size_t zero_bytes = (z.n16[0] + z.n16[1]) * 16;
     int zero_ctas = (int)(zero_bytes / (64 * 1024));
     if (zero_ctas < 1) zero_ctas = 1;
     if (zero_ctas > 2 * sms) zero_ctas = 2 * sms;
     if (launch_align(al, z, zero_ctas, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gather_rows(x, sorted, npp, pl.P, pl.k, pl.H, x16, pl.cap, sms, s, &launches) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
     prof_record(1, s);
 
     GemmParams g{};
@@ -354,7 +354,6 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     GemmParams g1 = g;
     g1.wq = reinterpret_cast<const uint8_t *>(w13_packed);
     g1.wsc = reinterpret_cast<const uint8_t *>(w13_scales);
-    g1.x = x16;
     g1.a_out = a_buf;
     g1.partial = reinterpret_cast<float *>(ws + pl.off_partial);
     g1.tile_cnt = reinterpret_cast<int32_t *>(ws + pl.off_cnt);
@@ -362,9 +361,9 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     g1.KSS = pl.H / 64;
     g1.KS = (g1.KSS + 1) / 2;
     if (!plan_gemm_smem(1, g1)) return MOE_ERR_SHAPE;
-    CUtensorMap dummy;
-    memset(&dummy, 0, sizeof dummy);
-    if (launch_gemm(1, g1, &dummy, grid, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+    CUtensorMap tmap_x;
+    if (!encode_rows_map(&tmap_x, x16, pl.cap, pl.H, pl.BM)) return MOE_ERR_CUDA;
+    if (launch_gemm(1, g1, &tmap_x, grid, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
     prof_record(2, s);
 
     GemmParams g2 = g;
@@ -376,7 +375,7 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     g2.KS = (g2.KSS + 1) / 2;
     if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
     CUtensorMap tmap;
-    if (!encode_intermediate_map(&tmap, a_buf, pl.cap, pl.I, pl.BM)) return MOE_ERR_CUDA;
+    if (!encode_rows_map(&tmap, a_buf, pl.cap, pl.I, pl.BM)) return MOE_ERR_CUDA;
     if (launch_gemm(2, g2, &tmap, grid, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
     prof_record(3, s);
 

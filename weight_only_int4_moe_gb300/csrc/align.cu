@@ -118,16 +118,43 @@ __device__ void zero_regions(const ZeroArgs &z, int cta, int nctas) {
         const size_t n = z.n16[r];
         for (size_t idx = first; idx < n; idx += stride) p[idx] = zero;
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(z.x_bf16);
-    uint4 *dst = reinterpret_cast<uint4 *>(z.x_f16);
-    for (size_t idx = first; idx < z.x_n8; idx += stride) {
-        uint4 v = src[idx];
-        v.x = bf16x2_to_f16x2_sat(v.x);
-        v.y = bf16x2_to_f16x2_sat(v.y);
-        v.z = bf16x2_to_f16x2_sat(v.z);
-        v.w = bf16x2_to_f16x2_sat(v.w);
-        dst[idx] = v;
+}
+
+// Rows of x in bucketed order, as the fp16 tensor-core operand of the gate/up
+// GEMM: xs[pos] = fp16(x[sorted_ids[pos] / top_k]) for every real entry (pad
+// rows are left as they are; the GEMM ignores their results).  One warp per row.
+__global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ sorted,
+                                   const int32_t *__restrict__ num_post_pad, int P, int top_k, int H,
+                                   uint16_t *__restrict__ xs) {
+    const int npp = *num_post_pad;
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    const int n8 = H / 8;
+    for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < npp; pos += warps) {
+        const int pair = sorted[pos];
+        if (pair >= P) continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(pair / top_k) * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)pos * H);
+        for (int c = lane; c < n8; c += 32) {
+            uint4 v = src[c];
+            v.x = bf16x2_to_f16x2_sat(v.x);
+            v.y = bf16x2_to_f16x2_sat(v.y);
+            v.z = bf16x2_to_f16x2_sat(v.z);
+            v.w = bf16x2_to_f16x2_sat(v.w);
+            dst[c] = v;
+        }
     }
+}
+
+cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const int32_t *npp, int P,
+                               int top_k, int H, uint16_t *xs, size_t cap_rows, int sms,
+                               cudaStream_t s, int *launches) {
+    size_t blocks = (cap_rows + 7) / 8;  // 8 warps (rows) per block
+    if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
+    if (blocks < 1) blocks = 1;
+    gather_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, sorted, npp, P, top_k, H, xs);
+    if (launches) *launches += 1;
+    return cudaGetLastError();
 }
 
 // Whole align in one block (P small); blocks 1.. zero the accumulators.

@@ -61,21 +61,35 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on the phase with the given parity.  Returns false (and records
-// the timeout) if the wait gives up or another role of the CTA already aborted.
-MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                       uint32_t *err) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait on the phase with the given parity.  Polls try_wait; after a
+// few polls it sleeps `backoff_ns` between polls (0: keep polling, for waits on
+// the critical path) and only then starts reading the cycle counter.  Returns
+// false (and records the timeout) if the wait gives up or another role of the
+// CTA already aborted.
+MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint32_t *err,
+                       uint32_t backoff_ns = 0) {
+#pragma unroll 1
+    for (int it = 0; it < 8; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
 #pragma unroll 1
     for (uint32_t round = 0; round < (1u << 24); ++round) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int it = 0; it < 16; ++it) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if (backoff_ns) __nanosleep(backoff_ns);
+        }
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitTimeoutCycles) break;
     }
     *abort_flag = 1;
     if (err) atomicOr(err, kErrTimeout);
     return false;
+}
+
+// Producer/consumer named barrier: arrive without waiting / wait for `threads`.
+MOE_DEV void named_bar_arrive(uint32_t id, uint32_t threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Position in a ring of n stages: index and the parity of the current lap.

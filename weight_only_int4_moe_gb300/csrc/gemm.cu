@@ -15,14 +15,15 @@
 //    plus 2 KB of bf16 scales), stored contiguously by the pack step.  Two
 //    producer threads fetch a stage with one bulk TMA copy each (weights and
 //    scales), so the weight stream reaches HBM speed with few, large requests.
-//  * Sixteen dequant warps (four per scheduler) each turn one slab row of one
-//    sub-stage into 64 fp16 weights (q-8)*s -- a mask/OR into an fp16 with
+//  * Two teams of eight dequant warps (alternate stages) each turn one slab row
+//    of both sub-stages into 128 fp16 weights (q-8)*s -- a mask/OR into an fp16 with
 //    exponent 2^10, an exact subtraction (or 1/16-scaled FMA for the high
 //    nibble), one multiply by the scale; two weights per instruction -- and
 //    store them into tensor memory, which tcgen05.mma reads as its A operand.
 //  * The B operand (fp16 activations) sits in shared memory in the 128-byte-
-//    swizzled K-major layout: rows of x gathered with cp.async for gate/up,
-//    contiguous rows of the intermediate by 2-D TMA tensor copies for down.
+//    swizzled K-major layout, fetched by 2-D TMA tensor copies of rows in
+//    bucketed order: x gathered once per call into that order (gate/up), the
+//    intermediate (down).
 //  * Accumulators live in tensor memory.  gate/up keeps the gate and up rows of
 //    the same 128 intermediate features in the same lanes (two accumulators), so
 //    the epilogue forms SiLU(g)*u in registers and writes the fp16 intermediate.
@@ -34,9 +35,10 @@
 //    per-CTA slots + a counter); no CTA ever waits for another.
 //
 // Warp roles (768 threads): 0 weight producer, 1 TMEM owner, 2 B loader,
-// 3 scale producer, 4-19 dequant in four groups (slab x sub-stage), 20-23 MMA
-// issue + epilogue.  A thread issuing tcgen05.mma waits ~90 cycles per
-// instruction while MMAs from several warps overlap, so each dequant group has
+// 3 scale producer, 4-19 dequant (two teams of eight taking alternate stages;
+// in a team, slab 0: 4 warps, slab 1: 4 warps, each both sub-stages of its 32
+// rows), 20-23 MMA issue + epilogue.  A thread issuing tcgen05.mma waits ~90 cycles per
+// instruction while MMAs from several warps overlap, so each (slab, sub-stage) has
 // its own issuing warp and accumulator (the epilogue sums them).  Every wait is
 // bounded (MOE_DEVERR_TIMEOUT).
 #include <cuda_fp16.h>
@@ -49,13 +51,17 @@ namespace {
 
 constexpr int kThreads = 768;
 constexpr int kTmemCols = 512;
-constexpr int kDequantWarps = 16;
+constexpr int kTeamWarps = 8;                   // dequant warps per team
+constexpr int kDequantWarps = 2 * kTeamWarps;  // two teams, alternate stages
 constexpr int kFirstDequantWarp = 4;
 constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
 constexpr uint32_t kStageW = 2 * kStageWBytes;  // 16 KB of INT4 per stage
 constexpr uint32_t kStageS = 2 * kStageSBytes;  // 2 KB of scales per stage
 constexpr uint32_t kStage = kStageW + kStageS;  // 18 KB
 constexpr uint32_t kACols = 128;                // TMEM columns per A stage
+// hardware named barriers (0 is __syncthreads)
+constexpr uint32_t kBarEpi = 1;     // the four issue/epilogue warps
+constexpr uint32_t kBarSlot0 = 2;   // A stage s written: all dequant warps arrive, issuers wait
 
 struct Sched {
     long long start, end;  // stage range of this CTA (split mode)
@@ -119,8 +125,8 @@ __device__ __forceinline__ int block_rows(const int32_t *sorted, int pos0, int B
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          uint32_t *err) {
-    bool ok = mbar_wait(bar, parity, abort, err);
+                                          uint32_t *err, uint32_t backoff_ns = 0) {
+    bool ok = mbar_wait(bar, parity, abort, err, backoff_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -182,7 +188,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_a) {
+    moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_b) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -202,8 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_w_empty = bar_w_full + 8 * n_w;
     const uint32_t bar_b_full = bar_w_empty + 8 * n_w;
     const uint32_t bar_b_empty = bar_b_full + 8 * n_b;
-    const uint32_t bar_a_full = bar_b_empty + 8 * n_b;  // [4 groups][n_a]
-    const uint32_t bar_a_empty = bar_a_full + 8 * 4 * n_a;
+    const uint32_t bar_a_empty = bar_b_empty + 8 * n_b;
     const uint32_t bar_acc_full = bar_a_empty + 8 * n_a;
     const uint32_t bar_acc_empty = bar_acc_full + 8;
     const uint32_t bar_drain = bar_acc_empty + 8;
@@ -212,19 +217,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc_ptr + 4);
     volatile int *bcast = reinterpret_cast<volatile int *>(misc_ptr + 8);
-    int32_t *tok_off = reinterpret_cast<int32_t *>(misc_ptr + 16);  // [BM] B-loader table
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_w; ++i) {
             mbar_init(bar_w_full + 8 * i, 2);  // weight + scale producers
-            mbar_init(bar_w_empty + 8 * i, kDequantWarps);
+            mbar_init(bar_w_empty + 8 * i, kTeamWarps);
         }
         for (int i = 0; i < n_b; ++i) {
             mbar_init(bar_b_full + 8 * i, 1);
             mbar_init(bar_b_empty + 8 * i, ni);
         }
         for (int i = 0; i < n_a; ++i) mbar_init(bar_a_empty + 8 * i, ni);
-        for (int i = 0; i < 4 * n_a; ++i) mbar_init(bar_a_full + 8 * i, 4);  // a group's 4 warps
         mbar_init(bar_acc_full, ni);
         mbar_init(bar_acc_empty, 4);
         mbar_init(bar_drain, ni);
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int e = p.expert_ids[b];
                 const size_t sub0 = ((size_t)e * p.RT + r) * kss;  // first sub-stage of the tile
                 for (int j = kb0; j < kb1; ++j, ++i, w.next()) {
-                    if (!mbar_wait(bar_w_empty + 8 * w.idx, w.ph ^ 1, abort_flag, p.err)) {
+                    if (!mbar_wait(bar_w_empty + 8 * w.idx, w.ph ^ 1, abort_flag, p.err, 128)) {
                         ok = false;
                         break;
                     }
@@ -287,131 +290,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (wid == 2) {
         // ------------------------------------------------------ B loader --
-        uint32_t i = 0;
-        bool ok = true;
-        if (KIND == 1) {
-            // x rows gathered by cp.async; stage i is published once stage
-            // i + depth has been issued (depth <= n_b / 2 keeps n_b - depth
-            // stages of slack between this loader and the MMAs).
-            const uint32_t depth = (uint32_t)(n_b / 2);
-            Ring bq(n_b), pub(n_b);
+        // B rows of the block (bucketed order) by 2-D TMA tensor copies: one
+        // 64-column k block per copy, gate/up one per sub-stage, down two.
+        if (lane == 0) {
+            const int kb_per_sub = (KIND == 1) ? 1 : 2;
+            uint32_t i = 0;
+            bool ok = true;
+            Ring bq(n_b);
             while (ok && pi.next(sched, tile, kb0, kb1)) {
                 const int b = tile / p.RT;
-                const int pos0 = b * BM;
-                const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
-                __syncwarp();
-                for (int jr = lane; jr < nr; jr += 32)
-                    tok_off[jr] = (p.sorted_ids[pos0 + jr] / p.top_k) * p.H;
-                __syncwarp();
                 for (int j = kb0; j < kb1; ++j, ++i, bq.next()) {
-                    if (!warp_wait(bar_b_empty + 8 * bq.idx, bq.ph ^ 1, abort_flag, p.err)) {
+                    const uint32_t s = bq.idx;
+                    if (!mbar_wait(bar_b_empty + 8 * s, bq.ph ^ 1, abort_flag, p.err, 128)) {
                         ok = false;
                         break;
                     }
-                    const int nsub = stage_subs(j, kss);
-                    for (int u = 0; u < nsub; ++u) {
-                        const uint32_t dst0 = b_ring + bq.idx * p.b_stage_bytes + u * BM * 128;
-                        const uint16_t *src0 = p.x + (2 * j + u) * 64;
-                        for (int idx = lane; idx < nr * 8; idx += 32) {
-                            const int jr = idx >> 3, ch = idx & 7;
-                            cp_async_16(dst0 + jr * 128 + ((ch ^ (jr & 7)) << 4),
-                                        src0 + tok_off[jr] + ch * 8);
-                        }
-                    }
-                    cp_async_commit();
-                    if (i >= depth) {
-                        cp_async_wait_depth(depth);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_b_full + 8 * pub.idx);
-                        pub.next();
-                    }
+                    const int nblk = stage_subs(j, kss) * kb_per_sub;
+                    const uint32_t dst = b_ring + s * p.b_stage_bytes;
+                    mbar_arrive_expect_tx(bar_b_full + 8 * s, (uint32_t)nblk * BM * 128u);
+                    for (int qb = 0; qb < nblk; ++qb)
+                        tma_load_2d(dst + qb * BM * 128, &tmap_b, (2 * kb_per_sub * j + qb) * 64,
+                                    b * BM, bar_b_full + 8 * s);
                 }
             }
-            cp_async_wait_0();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (ok && lane == 0) {
-                const uint32_t pending = (i > depth) ? depth : i;
-                for (uint32_t j = 0; j < pending; ++j, pub.next())
-                    mbar_arrive(bar_b_full + 8 * pub.idx);
-            }
-        } else {
-            if (lane == 0) {
-                Ring bq(n_b);
-                while (ok && pi.next(sched, tile, kb0, kb1)) {
-                    const int b = tile / p.RT;
-                    for (int j = kb0; j < kb1; ++j, ++i, bq.next()) {
-                        const uint32_t s = bq.idx;
-                        if (!mbar_wait(bar_b_empty + 8 * s, bq.ph ^ 1, abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        const int nsub = stage_subs(j, kss);
-                        const uint32_t dst = b_ring + s * p.b_stage_bytes;
-                        mbar_arrive_expect_tx(bar_b_full + 8 * s,
-                                              (uint32_t)nsub * 2u * BM * 128u);
-                        for (int q = 0; q < 2 * nsub; ++q)  // k blocks 4j .. 4j + 2 nsub - 1
-                            tma_load_2d(dst + q * BM * 128, &tmap_a, (4 * j + q) * 64, b * BM,
-                                        bar_b_full + 8 * s);
-                    }
-                }
-                if (!ok) {
-                    volatile int never = 0;
-                    const uint32_t first = (i > (uint32_t)n_b) ? i - n_b : 0;
-                    for (uint32_t j = first; j < i; ++j)
-                        mbar_wait(bar_b_full + 8 * (j % n_b), (j / n_b) & 1, &never, nullptr);
-                }
+            if (!ok) {
+                volatile int never = 0;
+                const uint32_t first = (i > (uint32_t)n_b) ? i - n_b : 0;
+                for (uint32_t jj = first; jj < i; ++jj)
+                    mbar_wait(bar_b_full + 8 * (jj % n_b), (jj / n_b) & 1, &never, nullptr, 64);
             }
         }
     } else if (wid >= kFirstDequantWarp && wid < kFirstEpilogueWarp) {
         // ------------------------------------------------------- dequant --
-        const int d = (wid - kFirstDequantWarp) >> 2;  // group: slab g, sub-stage u
-        const int g = d & 1;
-        const int u = d >> 1;
+        // Two teams of eight warps take alternate stages, so one team's waits
+        // overlap the other's arithmetic.  Warp 4 + 8t + 4g + q of team t
+        // dequantises rows 32q..32q+31 of slab g for both sub-stages.  Every
+        // stage of the team is visited even after an error (no work, but every
+        // barrier arrival still happens), so no named barrier can be left
+        // waiting.
+        const int dw = wid - kFirstDequantWarp;
+        const int team = dw >> 3;
+        const int g = (dw >> 2) & 1;  // slab
         const int q = wid & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint8_t *my_w = smem + u * kStageWBytes + g * kSlabBytes + row * 16;
-        const uint8_t *my_s = smem + kStageW + u * kStageSBytes + g * 512 + row * 4;
-        const uint32_t my_t = tmem + lane_off + col_a + u * 64 + g * 32;
+        const uint8_t *my_w = smem + g * kSlabBytes + row * 16;
+        const uint8_t *my_s = smem + kStageW + g * 512 + row * 4;
+        const uint32_t my_t = tmem + lane_off + col_a + g * 32;
+        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
+        volatile int no_abort = 0;
         Ring w(n_w), a(n_a);
+        uint32_t si = 0;  // stage counter of this CTA
         bool ok = true;
-        while (ok && pi.next(sched, tile, kb0, kb1)) {
-            for (int j = kb0; j < kb1; ++j, w.next(), a.next()) {
-                if (!warp_wait(bar_w_full + 8 * w.idx, w.ph, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                const bool active = u < stage_subs(j, kss);
-                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                uint32_t sc = 0;
-                if (active) {
-                    const size_t so = (size_t)w.idx * kStage;
-                    lo = *reinterpret_cast<const uint4 *>(my_w + so);
-                    hi = *reinterpret_cast<const uint4 *>(my_w + so + 2048);
-                    sc = *reinterpret_cast<const uint32_t *>(my_s + so);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
-                if (!warp_wait(bar_a_empty + 8 * a.idx, a.ph ^ 1, abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                if (active) {
+        while (pi.next(sched, tile, kb0, kb1)) {
+            for (int j = kb0; j < kb1; ++j, w.next(), a.next(), ++si) {
+                if ((si & 1u) != (uint32_t)team) continue;  // the other team's stage
+                if (ok) ok = warp_wait(bar_w_full + 8 * w.idx, w.ph, abort_flag, p.err);
+                const int nsub = ok ? stage_subs(j, kss) : 0;
+                // The A slot is reused only once the issuers' MMAs on it are done.
+                // This wait happens even after an error: it keeps this warp from
+                // arriving on the slot's named barrier again before the issuers
+                // have consumed the previous arrival.
+                const bool freed = warp_wait(bar_a_empty + 8 * a.idx, a.ph ^ 1, &no_abort, p.err);
+                if (!freed) ok = false;
+                for (int uu = 0; uu < nsub && ok; ++uu) {
+                    const uint8_t *sw = my_w + (size_t)w.idx * kStage + uu * kStageWBytes;
+                    const uint4 lo = *reinterpret_cast<const uint4 *>(sw);
+                    const uint4 hi = *reinterpret_cast<const uint4 *>(sw + 2048);
+                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(
+                        my_s + (size_t)w.idx * kStage + uu * kStageSBytes);
+                    if (uu == nsub - 1) {  // every load of this stage is done
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
+                    }
                     uint32_t v[32];
                     dequant_row(lo, hi, sc, v);
                     tc_fence_after();
-                    tmem_st_32x32b_x32_wait(my_t + a.idx * kACols, v);
+                    tmem_st_32x32b_x32_wait(my_t + a.idx * kACols + uu * 64, v);
                 }
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_a_full + 8 * (d * n_a + a.idx));
+                named_bar_arrive(kBarSlot0 + a.idx, slot_cnt);  // A stage written
             }
         }
     } else if (wid >= kFirstEpilogueWarp) {
         // -------------------------------------------- MMA issue + epilogue --
-        // Warp 20 + qe issues the MMAs of dequant group qe (slab qe & 1,
+        // Warp 20 + qe issues the MMAs of sub-tile qe (slab qe & 1,
         // sub-stage qe >> 1) into its own accumulator; with two issuers, warps
         // 20 and 21 each cover both sub-stages of slab 0 / 1.  At the end of a
         // piece all four warps read the accumulators for their 32 TMEM lanes.
@@ -423,171 +386,172 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int iu_lo = (ni == 4) ? (qe >> 1) : 0;  // sub-stages of this issuer
         const int iu_hi = (ni == 4) ? (qe >> 1) + 1 : 2;
         const uint32_t acc_col = tmem + (uint32_t)(((ni == 4) ? 2 * ig + (qe >> 1) : ig) * BM);
+        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
         const long long T = (long long)sched.tiles * sched.KS;
         Ring a(n_a), bq(n_b);
         uint32_t c = 0;
         bool ok = true;
-        while (ok && pi.next(sched, tile, kb0, kb1)) {
+        while (pi.next(sched, tile, kb0, kb1)) {
             const int b = tile / p.RT, r = tile % p.RT;
             const int pos0 = b * BM;
             const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
-            // ---- issue
-            bool iok = true;
+            // ---- issue (every stage is visited, see the dequant role)
             if (issuer) {
                 const uint32_t idesc = idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
                 bool fresh = true;
-                iok = warp_wait(bar_acc_empty, (c & 1) ^ 1, abort_flag, p.err);
-                for (int j = kb0; iok && j < kb1; ++j, a.next(), bq.next()) {
-                    const int nsub = stage_subs(j, kss);
-                    const int uhi = iu_hi < nsub ? iu_hi : nsub;
-                    for (int uu = iu_lo; iok && uu < iu_hi; ++uu)
-                        iok = warp_wait(bar_a_full + 8 * ((2 * uu + ig) * n_a + a.idx), a.ph,
-                                        abort_flag, p.err);
-                    if (iok) iok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
-                    if (!iok) break;
-                    tc_fence_after();
-                    const uint32_t a_st = tmem + col_a + a.idx * kACols;
-                    const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
-                    for (int uu = iu_lo; uu < uhi; ++uu) {
-                        const uint32_t sub = (KIND == 1) ? (uint32_t)uu : (uint32_t)(2 * uu + ig);
-                        const uint64_t bd = smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
+                if (ok) ok = warp_wait(bar_acc_empty, (c & 1) ^ 1, abort_flag, p.err, 32);
+                for (int j = kb0; j < kb1; ++j, a.next(), bq.next()) {
+                    named_bar_sync(kBarSlot0 + a.idx, slot_cnt);  // the stage's A is in TMEM
+                    if (ok) ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
+                    if (ok) {
+                        const int nsub = stage_subs(j, kss);
+                        const int uhi = iu_hi < nsub ? iu_hi : nsub;
+                        tc_fence_after();
+                        const uint32_t a_st = tmem + col_a + a.idx * kACols;
+                        const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
+                        for (int uu = iu_lo; uu < uhi; ++uu) {
+                            const uint32_t sub = (KIND == 1) ? (uint32_t)uu : (uint32_t)(2 * uu + ig);
+                            const uint64_t bd = smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            mma_ts_f16_elect(acc_col, a_st + uu * 64 + ig * 32 + 8 * k, bd + 2 * k,
-                                             idesc, fresh ? 0u : 1u);
-                            fresh = false;
+                            for (int k = 0; k < 4; ++k) {
+                                mma_ts_f16_elect(acc_col, a_st + uu * 64 + ig * 32 + 8 * k,
+                                                 bd + 2 * k, idesc, fresh ? 0u : 1u);
+                                fresh = false;
+                            }
                         }
                     }
                     tc_commit_elect(bar_a_empty + 8 * a.idx);
                     tc_commit_elect(bar_b_empty + 8 * bq.idx);
                 }
-                if (iok) tc_commit_elect(bar_acc_full);
+                tc_commit_elect(bar_acc_full);
             }
             // ---- epilogue (all four warps)
             const bool u1 = !(kb1 - kb0 == 1 && stage_subs(kb0, p.KSS) == 1);
-            const bool got = iok && warp_wait(bar_acc_full, c & 1, abort_flag, p.err);
-            // the four warps leave together (they share named barrier 1)
-            if (named_bar_or(1, 128, !got)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const int feat = r * kSlabRows + row;
-            const uint32_t tl = tmem + lane_off;
-            if (KIND == 1) {
-                const bool full = (kb0 == 0 && kb1 == p.KS);
-                float *sl = nullptr;
-                if (!full) {
-                    const long long piece_start = (long long)tile * p.KS + kb0;
-                    const int slot = (piece_start == sched.start) ? 0 : 1;
-                    sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
-                }
-                for (int j0 = 0; j0 < nr; j0 += 16) {
-                    float gv[16], uv[16];
-                    if (ni == 4) {
-                        // accumulator of (slab g, sub-stage u) is column (2g + u) * BM
-                        tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, gv, uv);
-                        if (u1) {
-                            float g1[16], u1v[16];
-                            tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, g1, u1v);
+            const bool got = ok && warp_wait(bar_acc_full, c & 1, abort_flag, p.err, 32);
+            // the four warps decide together (they share named barrier 1)
+            if (named_bar_or(kBarEpi, 128, !got)) ok = false;
+            if (ok) {
+                tc_fence_after();
+                const int feat = r * kSlabRows + row;
+                const uint32_t tl = tmem + lane_off;
+                if (KIND == 1) {
+                    const bool full = (kb0 == 0 && kb1 == p.KS);
+                    float *sl = nullptr;
+                    if (!full) {
+                        const long long piece_start = (long long)tile * p.KS + kb0;
+                        const int slot = (piece_start == sched.start) ? 0 : 1;
+                        sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
+                    }
+                    for (int j0 = 0; j0 < nr; j0 += 16) {
+                        float gv[16], uv[16];
+                        if (ni == 4) {
+                            // accumulator of (slab g, sub-stage u) is column (2g + u) * BM
+                            tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, gv, uv);
+                            if (u1) {
+                                float g1[16], u1v[16];
+                                tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, g1,
+                                                         u1v);
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) {
-                                gv[jj] += g1[jj];
-                                uv[jj] += u1v[jj];
+                                for (int jj = 0; jj < 16; ++jj) {
+                                    gv[jj] += g1[jj];
+                                    uv[jj] += u1v[jj];
+                                }
+                            }
+                        } else {
+                            tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int jr = j0 + jj;
+                            if (jr < nr) {
+                                if (full) {
+                                    p.a_out[(size_t)(pos0 + jr) * p.I + feat] =
+                                        f16_sat(silu_mul(gv[jj], uv[jj]));
+                                } else {
+                                    sl[(size_t)jr * 128 + row] = gv[jj];
+                                    sl[(size_t)(BM + jr) * 128 + row] = uv[jj];
+                                }
                             }
                         }
-                    } else {
-                        tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
                     }
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int jr = j0 + jj;
-                        if (jr < nr) {
-                            if (full) {
-                                p.a_out[(size_t)(pos0 + jr) * p.I + feat] =
-                                    f16_sat(silu_mul(gv[jj], uv[jj]));
-                            } else {
-                                sl[(size_t)jr * 128 + row] = gv[jj];
-                                sl[(size_t)(BM + jr) * 128 + row] = uv[jj];
-                            }
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_acc_empty);
-                if (!full) {
-                    __threadfence();
-                    named_bar_sync(1, 128);
-                    if (row == 0) {
-                        const int len = kb1 - kb0;
-                        const int old = atomicAdd(&p.tile_cnt[tile], len);
-                        *bcast = (old + len == p.KS) ? 1 : 0;
-                    }
-                    named_bar_sync(1, 128);
-                    const bool last = *bcast != 0;
-                    named_bar_sync(1, 128);
-                    if (last) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty);
+                    if (!full) {
                         __threadfence();
-                        const long long ts = (long long)tile * p.KS, te = ts + p.KS;
-                        const int c_first = range_owner(T, sched.G, ts);
-                        const int c_last = range_owner(T, sched.G, te - 1);
-                        for (int jr = 0; jr < nr; ++jr) {
-                            float gs = 0.f, us = 0.f;
-                            for (int cc = c_first; cc <= c_last; ++cc) {
-                                const long long cs = range_start(T, sched.G, cc);
-                                if (range_start(T, sched.G, cc + 1) == cs) continue;  // empty
-                                const int sslot = (cs >= ts) ? 0 : 1;
-                                const float *ps =
-                                    p.partial + ((size_t)(cc * 2 + sslot) * 2) * BM * 128;
-                                gs += __ldcg(ps + (size_t)jr * 128 + row);
-                                us += __ldcg(ps + (size_t)(BM + jr) * 128 + row);
+                        named_bar_sync(kBarEpi, 128);
+                        if (row == 0) {
+                            const int len = kb1 - kb0;
+                            const int old = atomicAdd(&p.tile_cnt[tile], len);
+                            *bcast = (old + len == p.KS) ? 1 : 0;
+                        }
+                        named_bar_sync(kBarEpi, 128);
+                        const bool last = *bcast != 0;
+                        named_bar_sync(kBarEpi, 128);
+                        if (last) {
+                            __threadfence();
+                            const long long ts = (long long)tile * p.KS, te = ts + p.KS;
+                            const int c_first = range_owner(T, sched.G, ts);
+                            const int c_last = range_owner(T, sched.G, te - 1);
+                            for (int jr = 0; jr < nr; ++jr) {
+                                float gs = 0.f, us = 0.f;
+                                for (int cc = c_first; cc <= c_last; ++cc) {
+                                    const long long cs = range_start(T, sched.G, cc);
+                                    if (range_start(T, sched.G, cc + 1) == cs) continue;  // empty
+                                    const int sslot = (cs >= ts) ? 0 : 1;
+                                    const float *ps =
+                                        p.partial + ((size_t)(cc * 2 + sslot) * 2) * BM * 128;
+                                    gs += __ldcg(ps + (size_t)jr * 128 + row);
+                                    us += __ldcg(ps + (size_t)(BM + jr) * 128 + row);
+                                }
+                                p.a_out[(size_t)(pos0 + jr) * p.I + feat] =
+                                    f16_sat(silu_mul(gs, us));
                             }
-                            p.a_out[(size_t)(pos0 + jr) * p.I + feat] = f16_sat(silu_mul(gs, us));
                         }
                     }
+                } else {
+                    for (int j0 = 0; j0 < nr; j0 += 16) {
+                        float dv[16];
+                        if (ni == 4) {
+                            float d1[16];
+                            tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, dv, d1);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
+                            if (u1) {
+                                float d2[16], d3[16];
+                                tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, d2,
+                                                         d3);
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj) dv[jj] += d2[jj] + d3[jj];
+                            }
+                        } else {
+                            float d1[16];
+                            tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, dv, d1);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int jr = j0 + jj;
+                            if (jr < nr) {
+                                const int pair = p.sorted_ids[pos0 + jr];
+                                const int t = pair / p.top_k;
+                                atomicAdd(p.out_acc + (size_t)t * p.H + feat,
+                                          p.topk_weights[pair] * dv[jj]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty);
                 }
-            } else {
-                for (int j0 = 0; j0 < nr; j0 += 16) {
-                    float dv[16];
-                    if (ni == 4) {
-                        float d1[16];
-                        tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, dv, d1);
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
-                        if (u1) {
-                            float d2[16], d3[16];
-                            tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, d2, d3);
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) dv[jj] += d2[jj] + d3[jj];
-                        }
-                    } else {
-                        float d1[16];
-                        tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, dv, d1);
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int jr = j0 + jj;
-                        if (jr < nr) {
-                            const int pair = p.sorted_ids[pos0 + jr];
-                            const int t = pair / p.top_k;
-                            atomicAdd(p.out_acc + (size_t)t * p.H + feat,
-                                      p.topk_weights[pair] * dv[jj]);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_acc_empty);
             }
             ++c;
         }
         if (issuer) {  // every MMA of this CTA must finish before TMEM is released
             volatile int never = 0;
             tc_commit_elect(bar_drain);
-            warp_wait(bar_drain, 0, &never, nullptr);
+            warp_wait(bar_drain, 0, &never, nullptr, 32);
         }
     }
 
@@ -608,12 +572,12 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
     p.ni = (4 * BM + 2 * (int)kACols <= kTmemCols) ? 4 : 2;
     const int n_acc = (p.ni == 1 && kind == 1) ? 2 : p.ni;
     p.n_a = (kTmemCols - n_acc * BM) / (int)kACols;
-    if (p.n_a > 3) p.n_a = 3;
+    if (p.n_a > 3) p.n_a = 3;  // one named barrier per A stage (ids 2..4)
     if (p.n_a < 2) return false;
     const uint32_t limit = 227 * 1024 - 1024;  // opt-in maximum minus alignment slack
-    const uint32_t misc = 1024 + 16 + 4 * 128;  // barriers + words + loader table
+    const uint32_t misc = 1024 + 16;  // barriers + words
     int n_b = (BM <= 32) ? 8 : (BM <= 64) ? 4 : 3;
-    if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;
+    if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;  // down stages carry four k blocks
     p.n_b = n_b;
     const uint32_t b_bytes = (uint32_t)n_b * p.b_stage_bytes;
     int n_w = (int)((limit - b_bytes - misc) / kStage);
@@ -627,7 +591,7 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
     return p.smem_bytes <= 227u * 1024u;
 }
 
-cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_a, int grid,
+cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_b, int grid,
                         cudaStream_t s, int *launches) {
     static bool attr_done[64][2] = {};
     int dev = 0;
@@ -642,9 +606,9 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_a
         attr_done[dev][kind - 1] = true;
     }
     if (kind == 1)
-        moe_gemm_kernel<1><<<grid, kThreads, p.smem_bytes, s>>>(p, *tmap_a);
+        moe_gemm_kernel<1><<<grid, kThreads, p.smem_bytes, s>>>(p, *tmap_b);
     else
-        moe_gemm_kernel<2><<<grid, kThreads, p.smem_bytes, s>>>(p, *tmap_a);
+        moe_gemm_kernel<2><<<grid, kThreads, p.smem_bytes, s>>>(p, *tmap_b);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }

@@ -20,18 +20,17 @@ struct AlignArgs {
     int n_chunks;          // 0: single-block path
 };
 
-// Per-call preparation done by the align launch's spare blocks: zero two
-// regions and convert the bf16 activations to the fp16 tensor-core operand.
+// Per-call zeroing done by the align launch's spare blocks.
 struct ZeroArgs {
     void *ptr[2];
-    size_t n16[2];         // 16-byte units
-    const uint16_t *x_bf16;  // [n8 * 8] or null
-    uint16_t *x_f16;
-    size_t x_n8;           // 8-element units
+    size_t n16[2];  // 16-byte units
 };
 
 cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas, cudaStream_t s,
                          int *launches);
+cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const int32_t *npp, int P,
+                               int top_k, int H, uint16_t *xs, size_t cap_rows, int sms,
+                               cudaStream_t s, int *launches);
 cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, cudaStream_t s,
                             int *launches);
 cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
@@ -48,7 +47,6 @@ constexpr int kStageBytes = kStageWBytes + kStageSBytes;  // 9216
 struct GemmParams {
     const uint8_t *wq;         // packed INT4 stages
     const uint8_t *wsc;        // packed scales
-    const uint16_t *x;         // gate/up: fp16 activations [M][H]
     const int32_t *sorted_ids; // align output
     const int32_t *expert_ids;
     const int32_t *num_post_pad;
@@ -70,8 +68,10 @@ struct GemmParams {
     uint32_t smem_b_off, smem_misc_off, smem_bytes;
 };
 
-// kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine.
-cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_a, int grid,
+// kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine.  tmap_b
+// maps the B operand rows in bucketed order: fp16 x (gate/up) or the fp16
+// intermediate (down), 64-column x block_m-row boxes, 128-byte swizzle.
+cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_b, int grid,
                         cudaStream_t s, int *launches);
 // Fills the ring depths and shared-memory layout of p for the given kind.
 bool plan_gemm_smem(int kind, GemmParams &p);
