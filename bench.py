@@ -15,6 +15,7 @@ each rank runs an independent replica on its own GPU (the layer does not shard).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -38,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1)
@@ -50,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (a smaller case of the same kernels, for ncu captures)")
     return ap.parse_args()
 
 
@@ -99,6 +102,10 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
 
     def stop(self):
         if not self.proc:
@@ -221,7 +228,7 @@ def run_reference(args, cfg, Ms, world, rank):
     value = toks / secs
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
-        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": statistics.mean(step_ms), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "E": cfg.E, "top_k": cfg.top_k, "hidden": cfg.H,
@@ -416,7 +423,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": "f16", "data": "synthetic",
             "config": {"workload": cfg.name, "E": cfg.E, "top_k": cfg.top_k, "hidden": cfg.H,
                        "inter": cfg.I, "group": 32, "Ms": list(Ms),
                        "step": "one moe_int4_forward per M",
@@ -436,6 +443,8 @@ def run_ours(args, cfg, Ms, world, rank, local):
 def main():
     args = parse_args()
     cfg = inputs.CONFIGS[args.config]
+    if args.experts:
+        cfg = dataclasses.replace(cfg, E=args.experts, name=f"{cfg.name}_E{args.experts}")
     Ms = tuple(int(m) for m in args.ms.split(",")) if args.ms else cfg.Ms
     world, rank, local = dist_setup()
     if args.impl == "reference":
