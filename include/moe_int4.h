@@ -55,7 +55,8 @@ enum {
     MOE_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
     MOE_ERR_WORKSPACE = -4,   /* workspace too small */
     MOE_ERR_CUDA = -5,        /* a CUDA runtime call failed (launch, copy) */
-    MOE_ERR_UNSUPPORTED = -6  /* current device is not compute capability 10.3 */
+    MOE_ERR_UNSUPPORTED = -6, /* current device is not compute capability 10.3 */
+    MOE_ERR_NOALLOC_LIMIT = -7 /* too large for moe_align_noalloc's fixed scratch */
 };
 
 /* Device-side error flags (bit set), read with moe_int4_get_errors. */
@@ -149,6 +150,32 @@ int moe_align(const int32_t *topk_ids, int M, int top_k, int E, int block_m,
               int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
               uint32_t *err_flags, void *scratch, size_t scratch_bytes,
               moe_stream_t stream);
+
+/*
+ * moe_align_noalloc: moe_align for callers that cannot allocate device memory.
+ * (The pages have no counterpart: this entry point serves callers of this
+ * library, such as a plugin that a host runtime hands only its input and
+ * output buffers, or a latency-critical path where cudaMalloc/cudaFree may
+ * block or synchronise the device.)
+ * Same inputs, outputs and results as moe_align; the per-chunk scratch table
+ * comes from a fixed 1 MiB device array inside the library instead of the
+ * caller, held on every GPU that loads the library until the process exits.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * Limit: moe_align_scratch_bytes(M, top_k, E) <= 1 MiB (E = 384: up to
+ * 698,368 pairs; E = 1024: 262,144), else MOE_ERR_NOALLOC_LIMIT and nothing
+ * is launched.
+ * The first call on each device looks up the array's device address on the
+ * current device (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Nothing in the array needs to start at zero (each call
+ * writes every entry it reads), but all calls share it: calls whose kernels
+ * overlap on the GPU (different streams, or host threads) race and give wrong
+ * results; serialise them, e.g. on one stream.
+ * Errors: those of moe_align (MOE_ERR_WORKSPACE excepted), MOE_ERR_NOALLOC_LIMIT,
+ * MOE_ERR_UNSUPPORTED (device ordinal >= 64).
+ */
+int moe_align_noalloc(const int32_t *topk_ids, int M, int top_k, int E, int block_m,
+                      int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_post_pad,
+                      uint32_t *err_flags, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Forward                                                                    */

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe_int4.so")
-SOURCES = ["abi.cu", "align.cu", "pack.cu", "gemm.cu"]
+SOURCES = ["abi.cu", "align.cu", "pack.cu", "gemm.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -454,6 +454,7 @@ const char *moe_int4_strerror(int code) {
         case MOE_ERR_WORKSPACE: return "workspace too small";
         case MOE_ERR_CUDA: return "a CUDA runtime call failed";
         case MOE_ERR_UNSUPPORTED: return "device is not compute capability 10.3 (sm_103a)";
+        case MOE_ERR_NOALLOC_LIMIT: return "routing too large for moe_align_noalloc's 1 MiB scratch";
         default: return "unknown error code";
     }
 }

@@ -29,7 +29,7 @@ EXPORTED = [
     "moe_int4_forward",
     "moe_int4_forward_host", "moe_int4_get_errors", "moe_int4_clear_errors",
     "moe_int4_strerror", "moe_int4_profile_enable", "moe_int4_profile_read",
-    "moe_int4_last_launch_count",
+    "moe_int4_last_launch_count", "moe_align_noalloc",
 ]
 
 
@@ -83,6 +83,7 @@ def load_library(build_if_missing: bool = True):
             "moe_int4_profile_enable": ([i], i),
             "moe_int4_profile_read": ([p], i),
             "moe_int4_last_launch_count": ([], i),
+            "moe_align_noalloc": ([p, i, i, i, i, p, p, p, p, p], i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -170,6 +171,27 @@ def moe_align(topk_ids: torch.Tensor, E: int, block_m: int, stream=None):
     rc = lib.moe_align(_dptr(topk_ids), M, k, E, block_m, _dptr(sorted_ids), _dptr(expert_ids),
                        _dptr(npp), _dptr(err), _dptr(scratch), scratch_bytes, _stream(stream))
     _check(rc, "moe_align")
+    return sorted_ids, expert_ids, npp, err
+
+
+def moe_align_noalloc(topk_ids: torch.Tensor, E: int, block_m: int, out=None, stream=None):
+    """moe_align without caller scratch: the library's fixed device table is
+    used instead (limit: moe_align_scratch_bytes <= 1 MiB).  ``out`` may give
+    preallocated (sorted_ids, expert_ids, num_post_pad, err) buffers, so that
+    the call itself allocates nothing; otherwise they are created here."""
+    lib = load_library()
+    M, k = topk_ids.shape
+    if out is None:
+        cap = max(lib.moe_align_capacity(M, k, E, block_m), 1)
+        dev = topk_ids.device
+        out = (torch.empty(cap, dtype=torch.int32, device=dev),
+               torch.empty(cap // block_m + 1, dtype=torch.int32, device=dev),
+               torch.zeros(1, dtype=torch.int32, device=dev),
+               torch.zeros(2, dtype=torch.int32, device=dev))
+    sorted_ids, expert_ids, npp, err = out
+    rc = lib.moe_align_noalloc(_dptr(topk_ids), M, k, E, block_m, _dptr(sorted_ids),
+                               _dptr(expert_ids), _dptr(npp), _dptr(err), _stream(stream))
+    _check(rc, "moe_align_noalloc")
     return sorted_ids, expert_ids, npp, err
 
 
