@@ -71,6 +71,30 @@ def expert_bytes(H, I):
     return w13, w2
 
 
+GEMM_SOURCES = ("gemm.cu", "kernels.cuh", "common.cuh")
+
+
+def kernel_traffic(kernel, workload, bytes_per_launch):
+    """DRAM traffic per launch of `kernel`, from the committed ncu summary of a
+    smaller case of the same kernel, scaled by algorithmic bytes.  None when no
+    summary exists or the kernel's source changed since it was captured."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.json")
+    if not os.path.exists(path):
+        return None, "no ncu summary for this kernel and workload"
+    with open(path) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "weight_only_int4_moe_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != d.get("kernel_source_sha256"):
+        return None, "kernel changed since the ncu capture"
+    ratio = float(d["traffic_per_algorithmic_byte"])
+    return ratio * bytes_per_launch, (f"ncu dram bytes of {d['captured_case']}: "
+                                      f"{ratio:.4f} x algorithmic bytes, scaled")
+
+
 def host_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -362,16 +386,13 @@ def run_ours(args, cfg, Ms, world, rank, local):
         ach = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
     else:
         ach = sum(r["touched"] * w2_b for r in rec) / (sum(g2_ms) / 1e3) / 1e9
-    traffic = None
-    prof_json = os.path.join(ROOT, "profiles", f"{dominant}_{cfg.name}_traffic.json")
-    if os.path.exists(prof_json):
-        with open(prof_json) as f:
-            traffic = json.load(f).get("traffic_bytes_per_launch")
+    bytes_mean = statistics.mean(
+        g1_bytes if dominant == "gate_up" else [r["touched"] * w2_b for r in rec])
+    traffic, traffic_src = kernel_traffic(dominant, cfg.name, bytes_mean)
     roofline = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
                 "frac": ach / hbm_peak, "traffic": traffic, "kernel": dominant,
-                "peak_source": f"{peak_src} (hbm_gbs)",
-                "bytes_per_launch_mean": statistics.mean(
-                    g1_bytes if dominant == "gate_up" else [r["touched"] * w2_b for r in rec]),
+                "peak_source": f"{peak_src} (hbm_gbs)", "traffic_source": traffic_src,
+                "bytes_per_launch_mean": bytes_mean,
                 "launch_ms_mean": statistics.mean(g1_ms if dominant == "gate_up" else g2_ms)}
 
     # end to end through the host-buffer entry point
