@@ -102,6 +102,14 @@ struct Ring {
             ph ^= 1u;
         }
     }
+    // Moves k positions ahead (k >= 0; any number of laps).
+    MOE_DEV void advance(uint32_t k) {
+        idx += k;
+        while (idx >= n) {
+            idx -= n;
+            ph ^= 1u;
+        }
+    }
 };
 
 // ------------------------------------------------------------- async copies --

@@ -51,8 +51,10 @@ namespace {
 
 constexpr int kThreads = 768;
 constexpr int kTmemCols = 512;
-constexpr int kTeamWarps = 8;                   // dequant warps per team
-constexpr int kDequantWarps = 2 * kTeamWarps;  // two teams, alternate stages
+constexpr int kTeams = 4;                        // dequant teams, taking stages in turn
+static_assert((kTeams & (kTeams - 1)) == 0, "team index arithmetic uses a mask");
+constexpr int kTeamWarps = 4;                    // dequant warps per team (one per lane quadrant)
+constexpr int kDequantWarps = kTeams * kTeamWarps;
 constexpr int kFirstDequantWarp = 4;
 constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
 constexpr uint32_t kStageW = 2 * kStageWBytes;  // 16 KB of INT4 per stage
@@ -130,19 +132,34 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
+// Whole-warp wait for CTA stage `stage` in a weight-ring slot.  A team sees
+// only every fourth stage, so it does not follow every phase of a slot; a
+// parity match could be the phase two laps back if copies landed out of order.
+// The producer writes the stage index into the slot's tag before issuing its
+// copy, and it issues stage i only after stage i - n_w was consumed, so a
+// parity match together with a matching tag is the right phase.
+__device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity,
+                                           const volatile uint32_t *tag, uint32_t stage,
+                                           volatile int *abort, uint32_t *err) {
+    const long long t0 = clock64();
+#pragma unroll 1
+    while (true) {
+        if (!warp_wait(bar, parity, abort, err)) return false;
+        if (__all_sync(0xffffffffu, *tag == stage)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitTimeoutCycles) {
+            *abort = 1;
+            if (err) atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
 // Sub-stages of stage j of a tile with `kss` sub-stages (the last may hold one).
 __device__ __forceinline__ int stage_subs(int j, int kss) {
     return (2 * j + 2 <= kss) ? 2 : 1;
 }
 
-// fp16 pair (1024 + q_lo, 1024 + q_hi) from the nibbles at bits 0..3 and 16..19.
-__device__ __forceinline__ uint32_t magic_lo(uint32_t w) {
-    return (w & 0x000F000Fu) | 0x64006400u;
-}
-// fp16 pair (1024 + 16 q_lo, 1024 + 16 q_hi) from the nibbles at bits 4..7 and 20..23.
-__device__ __forceinline__ uint32_t magic_hi(uint32_t w) {
-    return (w & 0x00F000F0u) | 0x64006400u;
-}
 __device__ __forceinline__ __half2 as_h2(uint32_t v) {
     return *reinterpret_cast<const __half2 *>(&v);
 }
@@ -153,24 +170,27 @@ __device__ __forceinline__ uint32_t as_u32(__half2 h) {
 // One slab row of a sub-stage: 64 weights (k = 0..63 of the slab's k block) as
 // 32 fp16 pairs (q - 8) * s, out[c] holding k = 2c (low half) and 2c + 1 (high).
 // Word v holds k = 8v..8v+7: bits 4s and 16+4s are k = 8v+2s and 8v+2s+1.
-// The subtraction of 1032 (or the 1/16-scaled FMA with -72) is exact; the one
-// rounding is the final product with the fp16 scale (two per word `sc`).
+// (w & mask) | magic is the fp16 pair (1024 + q) (or 1024 + 16 q for the odd
+// nibble position); subtracting 1032 (or the FMA x/16 - 72) is exact, and the
+// one rounding is the final product with the fp16 scale (two per word `sc`).
 __device__ __forceinline__ void dequant_row(const uint4 lo, const uint4 hi, uint32_t sc,
-                                            uint32_t (&out)[32]) {
+                                            const DequantConsts &k, uint32_t (&out)[32]) {
     const __half2 s0 = as_h2(__byte_perm(sc, 0, 0x1010));  // group 0 scale, both halves
     const __half2 s1 = as_h2(__byte_perm(sc, 0, 0x3232));  // group 1 scale
-    const __half2 c1032 = as_h2(0x64086408u);  // 1032
-    const __half2 c16th = as_h2(0x2C002C00u);  // 1/16
-    const __half2 cm72 = as_h2(0xD480D480u);   // -72
+    const __half2 c1032 = as_h2(k.c1032);
+    const __half2 c16th = as_h2(k.c16th);
+    const __half2 cm72 = as_h2(k.cm72);
     const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
     for (int v = 0; v < 8; ++v) {
         const __half2 s2 = (v < 4) ? s0 : s1;
         const uint32_t w8 = w[v] >> 8;
-        out[4 * v + 0] = as_u32(__hmul2(__hsub2(as_h2(magic_lo(w[v])), c1032), s2));
-        out[4 * v + 1] = as_u32(__hmul2(__hfma2(as_h2(magic_hi(w[v])), c16th, cm72), s2));
-        out[4 * v + 2] = as_u32(__hmul2(__hsub2(as_h2(magic_lo(w8)), c1032), s2));
-        out[4 * v + 3] = as_u32(__hmul2(__hfma2(as_h2(magic_hi(w8)), c16th, cm72), s2));
+        out[4 * v + 0] = as_u32(__hmul2(__hsub2(as_h2((w[v] & k.mask_lo) | k.magic), c1032), s2));
+        out[4 * v + 1] =
+            as_u32(__hmul2(__hfma2(as_h2((w[v] & k.mask_hi) | k.magic), c16th, cm72), s2));
+        out[4 * v + 2] = as_u32(__hmul2(__hsub2(as_h2((w8 & k.mask_lo) | k.magic), c1032), s2));
+        out[4 * v + 3] =
+            as_u32(__hmul2(__hfma2(as_h2((w8 & k.mask_hi) | k.magic), c16th, cm72), s2));
     }
 }
 
@@ -208,8 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_w_empty = bar_w_full + 8 * n_w;
     const uint32_t bar_b_full = bar_w_empty + 8 * n_w;
     const uint32_t bar_b_empty = bar_b_full + 8 * n_b;
-    const uint32_t bar_a_empty = bar_b_empty + 8 * n_b;
-    const uint32_t bar_acc_full = bar_a_empty + 8 * n_a;
+    // a_free[t]: the A slot of team t's next stage is free (the MMAs of the
+    // stage n_a earlier, which used the same slot, are done)
+    const uint32_t bar_a_free = bar_b_empty + 8 * n_b;
+    const uint32_t bar_acc_full = bar_a_free + 8 * kTeams;
     const uint32_t bar_acc_empty = bar_acc_full + 8;
     const uint32_t bar_drain = bar_acc_empty + 8;
     const uint32_t misc_words = bar_drain + 8;  // tmem slot, abort flag, bcast
@@ -217,6 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc_ptr + 4);
     volatile int *bcast = reinterpret_cast<volatile int *>(misc_ptr + 8);
+    // stage tags of the weight ring: the CTA stage index last issued into each slot
+    volatile uint32_t *w_tag = reinterpret_cast<volatile uint32_t *>(smem + (misc - base) + 384);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_w; ++i) {
@@ -227,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_b_full + 8 * i, 1);
             mbar_init(bar_b_empty + 8 * i, ni);
         }
-        for (int i = 0; i < n_a; ++i) mbar_init(bar_a_empty + 8 * i, ni);
+        for (int i = 0; i < kTeams; ++i) mbar_init(bar_a_free + 8 * i, ni);
+        for (int i = 0; i < n_w; ++i) w_tag[i] = 0xFFFFFFFFu;
         mbar_init(bar_acc_full, ni);
         mbar_init(bar_acc_empty, 4);
         mbar_init(bar_drain, ni);
@@ -276,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t bytes = stage_subs(j, kss) * sub_bytes;
+                    if (!scales) w_tag[w.idx] = i;
                     mbar_arrive_expect_tx(bar_w_full + 8 * w.idx, bytes);
                     bulk_g2s(w_ring + w.idx * kStage + dst_off, src + (sub0 + 2 * j) * sub_bytes,
                              bytes, bar_w_full + 8 * w.idx, pol);
@@ -322,55 +348,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (wid >= kFirstDequantWarp && wid < kFirstEpilogueWarp) {
         // ------------------------------------------------------- dequant --
-        // Two teams of eight warps take alternate stages, so one team's waits
-        // overlap the other's arithmetic.  Warp 4 + 8t + 4g + q of team t
-        // dequantises rows 32q..32q+31 of slab g for both sub-stages.  Every
-        // stage of the team is visited even after an error (no work, but every
+        // Four teams of four warps take stages in turn (stage i: team i % 4),
+        // so a team's waits overlap the other teams' arithmetic.  Warp
+        // 4 + 4t + q of team t dequantises rows 32q..32q+31 (its tensor-memory
+        // lane quadrant) of both slabs and both sub-stages.  A team visits
+        // every one of its stages even after an error (no work, but every
         // barrier arrival still happens), so no named barrier can be left
         // waiting.
-        const int dw = wid - kFirstDequantWarp;
-        const int team = dw >> 3;
-        const int g = (dw >> 2) & 1;  // slab
+        const int team = (wid - kFirstDequantWarp) >> 2;
         const int q = wid & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint8_t *my_w = smem + g * kSlabBytes + row * 16;
-        const uint8_t *my_s = smem + kStageW + g * 512 + row * 4;
-        const uint32_t my_t = tmem + lane_off + col_a + g * 32;
+        const uint8_t *my_w = smem + row * 16;
+        const uint8_t *my_s = smem + kStageW + row * 4;
+        const uint32_t my_t = tmem + lane_off + col_a;
         const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
+        const DequantConsts dqc = p.dq;
         volatile int no_abort = 0;
-        Ring w(n_w), a(n_a);
-        uint32_t si = 0;  // stage counter of this CTA
+        Ring w(n_w), a(n_a);  // a: the A slot only (its phase is not used)
+        w.advance(team);
+        a.advance(team);
+        uint32_t a_ph = 0;    // parity of this team's next a_free phase
+        long long s0 = 0;           // CTA stage index of the current piece's first stage
+        long long own = team;       // next stage of this team
         bool ok = true;
         while (pi.next(sched, tile, kb0, kb1)) {
-            for (int j = kb0; j < kb1; ++j, w.next(), a.next(), ++si) {
-                if ((si & 1u) != (uint32_t)team) continue;  // the other team's stage
-                if (ok) ok = warp_wait(bar_w_full + 8 * w.idx, w.ph, abort_flag, p.err);
+            const long long s1 = s0 + (kb1 - kb0);
+            for (; own < s1; own += kTeams, w.advance(kTeams), a.advance(kTeams)) {
+                const int j = kb0 + (int)(own - s0);
+                if (ok)
+                    ok = wait_stage(bar_w_full + 8 * w.idx, w.ph, w_tag + w.idx, (uint32_t)own,
+                                    abort_flag, p.err);
                 const int nsub = ok ? stage_subs(j, kss) : 0;
-                // The A slot is reused only once the issuers' MMAs on it are done.
+                // The A slot is reused only once the MMAs of the stage n_a
+                // earlier (which used it) are done; the issuers signal that on
+                // this team's own barrier, whose phases follow the team's stages
+                // in order, so a parity wait is never more than one phase behind.
                 // This wait happens even after an error: it keeps this warp from
                 // arriving on the slot's named barrier again before the issuers
                 // have consumed the previous arrival.
-                const bool freed = warp_wait(bar_a_empty + 8 * a.idx, a.ph ^ 1, &no_abort, p.err);
-                if (!freed) ok = false;
+                if (own >= n_a) {
+                    const bool freed = warp_wait(bar_a_free + 8 * team, a_ph, &no_abort, p.err);
+                    a_ph ^= 1u;
+                    if (!freed) ok = false;
+                }
+                const uint8_t *sw = my_w + w.idx * kStage;
+                const uint8_t *ss = my_s + w.idx * kStage;
+                const uint32_t st = my_t + a.idx * kACols;
                 for (int uu = 0; uu < nsub && ok; ++uu) {
-                    const uint8_t *sw = my_w + (size_t)w.idx * kStage + uu * kStageWBytes;
-                    const uint4 lo = *reinterpret_cast<const uint4 *>(sw);
-                    const uint4 hi = *reinterpret_cast<const uint4 *>(sw + 2048);
-                    const uint32_t sc = *reinterpret_cast<const uint32_t *>(
-                        my_s + (size_t)w.idx * kStage + uu * kStageSBytes);
-                    if (uu == nsub - 1) {  // every load of this stage is done
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        const uint8_t *src = sw + uu * kStageWBytes + g * kSlabBytes;
+                        const uint4 lo = *reinterpret_cast<const uint4 *>(src);
+                        const uint4 hi = *reinterpret_cast<const uint4 *>(src + 2048);
+                        const uint32_t sc =
+                            *reinterpret_cast<const uint32_t *>(ss + uu * kStageSBytes + g * 512);
+                        if (g == 1 && uu == nsub - 1) {  // every load of this stage is done
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
+                        }
+                        uint32_t v[32];
+                        dequant_row(lo, hi, sc, dqc, v);
+                        tc_fence_after();
+                        tmem_st_32x32b_x32_wait(st + uu * 64 + g * 32, v);
                     }
-                    uint32_t v[32];
-                    dequant_row(lo, hi, sc, v);
-                    tc_fence_after();
-                    tmem_st_32x32b_x32_wait(my_t + a.idx * kACols + uu * 64, v);
                 }
                 tc_fence_before();
                 named_bar_arrive(kBarSlot0 + a.idx, slot_cnt);  // A stage written
             }
+            s0 = s1;
         }
     } else if (wid >= kFirstEpilogueWarp) {
         // -------------------------------------------- MMA issue + epilogue --
@@ -389,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
         const long long T = (long long)sched.tiles * sched.KS;
         Ring a(n_a), bq(n_b);
+        uint32_t next_team = (uint32_t)(n_a % kTeams);  // team of stage (CTA stage + n_a)
         uint32_t c = 0;
         bool ok = true;
         while (pi.next(sched, tile, kb0, kb1)) {
@@ -400,7 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc = idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
                 bool fresh = true;
                 if (ok) ok = warp_wait(bar_acc_empty, (c & 1) ^ 1, abort_flag, p.err, 32);
-                for (int j = kb0; j < kb1; ++j, a.next(), bq.next()) {
+                for (int j = kb0; j < kb1; ++j, a.next(), bq.next(),
+                                         next_team = (next_team + 1) & (kTeams - 1)) {
                     named_bar_sync(kBarSlot0 + a.idx, slot_cnt);  // the stage's A is in TMEM
                     if (ok) ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
                     if (ok) {
@@ -420,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    tc_commit_elect(bar_a_empty + 8 * a.idx);
+                    tc_commit_elect(bar_a_free + 8 * next_team);
                     tc_commit_elect(bar_b_empty + 8 * bq.idx);
                 }
                 tc_commit_elect(bar_acc_full);
@@ -563,6 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 bool plan_gemm_smem(int kind, GemmParams &p) {
+    p.dq.mask_lo = 0x000F000Fu;
+    p.dq.mask_hi = 0x00F000F0u;
+    p.dq.magic = 0x64006400u;  // fp16 1024 in both halves
+    p.dq.c1032 = 0x64086408u;  // fp16 1032
+    p.dq.c16th = 0x2C002C00u;  // fp16 1/16
+    p.dq.cm72 = 0xD480D480u;   // fp16 -72
     const int BM = p.block_m;
     if (BM < 16 || BM % 16 != 0 || BM > 128) return false;
     // k blocks per B stage: gate/up two 64-wide blocks, down four

@@ -44,6 +44,16 @@ constexpr int kStageWBytes = 2 * kSlabBytes;            // 8192
 constexpr int kStageSBytes = 2 * kSlabRows * 2 * 2;     // 1024
 constexpr int kStageBytes = kStageWBytes + kStageSBytes;  // 9216
 
+// Dequantisation constants (fp16 pairs and nibble masks), passed as kernel
+// parameters so that they stay constant-bank operands instead of immediates
+// the compiler re-materialises in registers for every use.
+struct DequantConsts {
+    uint32_t mask_lo, mask_hi;  // nibble masks 0x000F000F, 0x00F000F0
+    uint32_t magic;             // fp16 pair (1024, 1024): 0x6400 exponent bits
+    uint32_t c1032;             // fp16 pair 1032 = 1024 + 8
+    uint32_t c16th, cm72;       // fp16 pairs 1/16 and -72 (high nibble: x/16 - 72)
+};
+
 struct GemmParams {
     const uint8_t *wq;         // packed INT4 stages
     const uint8_t *wsc;        // packed scales
@@ -66,6 +76,7 @@ struct GemmParams {
     int split;                 // 1: partition k iterations evenly over CTAs
     uint32_t b_stage_bytes;
     uint32_t smem_b_off, smem_misc_off, smem_bytes;
+    DequantConsts dq;
 };
 
 // kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine.  tmap_b
