@@ -45,8 +45,11 @@ MOE_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
                  "r"(bytes)
                  : "memory");
 }
-// try_wait suspends the thread until the phase completes or kSuspendHintNs
-// passes, so a waiting warp does not spin on the issue slots.
+// try_wait with a suspend-time hint suspends the thread until the phase
+// completes or kSuspendHintNs passes, so a waiting warp does not spin on the
+// issue slots; but each call costs ~50 cycles alone and ~180 cycles on an SM
+// sub-partition busy with other warps, even when the phase is already complete.
+// Waits therefore test first without the hint and suspend only after that.
 constexpr uint32_t kSuspendHintNs = 20000;
 
 MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -60,14 +63,27 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+MOE_DEV bool mbar_try_wait_nohint(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
-// Bounded wait on the phase with the given parity.  Polls try_wait; after a
-// few polls it sleeps `backoff_ns` between polls (0: keep polling, for waits on
-// the critical path) and only then starts reading the cycle counter.  Returns
-// false (and records the timeout) if the wait gives up or another role of the
-// CTA already aborted.
+// Bounded wait on the phase with the given parity: one test without the
+// suspend hint (the common, already-complete case), then a few suspending
+// polls; after that it sleeps `backoff_ns` between polls (0: keep polling, for
+// waits on the critical path) and only then starts reading the cycle counter.
+// Returns false (and records the timeout) if the wait gives up or another role
+// of the CTA already aborted.
 MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint32_t *err,
                        uint32_t backoff_ns = 0) {
+    if (mbar_try_wait_nohint(bar, parity)) return true;
 #pragma unroll 1
     for (int it = 0; it < 8; ++it)
         if (mbar_try_wait(bar, parity)) return true;
@@ -234,6 +250,49 @@ MOE_DEV void tc_commit_elect(uint32_t bar) {
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
             bar)
+        : "memory");
+}
+
+// Four kind::f16 MMAs along K (K = 16 each: A columns +8, B descriptor start
+// +32 bytes) from one elected thread, then commits to bar1 and bar2 (each only
+// if non-zero).  One elect and one instruction block per 64-wide k step keeps
+// the issuing warp's instruction stream short while it shares its SM
+// sub-partition with busy dequantising warps.  The first MMA accumulates iff
+// `accumulate`.
+MOE_DEV void mma_ts_f16_k64_commit(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                   uint32_t idesc, uint32_t accumulate, uint32_t bar1,
+                                   uint32_t bar2) {
+    asm volatile(
+        "{\n\t.reg .pred p, t, e, c;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, %4, %4;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+        "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+        "setp.ne.and.b32 c, %5, 0, e;\n\t"
+        "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+        "setp.ne.and.b32 c, %6, 0, e;\n\t"
+        "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar1), "r"(bar2)
+        : "memory");
+}
+
+// Commits to bar1 and bar2 (each only if non-zero) from one elected thread.
+MOE_DEV void tc_commit2_elect(uint32_t bar1, uint32_t bar2) {
+    asm volatile(
+        "{\n\t.reg .pred e, c;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.and.b32 c, %0, 0, e;\n\t"
+        "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+        "setp.ne.and.b32 c, %1, 0, e;\n\t"
+        "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(
+            bar1),
+        "r"(bar2)
         : "memory");
 }
 

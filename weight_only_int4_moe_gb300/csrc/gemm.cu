@@ -460,16 +460,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int uu = iu_lo; uu < uhi; ++uu) {
                             const uint32_t sub = (KIND == 1) ? (uint32_t)uu : (uint32_t)(2 * uu + ig);
                             const uint64_t bd = smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                mma_ts_f16_elect(acc_col, a_st + uu * 64 + ig * 32 + 8 * k,
-                                                 bd + 2 * k, idesc, fresh ? 0u : 1u);
-                                fresh = false;
-                            }
+                            // the last block of the stage releases its A slot (to the
+                            // team that uses it next) and its B stage
+                            const bool last = (uu == uhi - 1);
+                            mma_ts_f16_k64_commit(acc_col, a_st + uu * 64 + ig * 32, bd, idesc,
+                                                  fresh ? 0u : 1u,
+                                                  last ? bar_a_free + 8 * next_team : 0u,
+                                                  last ? bar_b_empty + 8 * bq.idx : 0u);
+                            fresh = false;
                         }
+                        if (uhi <= iu_lo)  // no MMA of this issuer in the stage
+                            tc_commit2_elect(bar_a_free + 8 * next_team, bar_b_empty + 8 * bq.idx);
+                    } else {
+                        tc_commit2_elect(bar_a_free + 8 * next_team, bar_b_empty + 8 * bq.idx);
                     }
-                    tc_commit_elect(bar_a_free + 8 * next_team);
-                    tc_commit_elect(bar_b_empty + 8 * bq.idx);
                 }
                 tc_commit_elect(bar_acc_full);
             }
