@@ -200,8 +200,11 @@ __device__ __forceinline__ uint16_t f16_sat(float v) {
     return __half_as_ushort(__float2half_rn(v));
 }
 
+// SiLU(g) * u = g / (1 + e^-g) * u.  The fast divide is within a few ulp of
+// the IEEE one (its result is rounded to fp16 next) and gives g * 0 = -0 when
+// e^-g overflows for very negative g.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return g / (1.0f + __expf(-g)) * u;
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 }  // namespace
@@ -241,6 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *bcast = reinterpret_cast<volatile int *>(misc_ptr + 8);
     // stage tags of the weight ring: the CTA stage index last issued into each slot
     volatile uint32_t *w_tag = reinterpret_cast<volatile uint32_t *>(smem + (misc - base) + 384);
+    // down epilogue: (token, routing weight) of each column of the current block
+    int2 *col_tab = reinterpret_cast<int2 *>(smem + (misc - base) + 1024);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_w; ++i) {
@@ -442,6 +447,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b = tile / p.RT, r = tile % p.RT;
             const int pos0 = b * BM;
             const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
+            if (KIND == 2) {
+                // The combine needs each column's token and routing weight: look
+                // them up once per block here (the loads overlap the piece's MMAs)
+                // instead of as a dependent chain of global loads per column in the
+                // epilogue.  The epilogue's first barrier orders these writes.
+                if (row < nr) {
+                    const int pair = p.sorted_ids[pos0 + row];
+                    col_tab[row] = make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
+                }
+            }
             // ---- issue (every stage is visited, see the dequant role)
             if (issuer) {
                 const uint32_t idesc = idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
@@ -586,16 +601,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int jj = 0; jj < 16; ++jj) {
                             const int jr = j0 + jj;
                             if (jr < nr) {
-                                const int pair = p.sorted_ids[pos0 + jr];
-                                const int t = pair / p.top_k;
-                                atomicAdd(p.out_acc + (size_t)t * p.H + feat,
-                                          p.topk_weights[pair] * dv[jj]);
+                                const int2 tw = col_tab[jr];
+                                atomicAdd(p.out_acc + (size_t)tw.x * p.H + feat,
+                                          __int_as_float(tw.y) * dv[jj]);
                             }
                         }
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty);
+                    // every warp is done with the column table before any warp
+                    // writes the next block's
+                    named_bar_sync(kBarEpi, 128);
                 }
             }
             ++c;
@@ -633,7 +650,7 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
     if (p.n_a > 3) p.n_a = 3;  // one named barrier per A stage (ids 2..4)
     if (p.n_a < 2) return false;
     const uint32_t limit = 227 * 1024 - 1024;  // opt-in maximum minus alignment slack
-    const uint32_t misc = 1024 + 16;  // barriers + words
+    const uint32_t misc = 1024 + 16 + 128 * 8;  // barriers + words + column table
     int n_b = (BM <= 32) ? 8 : (BM <= 64) ? 4 : 3;
     if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;  // down stages carry four k blocks
     p.n_b = n_b;
