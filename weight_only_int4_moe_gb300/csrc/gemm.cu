@@ -12,35 +12,37 @@
 //    real row count rounded up to 16), so a decode call with one token per expert
 //    streams each touched weight once and wastes no weight traffic.
 //  * A pipeline stage is two k sub-stages of two 128x64 INT4 slabs each (16 KB,
-//    plus 2 KB of bf16 scales), stored contiguously by the pack step.  Two
+//    plus 2 KB of fp16 scales), stored contiguously by the pack step.  Two
 //    producer threads fetch a stage with one bulk TMA copy each (weights and
 //    scales), so the weight stream reaches HBM speed with few, large requests.
-//  * Two teams of eight dequant warps (alternate stages) each turn one slab row
-//    of both sub-stages into 128 fp16 weights (q-8)*s -- a mask/OR into an fp16 with
+//  * Three teams of four dequant warps take stages in turn; each warp covers
+//    its 32-row lane quadrant of both slabs and both sub-stages, turning the
+//    packed words into fp16 weights (q-8)*s -- a mask/OR into an fp16 with
 //    exponent 2^10, an exact subtraction (or 1/16-scaled FMA for the high
 //    nibble), one multiply by the scale; two weights per instruction -- and
-//    store them into tensor memory, which tcgen05.mma reads as its A operand.
+//    storing them into tensor memory, which tcgen05.mma reads as its A operand.
 //  * The B operand (fp16 activations) sits in shared memory in the 128-byte-
 //    swizzled K-major layout, fetched by 2-D TMA tensor copies of rows in
 //    bucketed order: x gathered once per call into that order (gate/up), the
 //    intermediate (down).
-//  * Accumulators live in tensor memory.  gate/up keeps the gate and up rows of
-//    the same 128 intermediate features in the same lanes (two accumulators), so
-//    the epilogue forms SiLU(g)*u in registers and writes the fp16 intermediate.
-//    The down epilogue scales by the routing weight and adds into the fp32
-//    [M][H] output (the top-k combine).
+//  * Accumulators live in tensor memory, in two alternating buffers where it
+//    has room, so the MMAs of the next piece run while dedicated epilogue warps
+//    read the previous one.  gate/up keeps the gate and up rows of the same
+//    128 intermediate features in the same lanes, so the epilogue forms
+//    SiLU(g)*u in registers and writes the fp16 intermediate.  The down
+//    epilogue scales by the routing weight and adds into the fp32 [M][H]
+//    output (the top-k combine).
 //  * Work = (expert block, 128-row tile) x stages, split evenly over a persistent
 //    grid of one CTA per SM (a CTA's range may cut a tile).  A gate/up tile cut
 //    between CTAs is finished by whichever piece arrives last (partial sums in
 //    per-CTA slots + a counter); no CTA ever waits for another.
 //
 // Warp roles (768 threads): 0 weight producer, 1 TMEM owner, 2 B loader,
-// 3 scale producer, 4-19 dequant (two teams of eight taking alternate stages;
-// in a team, slab 0: 4 warps, slab 1: 4 warps, each both sub-stages of its 32
-// rows), 20-23 MMA issue + epilogue.  A thread issuing tcgen05.mma waits ~90 cycles per
-// instruction while MMAs from several warps overlap, so each (slab, sub-stage) has
-// its own issuing warp and accumulator (the epilogue sums them).  Every wait is
-// bounded (MOE_DEVERR_TIMEOUT).
+// 3 scale producer, 4-15 dequant (three teams), 16-19 MMA issue, 20-23
+// epilogue.  Each (slab, sub-stage) has its own issuing warp and accumulator
+// (the epilogue sums them): one thread issuing tcgen05.mma waits tens of
+// cycles per instruction while MMAs from several warps overlap.  Every
+// mbarrier wait is bounded (MOE_DEVERR_TIMEOUT).
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
@@ -51,18 +53,19 @@ namespace {
 
 constexpr int kThreads = 768;
 constexpr int kTmemCols = 512;
-constexpr int kTeams = 4;                        // dequant teams, taking stages in turn
-static_assert((kTeams & (kTeams - 1)) == 0, "team index arithmetic uses a mask");
+constexpr int kTeams = 3;                        // dequant teams, taking stages in turn
 constexpr int kTeamWarps = 4;                    // dequant warps per team (one per lane quadrant)
 constexpr int kDequantWarps = kTeams * kTeamWarps;
 constexpr int kFirstDequantWarp = 4;
-constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
+constexpr int kFirstIssuerWarp = kFirstDequantWarp + kDequantWarps;  // 16..19: MMA issue
+constexpr int kFirstEpilogueWarp = kFirstIssuerWarp + 4;             // 20..23: epilogue
+static_assert(kFirstEpilogueWarp + 4 == kThreads / 32, "warp roles fill the block");
 constexpr uint32_t kStageW = 2 * kStageWBytes;  // 16 KB of INT4 per stage
 constexpr uint32_t kStageS = 2 * kStageSBytes;  // 2 KB of scales per stage
 constexpr uint32_t kStage = kStageW + kStageS;  // 18 KB
 constexpr uint32_t kACols = 128;                // TMEM columns per A stage
 // hardware named barriers (0 is __syncthreads)
-constexpr uint32_t kBarEpi = 1;     // the four issue/epilogue warps
+constexpr uint32_t kBarEpi = 1;     // the four epilogue warps
 constexpr uint32_t kBarSlot0 = 2;   // A stage s written: all dequant warps arrive, issuers wait
 
 struct Sched {
@@ -234,9 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a_free[t]: the A slot of team t's next stage is free (the MMAs of the
     // stage n_a earlier, which used the same slot, are done)
     const uint32_t bar_a_free = bar_b_empty + 8 * n_b;
+    // acc_full[b] / acc_empty[b]: accumulator buffer b holds a finished piece /
+    // has been read by the epilogue (buffers alternate between pieces)
     const uint32_t bar_acc_full = bar_a_free + 8 * kTeams;
-    const uint32_t bar_acc_empty = bar_acc_full + 8;
-    const uint32_t bar_drain = bar_acc_empty + 8;
+    const uint32_t bar_acc_empty = bar_acc_full + 16;
+    const uint32_t bar_drain = bar_acc_empty + 16;
     const uint32_t misc_words = bar_drain + 8;  // tmem slot, abort flag, bcast
     uint8_t *misc_ptr = smem + (misc_words - base);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(misc_ptr);
@@ -258,8 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kTeams; ++i) mbar_init(bar_a_free + 8 * i, ni);
         for (int i = 0; i < n_w; ++i) w_tag[i] = 0xFFFFFFFFu;
-        mbar_init(bar_acc_full, ni);
-        mbar_init(bar_acc_empty, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_acc_full + 8 * i, ni);
+            mbar_init(bar_acc_empty + 8 * i, 4);
+        }
         mbar_init(bar_drain, ni);
         *abort_flag = 0;
         mbar_fence_init();
@@ -273,12 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Tensor-memory column map: accumulators first, then the A ring.
-    // Accumulator of dequant group (slab g, sub-stage u): (ni == 4 ? 2g + u : g) * BM.
-    // gate/up: slab 0 feeds the gate accumulator(s), slab 1 the up accumulator(s).
-    // accumulators: one per issuer, but a single gate/up issuer keeps two
-    const int n_acc = (ni == 1 && KIND == 1) ? 2 : ni;
-    const uint32_t col_a = (uint32_t)(n_acc * BM);  // A ring: n_a stages x 128 columns
+    // Tensor-memory column map: nbuf accumulator buffers of ni accumulators
+    // (BM columns each), then the A ring of n_a stages x 128 columns.
+    // Accumulator of (slab g, sub-stage u): (ni == 4 ? 2g + u : g) within its
+    // buffer; gate/up: slab 0 feeds the gate accumulator(s), slab 1 the up ones.
+    const int nbuf = p.nbuf;
+    const uint32_t acc_buf_cols = (uint32_t)(ni * BM);
+    const uint32_t col_a = (uint32_t)nbuf * acc_buf_cols;
 
     const Sched sched = make_sched(p);
     PieceIter pi;
@@ -351,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(bar_b_full + 8 * (jj % n_b), (jj / n_b) & 1, &never, nullptr, 64);
             }
         }
-    } else if (wid >= kFirstDequantWarp && wid < kFirstEpilogueWarp) {
+    } else if (wid >= kFirstDequantWarp && wid < kFirstIssuerWarp) {
         // ------------------------------------------------------- dequant --
-        // Four teams of four warps take stages in turn (stage i: team i % 4),
+        // Three teams of four warps take stages in turn (stage i: team i % 3),
         // so a team's waits overlap the other teams' arithmetic.  Warp
         // 4 + 4t + q of team t dequantises rows 32q..32q+31 (its tensor-memory
         // lane quadrant) of both slabs and both sub-stages.  A team visits
@@ -423,22 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             s0 = s1;
         }
-    } else if (wid >= kFirstEpilogueWarp) {
-        // -------------------------------------------- MMA issue + epilogue --
-        // Warp 20 + qe issues the MMAs of sub-tile qe (slab qe & 1,
+    } else if (wid >= kFirstIssuerWarp && wid < kFirstEpilogueWarp) {
+        // ------------------------------------------------------- MMA issue --
+        // Warp 16 + qe issues the MMAs of sub-tile qe (slab qe & 1,
         // sub-stage qe >> 1) into its own accumulator; with two issuers, warps
-        // 20 and 21 each cover both sub-stages of slab 0 / 1.  At the end of a
-        // piece all four warps read the accumulators for their 32 TMEM lanes.
-        const int qe = wid & 3;
-        const int row = qe * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(qe * 32) << 16;
+        // 16 and 17 each cover both sub-stages of slab 0 / 1.  A piece goes to
+        // accumulator buffer c % nbuf, so with two buffers the next piece's
+        // MMAs run while the epilogue warps read the previous one.
+        const int qe = wid - kFirstIssuerWarp;
         const bool issuer = (ni == 4) || (qe < 2);
         const int ig = qe & 1;                        // slab of this issuer
         const int iu_lo = (ni == 4) ? (qe >> 1) : 0;  // sub-stages of this issuer
         const int iu_hi = (ni == 4) ? (qe >> 1) + 1 : 2;
-        const uint32_t acc_col = tmem + (uint32_t)(((ni == 4) ? 2 * ig + (qe >> 1) : ig) * BM);
+        const uint32_t acc_off = (uint32_t)(((ni == 4) ? 2 * ig + (qe >> 1) : ig) * BM);
         const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
-        const long long T = (long long)sched.tiles * sched.KS;
         Ring a(n_a), bq(n_b);
         uint32_t next_team = (uint32_t)(n_a % kTeams);  // team of stage (CTA stage + n_a)
         uint32_t c = 0;
@@ -447,23 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b = tile / p.RT, r = tile % p.RT;
             const int pos0 = b * BM;
             const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
-            if (KIND == 2) {
-                // The combine needs each column's token and routing weight: look
-                // them up once per block here (the loads overlap the piece's MMAs)
-                // instead of as a dependent chain of global loads per column in the
-                // epilogue.  The epilogue's first barrier orders these writes.
-                if (row < nr) {
-                    const int pair = p.sorted_ids[pos0 + row];
-                    col_tab[row] = make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
-                }
-            }
             // ---- issue (every stage is visited, see the dequant role)
             if (issuer) {
                 const uint32_t idesc = idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
+                const uint32_t buf = c % (uint32_t)nbuf;
+                const uint32_t acc_col = tmem + buf * acc_buf_cols + acc_off;
                 bool fresh = true;
-                if (ok) ok = warp_wait(bar_acc_empty, (c & 1) ^ 1, abort_flag, p.err, 32);
+                if (ok)
+                    ok = warp_wait(bar_acc_empty + 8 * buf, ((c / nbuf) & 1) ^ 1, abort_flag,
+                                   p.err, 32);
                 for (int j = kb0; j < kb1; ++j, a.next(), bq.next(),
-                                         next_team = (next_team + 1) & (kTeams - 1)) {
+                         next_team = (next_team + 1 == (uint32_t)kTeams) ? 0u : next_team + 1) {
                     named_bar_sync(kBarSlot0 + a.idx, slot_cnt);  // the stage's A is in TMEM
                     if (ok) ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
                     if (ok) {
@@ -490,17 +490,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_commit2_elect(bar_a_free + 8 * next_team, bar_b_empty + 8 * bq.idx);
                     }
                 }
-                tc_commit_elect(bar_acc_full);
+                tc_commit_elect(bar_acc_full + 8 * buf);
             }
-            // ---- epilogue (all four warps)
+            ++c;
+        }
+        if (issuer) {  // every MMA of this CTA must finish before TMEM is released
+            volatile int never = 0;
+            tc_commit_elect(bar_drain);
+            warp_wait(bar_drain, 0, &never, nullptr, 32);
+        }
+    } else if (wid >= kFirstEpilogueWarp) {
+        // -------------------------------------------------------- epilogue --
+        // At the end of each piece the four warps (lane quadrants 0..3) read the
+        // accumulators of its buffer for their 32 TMEM lanes.
+        const int q = wid & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const long long T = (long long)sched.tiles * sched.KS;
+        uint32_t c = 0;
+        bool ok = true;
+        while (pi.next(sched, tile, kb0, kb1)) {
+            const int b = tile / p.RT, r = tile % p.RT;
+            const int pos0 = b * BM;
+            const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
+            const uint32_t buf = c % (uint32_t)nbuf;
+            if (KIND == 2) {
+                // The combine needs each column's token and routing weight: look
+                // them up once per block (these loads overlap the wait for the
+                // piece's MMAs) instead of as a dependent chain of global loads per
+                // column.  The barrier below orders these writes before the reads.
+                if (row < nr) {
+                    const int pair = p.sorted_ids[pos0 + row];
+                    col_tab[row] = make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
+                }
+            }
             const bool u1 = !(kb1 - kb0 == 1 && stage_subs(kb0, p.KSS) == 1);
-            const bool got = ok && warp_wait(bar_acc_full, c & 1, abort_flag, p.err, 32);
+            const bool got =
+                ok && warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag, p.err, 32);
             // the four warps decide together (they share named barrier 1)
             if (named_bar_or(kBarEpi, 128, !got)) ok = false;
             if (ok) {
                 tc_fence_after();
                 const int feat = r * kSlabRows + row;
-                const uint32_t tl = tmem + lane_off;
+                const uint32_t tl = tmem + lane_off + buf * acc_buf_cols;
                 if (KIND == 1) {
                     const bool full = (kb0 == 0 && kb1 == p.KS);
                     float *sl = nullptr;
@@ -543,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty);
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
                     if (!full) {
                         __threadfence();
                         named_bar_sync(kBarEpi, 128);
@@ -609,18 +641,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty);
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
                     // every warp is done with the column table before any warp
                     // writes the next block's
                     named_bar_sync(kBarEpi, 128);
                 }
             }
             ++c;
-        }
-        if (issuer) {  // every MMA of this CTA must finish before TMEM is released
-            volatile int never = 0;
-            tc_commit_elect(bar_drain);
-            warp_wait(bar_drain, 0, &never, nullptr, 32);
         }
     }
 
@@ -642,12 +669,21 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
     if (BM < 16 || BM % 16 != 0 || BM > 128) return false;
     // k blocks per B stage: gate/up two 64-wide blocks, down four
     p.b_stage_bytes = (uint32_t)((kind == 1 ? 2 : 4) * BM * 128);
-    // four MMA issuers (one accumulator each) while tensor memory allows two A
-    // stages next to them; else two
-    p.ni = (4 * BM + 2 * (int)kACols <= kTmemCols) ? 4 : 2;
-    const int n_acc = (p.ni == 1 && kind == 1) ? 2 : p.ni;
-    p.n_a = (kTmemCols - n_acc * BM) / (int)kACols;
-    if (p.n_a > 3) p.n_a = 3;  // one named barrier per A stage (ids 2..4)
+    // MMA issuers (one accumulator each) and accumulator buffers: four issuers
+    // and two buffers where tensor memory still leaves two A stages, else two
+    // issuers with two buffers, else a single buffer (the issuers then wait for
+    // the epilogue at every piece end)
+    p.ni = 0;
+    const int opts[4][2] = {{4, 2}, {2, 2}, {4, 1}, {2, 1}};
+    for (int o = 0; o < 4 && !p.ni; ++o)
+        if (opts[o][0] * opts[o][1] * BM + 2 * (int)kACols <= kTmemCols) {
+            p.ni = opts[o][0];
+            p.nbuf = opts[o][1];
+        }
+    if (!p.ni) return false;
+    p.n_a = (kTmemCols - p.nbuf * p.ni * BM) / (int)kACols;
+    if (p.n_a > 3) p.n_a = 3;            // one named barrier per A stage (ids 2..4)
+    if (p.n_a > kTeams) p.n_a = kTeams;  // a team's A-slot barrier stays within one phase
     if (p.n_a < 2) return false;
     const uint32_t limit = 227 * 1024 - 1024;  // opt-in maximum minus alignment slack
     const uint32_t misc = 1024 + 16 + 128 * 8;  // barriers + words + column table

@@ -72,7 +72,8 @@ struct GemmParams {
     int KSS, KS;               // k sub-stages per tile (one 8 KB packed stage each) and
                                // pipeline stages per tile (two sub-stages, the last maybe one)
     int n_w, n_b, n_a;         // ring depths: weight stages, B stages, A (TMEM) stages
-    int ni;                    // MMA-issuing warps (= accumulators): 4 or 2
+    int ni;                    // MMA-issuing warps (= accumulators per buffer): 4 or 2
+    int nbuf;                  // accumulator buffers (pieces alternate between them)
     int split;                 // 1: partition k iterations evenly over CTAs
     uint32_t b_stage_bytes;
     uint32_t smem_b_off, smem_misc_off, smem_bytes;
