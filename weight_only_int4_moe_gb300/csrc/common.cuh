@@ -103,6 +103,23 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, 
     return false;
 }
 
+// Shared-memory loads by 32-bit shared address (ld.shared: the short-latency
+// path; a load through a generic pointer may be issued as a generic load).
+// volatile: they must stay after the mbarrier wait that publishes the data.
+MOE_DEV uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+MOE_DEV uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Producer/consumer named barrier: arrive without waiting / wait for `threads`.
 MOE_DEV void named_bar_arrive(uint32_t id, uint32_t threads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = wid & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint8_t *my_w = smem + row * 16;
-        const uint8_t *my_s = smem + kStageW + row * 4;
+        const uint32_t my_w = w_ring + (uint32_t)row * 16u;  // shared addresses
+        const uint32_t my_s = w_ring + kStageW + (uint32_t)row * 4u;
         const uint32_t my_t = tmem + lane_off + col_a;
         const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
         const DequantConsts dqc = p.dq;
@@ -405,17 +405,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a_ph ^= 1u;
                     if (!freed) ok = false;
                 }
-                const uint8_t *sw = my_w + w.idx * kStage;
-                const uint8_t *ss = my_s + w.idx * kStage;
+                const uint32_t sw = my_w + w.idx * kStage;
+                const uint32_t ss = my_s + w.idx * kStage;
                 const uint32_t st = my_t + a.idx * kACols;
                 for (int uu = 0; uu < nsub && ok; ++uu) {
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
-                        const uint8_t *src = sw + uu * kStageWBytes + g * kSlabBytes;
-                        const uint4 lo = *reinterpret_cast<const uint4 *>(src);
-                        const uint4 hi = *reinterpret_cast<const uint4 *>(src + 2048);
-                        const uint32_t sc =
-                            *reinterpret_cast<const uint32_t *>(ss + uu * kStageSBytes + g * 512);
+                        const uint32_t src = sw + uu * kStageWBytes + g * kSlabBytes;
+                        const uint4 lo = lds128(src);
+                        const uint4 hi = lds128(src + 2048);
+                        const uint32_t sc = lds32(ss + uu * kStageSBytes + g * 512);
                         if (g == 1 && uu == nsub - 1) {  // every load of this stage is done
                             __syncwarp();
                             if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
