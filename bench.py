@@ -303,7 +303,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
-    def one_call(M, r, rec):
+    def one_call(M, r, rec, profiled=False):
         d = data[M]
         ids, tw, n_touched = d["routes"][r % len(d["routes"])]
         flush.zero_()
@@ -315,7 +315,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
         ev1.record(stream)
         launches = ops.moe_int4_last_launch_count()
         if rec is not None:
-            stages = ops.moe_int4_profile_read()  # waits for this call's events
+            stages = ops.moe_int4_profile_read() if profiled else None  # waits for the events
             ev1.synchronize()
             rec.append({"M": M, "ms": ev0.elapsed_time(ev1), "stages": stages,
                         "touched": n_touched, "launches": launches})
@@ -326,8 +326,8 @@ def run_ours(args, cfg, Ms, world, rank, local):
             one_call(M, s, None)
     torch.cuda.synchronize()
 
-    # timed region
-    ops.moe_int4_profile_enable(True)
+    # timed region: whole calls, no events between the kernels (they would
+    # hold back the overlap of each kernel's set-up with the previous one)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     barrier(dist, True)
     torch.cuda.synchronize()
@@ -341,6 +341,14 @@ def run_ours(args, cfg, Ms, world, rank, local):
     wall = time.perf_counter() - wall0
     barrier(dist, True)
     clk = clocks.stop()
+    # per-kernel times: the same calls again with CUDA events between the
+    # kernels, on the launching stream (for the stage split and the roofline)
+    ops.moe_int4_profile_enable(True)
+    prec = []
+    for s in range(args.steps):
+        for M in Ms:
+            one_call(M, args.warmup + s, prec, profiled=True)
+    torch.cuda.synchronize()
     ops.moe_int4_profile_enable(False)
 
     ms_per_step = sum(r["ms"] for r in rec) / args.steps
@@ -360,7 +368,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
         t_med = statistics.median(us)
         t_hbm = bytes_w / (hbm_peak * 1e9) * 1e6
         t_tc = flops / (tc_peak * 1e12) * 1e6
-        st = np.mean([r["stages"] for r in rs], axis=0)
+        st = np.mean([r["stages"] for r in prec if r["M"] == M], axis=0)
         per_m[str(M)] = {
             "us_per_call": t_med, "us_mean": statistics.mean(us),
             "tokens_per_s": M / (t_med / 1e6),
@@ -378,22 +386,32 @@ def run_ours(args, cfg, Ms, world, rank, local):
 
     # dominant kernel: the gate/up GEMM (largest stage share); algorithmic bytes
     # = touched experts x (w13 int4 + scales) per launch
-    g1_ms = [r["stages"][1] for r in rec]
-    g1_bytes = [r["touched"] * w13_b for r in rec]
-    g2_ms = [r["stages"][2] for r in rec]
+    g1_ms = [r["stages"][1] for r in prec]
+    g1_bytes = [r["touched"] * w13_b for r in prec]
+    g2_ms = [r["stages"][2] for r in prec]
     dominant = "gate_up" if sum(g1_ms) >= sum(g2_ms) else "down"
-    if dominant == "gate_up":
-        ach = sum(g1_bytes) / (sum(g1_ms) / 1e3) / 1e9
-    else:
-        ach = sum(r["touched"] * w2_b for r in rec) / (sum(g2_ms) / 1e3) / 1e9
-    bytes_mean = statistics.mean(
-        g1_bytes if dominant == "gate_up" else [r["touched"] * w2_b for r in rec])
+    k_ms = g1_ms if dominant == "gate_up" else g2_ms
+    k_bytes = g1_bytes if dominant == "gate_up" else [r["touched"] * w2_b for r in prec]
+    # algorithmic FLOPs of the launch: 2 x pairs x (2I x H for gate/up, H x I for down)
+    k_flops = [2.0 * r["M"] * cfg.top_k * cfg.H * cfg.I * (2 if dominant == "gate_up" else 1)
+               for r in prec]
+    t_hbm = sum(k_bytes) / (hbm_peak * 1e9)
+    t_tc = sum(k_flops) / (tc_peak * 1e12)
+    bytes_mean = statistics.mean(k_bytes)
     traffic, traffic_src = kernel_traffic(dominant, cfg.name, bytes_mean)
-    roofline = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                "frac": ach / hbm_peak, "traffic": traffic, "kernel": dominant,
-                "peak_source": f"{peak_src} (hbm_gbs)", "traffic_source": traffic_src,
-                "bytes_per_launch_mean": bytes_mean,
-                "launch_ms_mean": statistics.mean(g1_ms if dominant == "gate_up" else g2_ms)}
+    if t_hbm >= t_tc:  # weight streaming bound
+        ach = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": ach / hbm_peak, "peak_source": f"{peak_src} (hbm_gbs)"}
+    else:  # tensor bound; fp16 operands run at the bf16 dense rate
+        ach = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": ach / tc_peak,
+                    "peak_source": f"{peak_src} (bf16_tflops; fp16 has the same dense rate)"}
+    roofline.update({"traffic": traffic, "kernel": dominant, "traffic_source": traffic_src,
+                     "bytes_per_launch_mean": bytes_mean,
+                     "flops_per_launch_mean": statistics.mean(k_flops),
+                     "launch_ms_mean": statistics.mean(k_ms)})
 
     # end to end through the host-buffer entry point
     e2e = None

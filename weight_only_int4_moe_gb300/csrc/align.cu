@@ -126,6 +126,8 @@ __device__ void zero_regions(const ZeroArgs &z, int cta, int nctas) {
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ sorted,
                                    const int32_t *__restrict__ num_post_pad, int P, int top_k, int H,
                                    uint16_t *__restrict__ xs) {
+    pdl_wait();  // sorted_ids and num_post_pad come from the align launch
+    pdl_launch_dependents();
     const int npp = *num_post_pad;
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -152,7 +154,11 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const i
     size_t blocks = (cap_rows + 7) / 8;  // 8 warps (rows) per block
     if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
     if (blocks < 1) blocks = 1;
-    gather_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, sorted, npp, P, top_k, H, xs);
+    cudaLaunchConfig_t cfg = pdl_config((unsigned)blocks, 256, 0, s);
+    cudaLaunchAttribute attr;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl_attr(attr);
+    cudaLaunchKernelEx(&cfg, gather_rows_kernel, x, sorted, npp, P, top_k, H, xs);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }
@@ -161,6 +167,7 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const i
 __global__ void __launch_bounds__(kAlignThreads)
     align_fused_kernel(const AlignArgs a, const ZeroArgs z) {
     extern __shared__ int sm[];
+    pdl_launch_dependents();  // the gather may set up; it waits for this grid
     if (blockIdx.x > 0) {
         zero_regions(z, blockIdx.x - 1, gridDim.x - 1);
         return;
@@ -229,6 +236,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(const AlignAr
 // Step 3: each block places its chunk.
 __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const AlignArgs a) {
     extern __shared__ int sm[];
+    pdl_launch_dependents();  // the gather may set up; it waits for this grid
     int *base = sm;            // [E]
     int *wtab = base + a.E;    // [32][E]
     for (int e = threadIdx.x; e < a.E; e += kAlignThreads)
@@ -240,6 +248,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const Alig
 // out[i] = bf16(acc[i]) (round to nearest even), 8 elements per step.
 __global__ void finalize_kernel(const float *__restrict__ acc, uint16_t *__restrict__ out,
                                 size_t n8) {
+    pdl_wait();  // acc is the down GEMM's output
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
          i += (size_t)gridDim.x * blockDim.x) {
         const float4 a0 = reinterpret_cast<const float4 *>(acc)[2 * i];
@@ -292,7 +301,11 @@ cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, 
     size_t blocks = (n8 + 255) / 256;
     if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
     if (blocks < 1) blocks = 1;
-    finalize_kernel<<<(unsigned)blocks, 256, 0, s>>>(acc, out, n8);
+    cudaLaunchConfig_t cfg = pdl_config((unsigned)blocks, 256, 0, s);
+    cudaLaunchAttribute attr;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl_attr(attr);
+    cudaLaunchKernelEx(&cfg, finalize_kernel, acc, out, n8);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }

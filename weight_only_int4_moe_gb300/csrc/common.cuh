@@ -120,6 +120,13 @@ MOE_DEV uint32_t lds32(uint32_t addr) {
     return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream still runs;
+// it must call pdl_wait() before touching anything that kernel writes.
+// pdl_launch_dependents() lets the next such kernel start its own set-up.
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Producer/consumer named barrier: arrive without waiting / wait for `threads`.
 MOE_DEV void named_bar_arrive(uint32_t id, uint32_t threads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -279,6 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Everything above is set-up; from here on the kernel reads what the
+    // previous kernels of the forward wrote (routing buffers, gathered rows,
+    // zeroed counters and accumulators).
+    pdl_wait();
+    pdl_launch_dependents();
 
     // Tensor-memory column map: nbuf accumulator buffers of ni accumulators
     // (BM columns each), then the A ring of n_a stages x 128 columns.
@@ -715,10 +720,14 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_b
         if (e != cudaSuccess) return e;
         attr_done[dev][kind - 1] = true;
     }
+    cudaLaunchConfig_t cfg = pdl_config((unsigned)grid, kThreads, p.smem_bytes, s);
+    cudaLaunchAttribute attr;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl_attr(attr);
     if (kind == 1)
-        moe_gemm_kernel<1><<<grid, kThreads, p.smem_bytes, s>>>(p, *tmap_b);
+        cudaLaunchKernelEx(&cfg, moe_gemm_kernel<1>, p, *tmap_b);
     else
-        moe_gemm_kernel<2><<<grid, kThreads, p.smem_bytes, s>>>(p, *tmap_b);
+        cudaLaunchKernelEx(&cfg, moe_gemm_kernel<2>, p, *tmap_b);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }

@@ -9,6 +9,23 @@
 
 namespace moe {
 
+// Launch configuration with programmatic stream serialization: the kernel may
+// start before the previous kernel of the stream has finished (it waits with
+// griddepcontrol.wait before using that kernel's results).
+inline cudaLaunchConfig_t pdl_config(unsigned grid, unsigned block, size_t smem, cudaStream_t s) {
+    cudaLaunchConfig_t c{};
+    c.gridDim = dim3(grid);
+    c.blockDim = dim3(block);
+    c.dynamicSmemBytes = smem;
+    c.stream = s;
+    return c;
+}
+inline unsigned pdl_attr(cudaLaunchAttribute &a) {
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return 1;
+}
+
 struct AlignArgs {
     const int32_t *ids;    // [P]
     int P, E, block_m;
