@@ -71,6 +71,8 @@ def _load():
         lib.oracle_moe_intermediate_pairs.argtypes = [p] * 4 + [i64] * 5 + [p, i64, p]
         lib.oracle_moe_intermediate_pairs.restype = None
         lib.oracle_align.argtypes = [p, i64, i64, i64, i64, p, i64, p, i64, p]
+        lib.oracle_route.argtypes = [p, i64, i64, i64, p, p]
+        lib.oracle_route.restype = None
         lib.oracle_align.restype = i64
         _lib = lib
         return lib
@@ -204,3 +206,16 @@ def align(topk_ids, E: int, block_m: int):
     if n < 0:
         raise RuntimeError("oracle align capacity exceeded")
     return sorted_ids[:n].copy(), expert_ids[: n // block_m].copy(), int(n), int(dropped[0])
+
+
+def route(logits, top_k: int):
+    """Top-k experts per token by router logit (ties: lower index first) and their
+    renormalised softmax weights.  Returns (ids int32 [M, k], weights fp64 [M, k])."""
+    lg = _c(logits, np.float32)
+    M, E = lg.shape
+    ids = np.empty((M, top_k), dtype=np.int32)
+    w = np.empty((M, top_k), dtype=np.float64)
+    if M:
+        _load().oracle_route(_ptr(lg), M, E, top_k, _ptr(ids), _ptr(w))
+    return ids, w
+

@@ -183,3 +183,42 @@ int64_t oracle_align(const int32_t *topk_ids, int64_t M, int64_t top_k, int64_t 
     *n_dropped = dropped;
     return pos;
 }
+
+/*
+ * Router: for each token, the top_k experts by router logit (larger first;
+ * equal logits: the lower expert index first) and their renormalised softmax
+ * weights.  A softmax over all E experts renormalised over the k selected ones
+ * equals the softmax over the k selected logits alone (the common denominator
+ * cancels), so the weights are computed that way, in fp64 from the fp32
+ * logits.  Logits must be finite.
+ * Source: "The Throughput Lever", section "The Result: Two Regimes" (each
+ * token activates 8 of 384 experts through top-8 routing); the softmax /
+ * top-k / renormalise recipe is that of the routed workloads.
+ */
+void oracle_route(const float *logits, int64_t M, int64_t E, int64_t top_k, int32_t *ids,
+                  double *weights) {
+    for (int64_t t = 0; t < M; ++t) {
+        const float *l = logits + t * E;
+        int32_t *id = ids + t * top_k;
+        double *w = weights + t * top_k;
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                int taken = 0;
+                for (int64_t i = 0; i < j; ++i)
+                    if (id[i] == e) taken = 1;
+                if (taken) continue;
+                if (best < 0 || l[e] > l[best]) best = e;  /* strict: ties keep the lower index */
+            }
+            id[j] = (int32_t)best;
+        }
+        const double mx = (double)l[id[0]];
+        double sum = 0.0;
+        for (int64_t j = 0; j < top_k; ++j) {
+            w[j] = exp((double)l[id[j]] - mx);
+            sum += w[j];
+        }
+        for (int64_t j = 0; j < top_k; ++j) w[j] /= sum;
+    }
+}
+

@@ -327,3 +327,73 @@ def test_align_all_one_expert():
     ids = np.full((40, 2), 3, dtype=np.int32)
     s, e, n, d = oracle.align(ids, 8, 16)
     assert n == 80 and list(e) == [3] * 5 and list(s) == list(range(80))
+
+
+# --------------------------------------------------------------- router --
+# Router oracle (top-k by logit, renormalised softmax over the chosen k).
+
+def test_route_closed_form_two_experts():
+    """Logits 0 and ln 3: softmax weights 1/4 and 3/4 (closed form)."""
+    lg = np.array([[0.0, np.log(3.0), -2.0]], dtype=np.float32)
+    ids, w = oracle.route(lg, 2)
+    assert ids.tolist() == [[1, 0]]
+    l1 = float(np.float32(np.log(3.0)))
+    expect = np.array([np.exp(l1), 1.0]) / (np.exp(l1) + 1.0)
+    np.testing.assert_allclose(w[0], expect, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(w[0], [0.75, 0.25], atol=1e-7)
+
+
+def test_route_distinct_logits_reduce_to_library_sort_and_softmax():
+    """With distinct logits the ids are numpy's descending argsort and the
+    weights scipy's softmax of the chosen logits."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(5)
+    lg = rng.standard_normal((40, 96)).astype(np.float32)
+    for k in (1, 2, 8, 96):
+        ids, w = oracle.route(lg, k)
+        order = np.argsort(-lg.astype(np.float64), axis=1, kind="stable")[:, :k]
+        np.testing.assert_array_equal(ids, order)
+        chosen = np.take_along_axis(lg.astype(np.float64), order, axis=1)
+        np.testing.assert_allclose(w, special.softmax(chosen, axis=1), rtol=1e-13, atol=0)
+
+
+def test_route_invariants():
+    rng = np.random.default_rng(6)
+    lg = rng.standard_normal((64, 384)).astype(np.float32)
+    ids, w = oracle.route(lg, 8)
+    # weights sum to one, are positive and descending with the logits
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, atol=1e-14)
+    assert (w > 0).all() and (np.diff(w, axis=1) <= 0).all()
+    # ids are distinct and every chosen logit is >= every unchosen one
+    for t in range(64):
+        assert len(set(ids[t].tolist())) == 8
+        rest = np.delete(lg[t], ids[t])
+        assert lg[t, ids[t]].min() >= rest.max()
+    # a shift of every logit by an exactly representable constant changes nothing
+    ids2, w2 = oracle.route((lg.astype(np.float64) + 4.0).astype(np.float32), 8)
+    np.testing.assert_array_equal(ids2, ids)
+    np.testing.assert_allclose(w2, w, rtol=1e-6)
+    # top-1: weight exactly one
+    _, w1 = oracle.route(lg, 1)
+    assert (w1 == 1.0).all()
+
+
+def test_route_ties_take_the_lower_index_with_equal_weights():
+    lg = np.zeros((2, 16), dtype=np.float32)
+    lg[0, [3, 7, 11]] = 2.0  # three-way tie at the top
+    ids, w = oracle.route(lg, 4)
+    assert ids[0].tolist() == [3, 7, 11, 0]
+    assert ids[1].tolist() == [0, 1, 2, 3]
+    np.testing.assert_allclose(w[1], 0.25, atol=1e-15)
+    assert w[0, 0] == w[0, 1] == w[0, 2]
+
+
+def test_route_agrees_with_the_generator_recipe():
+    """The input generator routes by an independent recipe (fp32 softmax over
+    all experts, stable top-k of the probabilities, renormalise)."""
+    rng = np.random.default_rng(7)
+    lg = rng.standard_normal((128, 384)).astype(np.float32)
+    gid, gw = inputs.route(lg, 8)
+    ids, w = oracle.route(lg, 8)
+    np.testing.assert_array_equal(ids, gid)
+    np.testing.assert_allclose(w, gw, rtol=2e-6)
