@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--routed", action="store_true",
+                    help="time moe_int4_forward_routed: routing from router logits in the call")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (a smaller case of the same kernels, for ncu captures)")
     return ap.parse_args()
@@ -300,6 +302,11 @@ def run_ours(args, cfg, Ms, world, rank, local):
             routes.append((torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev), n))
         out = torch.empty((M, cfg.H), dtype=shape.torch_out_dtype, device=dev)
         data[M] = {"x": x, "routes": routes, "out": out, "host": t, "pool": pool}
+        if args.routed:
+            data[M]["logits"] = [torch.from_numpy(lg).to(dev)
+                                 for lg in inputs.router_logits_pool(cfg, M, args.pool - 1)]
+            data[M]["rids"] = torch.empty((M, cfg.top_k), dtype=torch.int32, device=dev)
+            data[M]["rw"] = torch.empty((M, cfg.top_k), dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -310,8 +317,14 @@ def run_ours(args, cfg, Ms, world, rank, local):
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
-        ops.moe_int4_forward(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales, ids, tw,
-                             shape, out=d["out"], workspace=ws, stream=stream)
+        if args.routed:
+            ops.moe_int4_forward_routed(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales,
+                                        d["logits"][r % len(d["logits"])], shape, out=d["out"],
+                                        topk_ids=d["rids"], topk_weights=d["rw"], workspace=ws,
+                                        stream=stream)
+        else:
+            ops.moe_int4_forward(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales, ids, tw,
+                                 shape, out=d["out"], workspace=ws, stream=stream)
         ev1.record(stream)
         launches = ops.moe_int4_last_launch_count()
         if rec is not None:
@@ -469,6 +482,8 @@ def run_ours(args, cfg, Ms, world, rank, local):
                        "l2": f"flushed by a {args.flush_mb} MB device write before every call; "
                              f"routing rotates over {args.pool} seeded routings per M",
                        "out_dtype": args.out_dtype, "parallelism": f"replicas x{world}",
+                       "routing": ("router logits -> top-k in the call (moe_int4_forward_routed)"
+                                   if args.routed else "precomputed top-k ids and weights"),
                        "block_m": {str(M): ops.moe_int4_block_m(M, shape) for M in Ms}},
             "per_m": per_m, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(sum(r["launches"] for r in rec)),

@@ -227,6 +227,39 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
                      void *out, int M, const moe_int4_shape *shape,
                      void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+/* Router ("The Throughput Lever", "The Result: Two Regimes": each token      */
+/* activates top_k of E experts through top-k routing)                        */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * moe_route: per token, the top_k experts by router logit and their weights.
+ * In:  router_logits fp32 [M][E] (finite).
+ * Out: topk_ids int32 [M][top_k]: experts in descending logit order; equal
+ *        logits are taken in ascending expert index (exact fp32 comparisons,
+ *        so the ids are reproducible bit for bit).
+ *      topk_weights fp32 [M][top_k]: the softmax over all E logits renormalised
+ *        over the chosen top_k, i.e. the softmax over the chosen logits.
+ * Sizes: 1 <= E <= 1024, 1 <= top_k <= min(E, 32), 0 <= M <= 1<<20.
+ * Errors: MOE_ERR_SHAPE, MOE_ERR_NULL, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ */
+int moe_route(const float *router_logits, int M, int E, int top_k, int32_t *topk_ids,
+              float *topk_weights, moe_stream_t stream);
+
+/*
+ * moe_int4_forward_routed: moe_int4_forward with the routing computed from
+ * router logits: the router (as moe_route) runs in the same launch as the
+ * align for routings up to 32 tokens, writes topk_ids and topk_weights (device
+ * buffers [M][top_k] owned by the caller, also returned), and the layer then
+ * runs exactly as moe_int4_forward on them.  router_logits: fp32 [M][E].
+ * Workspace, layout, errors and output: as moe_int4_forward.
+ */
+int moe_int4_forward_routed(const uint16_t *x, const void *w13_packed, const void *w13_scales,
+                            const void *w2_packed, const void *w2_scales,
+                            const float *router_logits, int32_t *topk_ids, float *topk_weights,
+                            void *out, int M, const moe_int4_shape *shape, void *workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
+
 /*
  * moe_int4_forward_host: the same layer with x, topk_ids, topk_weights and out
  * in HOST memory (pinned memory makes the copies asynchronous).  The inputs are

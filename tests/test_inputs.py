@@ -46,3 +46,13 @@ def test_routing_skewed_share():
     assert abs(t["hot_share"] - 0.5) <= 0.011
     assert len(t["hot"]) == 77
     assert cfg.routing == "skewed"
+
+
+def test_router_logits_reproduce_the_routings():
+    """Routing the generated router logits gives the generator's routings
+    (uniform and skewed recipes)."""
+    for cfg, M in ((inputs.CONFIGS[0], 16), (inputs.MoEConfig("s", 64, 8, 128, 128, (40,), "skewed", 2, 9), 40)):
+        pool = [inputs.make_tokens(cfg, M)["topk_ids"]] + [ids for ids, _ in inputs.routing_pool(cfg, M, 2)]
+        for ids, lg in zip(pool, inputs.router_logits_pool(cfg, M, 2)):
+            rid, _ = inputs.route(lg, cfg.top_k)
+            np.testing.assert_array_equal(rid, ids)

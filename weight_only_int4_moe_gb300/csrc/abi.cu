@@ -258,11 +258,17 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
     return MOE_OK;
 }
 
-int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_scales,
-                     const void *w2_packed, const void *w2_scales, const int32_t *topk_ids,
-                     const float *topk_weights, void *out, int M,
-                     const moe_int4_shape *shape, void *workspace, size_t workspace_bytes,
-                     moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward; with router_logits set, the routing (topk_ids / topk_weights,
+// written) is computed in the align launch, else it is read from them.
+int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scales,
+                 const void *w2_packed, const void *w2_scales, const float *router_logits,
+                 const int32_t *topk_ids, const float *topk_weights, void *out, int M,
+                 const moe_int4_shape *shape, void *workspace, size_t workspace_bytes,
+                 moe_stream_t stream) {
     g_last_launches = 0;
     int rc = check_shape(shape);
     if (rc != MOE_OK) return rc;
@@ -272,9 +278,9 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
         !topk_weights || !out || !workspace)
         return MOE_ERR_NULL;
     const void *ptrs[] = {x, w13_packed, w13_scales, w2_packed, w2_scales, topk_ids,
-                          topk_weights, out, workspace};
+                          topk_weights, out, workspace, router_logits};
     for (const void *q : ptrs)
-        if (!aligned16(q)) return MOE_ERR_ALIGN;
+        if (q && !aligned16(q)) return MOE_ERR_ALIGN;
     const Plan pl = make_plan(M, shape);
     if (workspace_bytes < pl.total) return MOE_ERR_WORKSPACE;
     int sms = 0;
@@ -331,7 +337,19 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     int zero_ctas = (int)(zero_bytes / (64 * 1024));
     if (zero_ctas < 1) zero_ctas = 1;
     if (zero_ctas > 2 * sms) zero_ctas = 2 * sms;
-    if (launch_align(al, z, zero_ctas, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+    if (router_logits) {
+        RouteArgs ra{};
+        ra.logits = router_logits;
+        ra.M = pl.M;
+        ra.E = pl.E;
+        ra.top_k = pl.k;
+        ra.ids = const_cast<int32_t *>(topk_ids);
+        ra.weights = const_cast<float *>(topk_weights);
+        if (launch_route_align(ra, al, z, zero_ctas, sms, s, &launches) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else if (launch_align(al, z, zero_ctas, s, &launches) != cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
     if (launch_gather_rows(x, sorted, npp, pl.P, pl.k, pl.H, x16, pl.cap, sms, s, &launches) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
@@ -385,6 +403,51 @@ int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_
     prof_record(4, s);
     g_last_launches = launches;
     return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_int4_forward(const uint16_t *x, const void *w13_packed, const void *w13_scales,
+                     const void *w2_packed, const void *w2_scales, const int32_t *topk_ids,
+                     const float *topk_weights, void *out, int M,
+                     const moe_int4_shape *shape, void *workspace, size_t workspace_bytes,
+                     moe_stream_t stream) {
+    return forward_impl(x, w13_packed, w13_scales, w2_packed, w2_scales, nullptr, topk_ids,
+                        topk_weights, out, M, shape, workspace, workspace_bytes, stream);
+}
+
+int moe_int4_forward_routed(const uint16_t *x, const void *w13_packed, const void *w13_scales,
+                            const void *w2_packed, const void *w2_scales,
+                            const float *router_logits, int32_t *topk_ids, float *topk_weights,
+                            void *out, int M, const moe_int4_shape *shape, void *workspace,
+                            size_t workspace_bytes, moe_stream_t stream) {
+    if (M > 0 && !router_logits) return MOE_ERR_NULL;
+    return forward_impl(x, w13_packed, w13_scales, w2_packed, w2_scales, router_logits,
+                        topk_ids, topk_weights, out, M, shape, workspace, workspace_bytes,
+                        stream);
+}
+
+int moe_route(const float *router_logits, int M, int E, int top_k, int32_t *topk_ids,
+              float *topk_weights, moe_stream_t stream) {
+    if (M < 0 || M > (1 << 20) || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E)
+        return MOE_ERR_SHAPE;
+    if (M == 0) return MOE_OK;
+    if (!router_logits || !topk_ids || !topk_weights) return MOE_ERR_NULL;
+    int sms = 0;
+    const int rc = device_info(&sms);
+    if (rc != MOE_OK) return rc;
+    RouteArgs ra{};
+    ra.logits = router_logits;
+    ra.M = M;
+    ra.E = E;
+    ra.top_k = top_k;
+    ra.ids = topk_ids;
+    ra.weights = topk_weights;
+    return launch_route(ra, sms, reinterpret_cast<cudaStream_t>(stream), nullptr) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 int moe_int4_forward_host(const uint16_t *x_host, const void *w13_packed,

@@ -163,15 +163,8 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const i
     return cudaGetLastError();
 }
 
-// Whole align in one block (P small); blocks 1.. zero the accumulators.
-__global__ void __launch_bounds__(kAlignThreads)
-    align_fused_kernel(const AlignArgs a, const ZeroArgs z) {
-    extern __shared__ int sm[];
-    pdl_launch_dependents();  // the gather may set up; it waits for this grid
-    if (blockIdx.x > 0) {
-        zero_regions(z, blockIdx.x - 1, gridDim.x - 1);
-        return;
-    }
+// Whole align in one block (P small).
+__device__ void align_one_block(const AlignArgs &a, int *sm) {
     int *cnt = sm;                    // [E]
     int *base = cnt + a.E;            // [E]
     int *scan_tmp = base + a.E;       // [33]
@@ -186,6 +179,92 @@ __global__ void __launch_bounds__(kAlignThreads)
     align_layout(a, cnt, base, scan_tmp);
     __syncthreads();
     for (int i0 = 0; i0 < a.P; i0 += kAlignThreads) align_place_round(a, i0, base, wtab);
+}
+
+// Whole align in one block (P small); blocks 1.. zero the accumulators.
+__global__ void __launch_bounds__(kAlignThreads)
+    align_fused_kernel(const AlignArgs a, const ZeroArgs z) {
+    extern __shared__ int sm[];
+    pdl_launch_dependents();  // the gather may set up; it waits for this grid
+    if (blockIdx.x > 0) {
+        zero_regions(z, blockIdx.x - 1, gridDim.x - 1);
+        return;
+    }
+    align_one_block(a, sm);
+}
+
+// ------------------------------------------------------------------ router --
+// "The Throughput Lever", section "The Result: Two Regimes": each token picks 8
+// of 384 experts by top-8 routing.  One warp per token: lane l holds logits
+// l, l + 32, ... (up to 32 of them, E <= 1024).  Each of the top_k rounds takes
+// the warp's largest remaining logit (ties: the lower expert index), so the
+// selection is decided by exact fp32 comparisons.  The weights are the softmax
+// over the chosen logits, which equals the softmax over all E renormalised over
+// the chosen k.  NaN logits rank as -inf.
+__device__ void route_token(const RouteArgs &r, int t, int lane) {
+    const float *lg = r.logits + (size_t)t * r.E;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int e = lane + 32 * i;
+        const float x = (e < r.E) ? lg[e] : -INFINITY;
+        v[i] = isnan(x) ? -INFINITY : x;
+    }
+    uint32_t taken = 0;
+    float my_sel = 0.f, mx = 0.f;
+    for (int j = 0; j < r.top_k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;  // no candidate
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int e = lane + 32 * i;
+            if (e < r.E && !((taken >> i) & 1u) && (be == 0x7fffffff || v[i] > bv)) {
+                bv = v[i];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == j) my_sel = bv;
+        if (j == 0) mx = bv;
+        if (lane == 0) r.ids[(size_t)t * r.top_k + j] = be;
+    }
+    const float ex = (lane < r.top_k) ? expf(my_sel - mx) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < r.top_k) r.weights[(size_t)t * r.top_k + lane] = ex / sum;
+}
+
+__global__ void route_kernel(const RouteArgs r) {
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < r.M; t += warps)
+        route_token(r, t, lane);
+}
+
+// Router and align in one launch (small routings): block 0 routes every token,
+// then aligns its own output; blocks 1.. zero the accumulators.
+__global__ void __launch_bounds__(kAlignThreads)
+    route_align_fused_kernel(const RouteArgs r, const AlignArgs a, const ZeroArgs z) {
+    extern __shared__ int sm[];
+    pdl_launch_dependents();  // the gather may set up; it waits for this grid
+    if (blockIdx.x > 0) {
+        zero_regions(z, blockIdx.x - 1, gridDim.x - 1);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    for (int t = threadIdx.x >> 5; t < r.M; t += kAlignWarps) route_token(r, t, lane);
+    __syncthreads();  // the block's routed ids are visible to the whole block
+    align_one_block(a, sm);
 }
 
 // Multi-block align, step 1: per-chunk histograms; extra blocks zero.
@@ -270,8 +349,7 @@ size_t align_smem_fused(int E) { return (size_t)(2 * E + 64 + kAlignWarps * E) *
 size_t align_smem_scan(int E) { return (size_t)(2 * E + 64) * sizeof(int); }
 size_t align_smem_scatter(int E) { return (size_t)(E + kAlignWarps * E) * sizeof(int); }
 
-cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas,
-                         cudaStream_t s, int *launches) {
+static cudaError_t launch_align_attrs() {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -281,8 +359,17 @@ cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas,
         cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
         cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
         cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+        cudaFuncSetAttribute(route_align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             maxs);
         attr_done[dev] = true;
     }
+    return cudaSuccess;
+}
+
+cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas,
+                         cudaStream_t s, int *launches) {
+    cudaError_t ea = launch_align_attrs();
+    if (ea != cudaSuccess) return ea;
     if (a.n_chunks <= 0) {
         align_fused_kernel<<<1 + zero_ctas, kAlignThreads, align_smem_fused(a.E), s>>>(a, z);
         if (launches) *launches += 1;
@@ -293,6 +380,33 @@ cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas,
         if (launches) *launches += 3;
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_route(const RouteArgs &r, int sms, cudaStream_t s, int *launches) {
+    size_t blocks = ((size_t)r.M + 3) / 4;  // 4 warps (tokens) per block
+    if (blocks > (size_t)sms * 16) blocks = (size_t)sms * 16;
+    if (blocks < 1) blocks = 1;
+    route_kernel<<<(unsigned)blocks, 128, 0, s>>>(r);
+    if (launches) *launches += 1;
+    return cudaGetLastError();
+}
+
+// Largest routing done by one block of the fused kernel (tokens): beyond one
+// token per warp, spreading the router over many SMs is faster.
+constexpr int kFusedRouteMaxTokens = kAlignWarps;  // one token per warp of the block
+
+cudaError_t launch_route_align(const RouteArgs &r, const AlignArgs &a, const ZeroArgs &z,
+                               int zero_ctas, int sms, cudaStream_t s, int *launches) {
+    if (a.n_chunks <= 0 && r.M <= kFusedRouteMaxTokens) {
+        cudaError_t e = launch_align_attrs();
+        if (e != cudaSuccess) return e;
+        route_align_fused_kernel<<<1 + zero_ctas, kAlignThreads, align_smem_fused(a.E), s>>>(r, a, z);
+        if (launches) *launches += 1;
+        return cudaGetLastError();
+    }
+    cudaError_t e = launch_route(r, sms, s, launches);
+    if (e != cudaSuccess) return e;
+    return launch_align(a, z, zero_ctas, s, launches);
 }
 
 cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, cudaStream_t s,

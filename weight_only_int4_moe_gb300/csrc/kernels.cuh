@@ -37,12 +37,27 @@ struct AlignArgs {
     int n_chunks;          // 0: single-block path
 };
 
+// Router: per token, the top_k experts by logit (ties: lower index first) and
+// their renormalised softmax weights.
+struct RouteArgs {
+    const float *logits;  // [M][E]
+    int M, E, top_k;
+    int32_t *ids;         // [M][top_k]
+    float *weights;       // [M][top_k]
+};
+
 // Per-call zeroing done by the align launch's spare blocks.
 struct ZeroArgs {
     void *ptr[2];
     size_t n16[2];  // 16-byte units
 };
 
+// Router alone (one warp per token).
+cudaError_t launch_route(const RouteArgs &r, int sms, cudaStream_t s, int *launches);
+// Router fused with the align (one kernel when the routing is small, else the
+// router kernel then the align launch); a.ids must be r.ids.
+cudaError_t launch_route_align(const RouteArgs &r, const AlignArgs &a, const ZeroArgs &z,
+                               int zero_ctas, int sms, cudaStream_t s, int *launches);
 cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas, cudaStream_t s,
                          int *launches);
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const int32_t *npp, int P,

@@ -177,3 +177,27 @@ def routing_pool(cfg: MoEConfig, M: int, n: int, base_seed: int = 1000):
             ids, w = route(logits, cfg.top_k)
         pool.append((ids, w))
     return pool
+
+
+def router_logits_pool(cfg: MoEConfig, M: int, n: int, base_seed: int = 1000):
+    """Router logits (fp32 [M, E]) behind make_tokens(cfg, M) followed by the n
+    routings of routing_pool(cfg, M, n): the same draws, with the hot-expert
+    bias of the skewed recipe added, so that routing them gives those routings."""
+    out = []
+    rng = np.random.default_rng([0, cfg.index, M])
+    rng.standard_normal((M, cfg.H), dtype=np.float32)  # x
+    seeds = [None] + [base_seed + r for r in range(n)]
+    for sd in seeds:
+        if sd is not None:
+            rng = np.random.default_rng([0, cfg.index, M, sd])
+        logits = rng.standard_normal((M, cfg.E), dtype=np.float32)
+        if cfg.routing == "skewed":
+            perm = rng.permutation(cfg.E)
+            hot = np.sort(perm[: math.ceil(0.2 * cfg.E)])
+            _, _, b, _ = route_skewed(logits, cfg.top_k, hot)
+            mask = np.zeros(cfg.E, dtype=np.float32)
+            mask[hot] = 1.0
+            logits = logits + np.float32(b) * mask
+        out.append(logits)
+    return out
+

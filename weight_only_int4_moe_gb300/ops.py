@@ -29,7 +29,7 @@ EXPORTED = [
     "moe_int4_forward",
     "moe_int4_forward_host", "moe_int4_get_errors", "moe_int4_clear_errors",
     "moe_int4_strerror", "moe_int4_profile_enable", "moe_int4_profile_read",
-    "moe_int4_last_launch_count", "moe_align_noalloc",
+    "moe_int4_last_launch_count", "moe_align_noalloc", "moe_route", "moe_int4_forward_routed",
 ]
 
 
@@ -84,6 +84,8 @@ def load_library(build_if_missing: bool = True):
             "moe_int4_profile_read": ([p], i),
             "moe_int4_last_launch_count": ([], i),
             "moe_align_noalloc": ([p, i, i, i, i, p, p, p, p, p], i),
+            "moe_route": ([p, i, i, i, p, p, p], i),
+            "moe_int4_forward_routed": ([p] * 9 + [i, sp, p, sz, p], i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -234,6 +236,40 @@ def moe_int4_forward(x, w13_packed, w13_scales, w2_packed, w2_scales, topk_ids, 
         ctypes.byref(shape), _dptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "moe_int4_forward")
     return out
+
+
+def moe_route(router_logits: torch.Tensor, top_k: int, stream=None):
+    """(topk_ids int32 [M, k], topk_weights fp32 [M, k]) from fp32 logits [M, E]."""
+    M, E = router_logits.shape
+    dev = router_logits.device
+    ids = torch.empty((M, top_k), dtype=torch.int32, device=dev)
+    w = torch.empty((M, top_k), dtype=torch.float32, device=dev)
+    _check(load_library().moe_route(_dptr(router_logits), M, E, top_k, _dptr(ids), _dptr(w),
+                                    _stream(stream)), "moe_route")
+    return ids, w
+
+
+def moe_int4_forward_routed(x, w13, w13_scales, w2, w2_scales, router_logits, shape: Shape,
+                            out=None, topk_ids=None, topk_weights=None, workspace=None,
+                            stream=None):
+    """moe_int4_forward with the routing computed from fp32 router logits [M, E].
+    Returns (out, topk_ids, topk_weights)."""
+    M = x.shape[0]
+    dev = x.device
+    if out is None:
+        out = torch.empty((M, shape.hidden), dtype=shape.torch_out_dtype, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((M, shape.top_k), dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((M, shape.top_k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(M, shape, device=dev)
+    rc = load_library().moe_int4_forward_routed(
+        _dptr(x), _dptr(w13), _dptr(w13_scales), _dptr(w2), _dptr(w2_scales),
+        _dptr(router_logits), _dptr(topk_ids), _dptr(topk_weights), _dptr(out), M,
+        ctypes.byref(shape), _dptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "moe_int4_forward_routed")
+    return out, topk_ids, topk_weights
 
 
 def moe_int4_forward_host(x_host, w13_packed, w13_scales, w2_packed, w2_scales, ids_host,
