@@ -188,7 +188,7 @@ int moe_align_noalloc(const int32_t *topk_ids, int M, int top_k, int E, int bloc
 /* Workspace bytes for a forward of M tokens (0 < M <= 1<<20). */
 size_t moe_int4_workspace_bytes(int M, const moe_int4_shape *shape, int flags);
 
-/* The routing block height the forward uses for M tokens (16..128). */
+/* The routing block height the forward uses for M tokens (16..192). */
 int moe_int4_block_m(int M, const moe_int4_shape *shape);
 
 /*

@@ -47,6 +47,8 @@ SMALL = [
     (8, 2, 512, 256, 1000, 4),    # ~250 tokens per expert -> block 192, 2 blocks
     (64, 6, 512, 256, 700, 5),    # P = 4200 -> multi-block align
     (32, 8, 1024, 384, 5, 6),     # many k stages per tile, stream-K splits
+    (4, 2, 1024, 384, 300, 7),    # ~150 tokens per expert -> wide block 192, odd down k tail
+    (8, 2, 256, 128, 500, 8),     # ~125 tokens per expert -> wide block 176
 ]
 
 

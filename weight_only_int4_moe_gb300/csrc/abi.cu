@@ -41,7 +41,7 @@ int choose_block_m(long long P, int E) {
     int bm = (int)(avg * 1.25 + 8.0);
     bm = (bm + 15) / 16 * 16;
     if (bm < 16) bm = 16;
-    if (bm > 128) bm = 128;
+    if (bm > 192) bm = 192;
     return bm;
 }
 

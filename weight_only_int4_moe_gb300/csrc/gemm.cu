@@ -8,7 +8,7 @@
 // both regimes:
 //
 //  * Swap-AB: the MMA's M side (128 lanes of tensor memory) is 128 weight rows,
-//    its N side is the tokens routed to one expert block (16..128, the block's
+//    its N side is the tokens routed to one expert block (16..192, the block's
 //    real row count rounded up to 16), so a decode call with one token per expert
 //    streams each touched weight once and wastes no weight traffic.
 //  * A pipeline stage is two k sub-stages of two 128x64 INT4 slabs each (16 KB,
@@ -206,13 +206,22 @@ __device__ __forceinline__ uint16_t f16_sat(float v) {
 // SiLU(g) * u = g / (1 + e^-g) * u.  The fast divide is within a few ulp of
 // the IEEE one (its result is rounded to fp16 next) and gives g * 0 = -0 when
 // e^-g overflows for very negative g.
+// Issuing warps that take part in (and release) one A part of a stage: with
+// four issuers (one per slab x sub-stage) a sub-stage part has two of them.
+__host__ __device__ __forceinline__ int part_issuers(int ni, int np) {
+    return (ni == 4) ? 4 / np : ni;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 }  // namespace
 
-template <int KIND>
+// WIDE: the wide-block configuration (blocks of 144..192 tokens): gate/up
+// releases A per sub-stage half (np = 2), down has one issuer and B slots of
+// one sub-stage.  Separate instantiations keep the common path's registers.
+template <int KIND, int WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_b) {
     extern __shared__ uint8_t smem_raw[];
@@ -234,12 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_w_empty = bar_w_full + 8 * n_w;
     const uint32_t bar_b_full = bar_w_empty + 8 * n_w;
     const uint32_t bar_b_empty = bar_b_full + 8 * n_b;
-    // a_free[t]: the A slot of team t's next stage is free (the MMAs of the
-    // stage n_a earlier, which used the same slot, are done)
+    // a_free[t][part]: part `part` of the A slot of team t's next stage is free
+    // (the MMAs of the stage n_a earlier on it are done); np = 2 releases each
+    // sub-stage half of a slot on its own
+    constexpr int np = (WIDE && KIND == 1) ? 2 : 1;
+    constexpr bool b_sub = (WIDE && KIND == 2);
     const uint32_t bar_a_free = bar_b_empty + 8 * n_b;
     // acc_full[b] / acc_empty[b]: accumulator buffer b holds a finished piece /
     // has been read by the epilogue (buffers alternate between pieces)
-    const uint32_t bar_acc_full = bar_a_free + 8 * kTeams;
+    const uint32_t bar_acc_full = bar_a_free + 8 * kTeams * np;
     const uint32_t bar_acc_empty = bar_acc_full + 16;
     const uint32_t bar_drain = bar_acc_empty + 16;
     const uint32_t misc_words = bar_drain + 8;  // tmem slot, abort flag, bcast
@@ -248,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc_ptr + 4);
     volatile int *bcast = reinterpret_cast<volatile int *>(misc_ptr + 8);
     // stage tags of the weight ring: the CTA stage index last issued into each slot
-    volatile uint32_t *w_tag = reinterpret_cast<volatile uint32_t *>(smem + (misc - base) + 384);
+    volatile uint32_t *w_tag = reinterpret_cast<volatile uint32_t *>(smem + (misc - base) + 512);
     // down epilogue: (token, routing weight) of each column of the current block
     int2 *col_tab = reinterpret_cast<int2 *>(smem + (misc - base) + 1024);
 
@@ -261,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_b_full + 8 * i, 1);
             mbar_init(bar_b_empty + 8 * i, ni);
         }
-        for (int i = 0; i < kTeams; ++i) mbar_init(bar_a_free + 8 * i, ni);
+        for (int i = 0; i < kTeams * np; ++i) mbar_init(bar_a_free + 8 * i, part_issuers(ni, np));
         for (int i = 0; i < n_w; ++i) w_tag[i] = 0xFFFFFFFFu;
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_acc_full + 8 * i, ni);
@@ -343,18 +355,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring bq(n_b);
             while (ok && pi.next(sched, tile, kb0, kb1)) {
                 const int b = tile / p.RT;
-                for (int j = kb0; j < kb1; ++j, ++i, bq.next()) {
-                    const uint32_t s = bq.idx;
-                    if (!mbar_wait(bar_b_empty + 8 * s, bq.ph ^ 1, abort_flag, p.err, 128)) {
-                        ok = false;
-                        break;
+                for (int j = kb0; j < kb1 && ok; ++j) {
+                    // one slot per stage, or (wide blocks) one per sub-stage
+                    const int nsub = stage_subs(j, kss);
+                    const int nslots = b_sub ? nsub : 1;
+                    const int nblk = b_sub ? kb_per_sub : nsub * kb_per_sub;
+                    for (int sl = 0; sl < nslots; ++sl, ++i, bq.next()) {
+                        const uint32_t s = bq.idx;
+                        if (!mbar_wait(bar_b_empty + 8 * s, bq.ph ^ 1, abort_flag, p.err, 128)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = b_ring + s * p.b_stage_bytes;
+                        const int kb_first = 2 * kb_per_sub * j + sl * kb_per_sub;
+                        mbar_arrive_expect_tx(bar_b_full + 8 * s, (uint32_t)nblk * BM * 128u);
+                        for (int qb = 0; qb < nblk; ++qb)
+                            tma_load_2d(dst + qb * BM * 128, &tmap_b, (kb_first + qb) * 64,
+                                        b * BM, bar_b_full + 8 * s);
                     }
-                    const int nblk = stage_subs(j, kss) * kb_per_sub;
-                    const uint32_t dst = b_ring + s * p.b_stage_bytes;
-                    mbar_arrive_expect_tx(bar_b_full + 8 * s, (uint32_t)nblk * BM * 128u);
-                    for (int qb = 0; qb < nblk; ++qb)
-                        tma_load_2d(dst + qb * BM * 128, &tmap_b, (2 * kb_per_sub * j + qb) * 64,
-                                    b * BM, bar_b_full + 8 * s);
                 }
             }
             if (!ok) {
@@ -380,13 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t my_w = w_ring + (uint32_t)row * 16u;  // shared addresses
         const uint32_t my_s = w_ring + kStageW + (uint32_t)row * 4u;
         const uint32_t my_t = tmem + lane_off + col_a;
-        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
+        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + part_issuers(ni, np)) * 32u;
         const DequantConsts dqc = p.dq;
         volatile int no_abort = 0;
         Ring w(n_w), a(n_a);  // a: the A slot only (its phase is not used)
         w.advance(team);
         a.advance(team);
-        uint32_t a_ph = 0;    // parity of this team's next a_free phase
+        uint32_t a_ph = 0;    // parity bits (per part) of this team's next a_free phases
         long long s0 = 0;           // CTA stage index of the current piece's first stage
         long long own = team;       // next stage of this team
         bool ok = true;
@@ -398,40 +416,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_stage(bar_w_full + 8 * w.idx, w.ph, w_tag + w.idx, (uint32_t)own,
                                     abort_flag, p.err);
                 const int nsub = ok ? stage_subs(j, kss) : 0;
-                // The A slot is reused only once the MMAs of the stage n_a
-                // earlier (which used it) are done; the issuers signal that on
-                // this team's own barrier, whose phases follow the team's stages
-                // in order, so a parity wait is never more than one phase behind.
-                // This wait happens even after an error: it keeps this warp from
-                // arriving on the slot's named barrier again before the issuers
-                // have consumed the previous arrival.
-                if (own >= n_a) {
-                    const bool freed = warp_wait(bar_a_free + 8 * team, a_ph, &no_abort, p.err);
-                    a_ph ^= 1u;
-                    if (!freed) ok = false;
-                }
                 const uint32_t sw = my_w + w.idx * kStage;
                 const uint32_t ss = my_s + w.idx * kStage;
                 const uint32_t st = my_t + a.idx * kACols;
-                for (int uu = 0; uu < nsub && ok; ++uu) {
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        const uint32_t src = sw + uu * kStageWBytes + g * kSlabBytes;
-                        const uint4 lo = lds128(src);
-                        const uint4 hi = lds128(src + 2048);
-                        const uint32_t sc = lds32(ss + uu * kStageSBytes + g * 512);
-                        if (g == 1 && uu == nsub - 1) {  // every load of this stage is done
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
-                        }
-                        uint32_t v[32];
-                        dequant_row(lo, hi, sc, dqc, v);
-                        tc_fence_after();
-                        tmem_st_32x32b_x32_wait(st + uu * 64 + g * 32, v);
+                for (int part = 0; part < np; ++part) {
+                    // Part `part` of the A slot is reused only once the MMAs of
+                    // the stage n_a earlier on it are done; the issuers signal
+                    // that on this team's own barrier for the part, whose phases
+                    // follow the team's stages in order, so a parity wait is never
+                    // more than one phase behind.  This wait happens even after an
+                    // error: it keeps this warp from arriving on the part's named
+                    // barrier again before the issuers have consumed the previous
+                    // arrival.
+                    if (own >= n_a) {
+                        const bool freed = warp_wait(bar_a_free + 8 * (team * np + part),
+                                                     (a_ph >> part) & 1u, &no_abort, p.err);
+                        a_ph ^= 1u << part;
+                        if (!freed) ok = false;
                     }
+                    const int u_lo = (np == 2) ? part : 0, u_hi = (np == 2) ? part + 1 : 2;
+                    for (int uu = u_lo; uu < u_hi && uu < nsub && ok; ++uu) {
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            const uint32_t src = sw + uu * kStageWBytes + g * kSlabBytes;
+                            const uint4 lo = lds128(src);
+                            const uint4 hi = lds128(src + 2048);
+                            const uint32_t sc = lds32(ss + uu * kStageSBytes + g * 512);
+                            if (g == 1 && uu == nsub - 1) {  // every load of this stage is done
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
+                            }
+                            uint32_t v[32];
+                            dequant_row(lo, hi, sc, dqc, v);
+                            tc_fence_after();
+                            tmem_st_32x32b_x32_wait(st + uu * 64 + g * 32, v);
+                        }
+                    }
+                    tc_fence_before();
+                    named_bar_arrive(kBarSlot0 + a.idx * np + part, slot_cnt);  // part written
                 }
-                tc_fence_before();
-                named_bar_arrive(kBarSlot0 + a.idx, slot_cnt);  // A stage written
             }
             s0 = s1;
         }
@@ -443,18 +466,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // accumulator buffer c % nbuf, so with two buffers the next piece's
         // MMAs run while the epilogue warps read the previous one.
         const int qe = wid - kFirstIssuerWarp;
-        const bool issuer = (ni == 4) || (qe < 2);
-        const int ig = qe & 1;                        // slab of this issuer
-        const int iu_lo = (ni == 4) ? (qe >> 1) : 0;  // sub-stages of this issuer
+        const bool issuer = qe < ni;
+        // units (slab, sub-stage) of this issuer: ni = 4 one, ni = 2 a slab's
+        // two, ni = 1 all four (slab loop inside)
+        const int ig = (ni == 1) ? 0 : (qe & 1);
+        const int g_hi = (ni == 1) ? 2 : ig + 1;
+        const int iu_lo = (ni == 4) ? (qe >> 1) : 0;
         const int iu_hi = (ni == 4) ? (qe >> 1) + 1 : 2;
-        const uint32_t acc_off = (uint32_t)(((ni == 4) ? 2 * ig + (qe >> 1) : ig) * BM);
-        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + ni) * 32u;
+        const uint32_t acc_off = (uint32_t)((ni == 4 ? 2 * ig + (qe >> 1) : ig) * BM);
+        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + part_issuers(ni, np)) * 32u;
+        const int kb_per_sub = (KIND == 1) ? 1 : 2;
         Ring a(n_a), bq(n_b);
         uint32_t next_team = (uint32_t)(n_a % kTeams);  // team of stage (CTA stage + n_a)
         uint32_t c = 0;
         bool ok = true;
         while (pi.next(sched, tile, kb0, kb1)) {
-            const int b = tile / p.RT, r = tile % p.RT;
+            const int b = tile / p.RT;
             const int pos0 = b * BM;
             const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
             // ---- issue (every stage is visited, see the dequant role)
@@ -466,33 +493,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok)
                     ok = warp_wait(bar_acc_empty + 8 * buf, ((c / nbuf) & 1) ^ 1, abort_flag,
                                    p.err, 32);
-                for (int j = kb0; j < kb1; ++j, a.next(), bq.next(),
+                for (int j = kb0; j < kb1; ++j, a.next(),
                          next_team = (next_team + 1 == (uint32_t)kTeams) ? 0u : next_team + 1) {
-                    named_bar_sync(kBarSlot0 + a.idx, slot_cnt);  // the stage's A is in TMEM
-                    if (ok) ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
-                    if (ok) {
-                        const int nsub = stage_subs(j, kss);
-                        const int uhi = iu_hi < nsub ? iu_hi : nsub;
-                        tc_fence_after();
-                        const uint32_t a_st = tmem + col_a + a.idx * kACols;
-                        const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
-                        for (int uu = iu_lo; uu < uhi; ++uu) {
-                            const uint32_t sub = (KIND == 1) ? (uint32_t)uu : (uint32_t)(2 * uu + ig);
-                            const uint64_t bd = smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
-                            // the last block of the stage releases its A slot (to the
-                            // team that uses it next) and its B stage
-                            const bool last = (uu == uhi - 1);
-                            mma_ts_f16_k64_commit(acc_col, a_st + uu * 64 + ig * 32, bd, idesc,
-                                                  fresh ? 0u : 1u,
-                                                  last ? bar_a_free + 8 * next_team : 0u,
-                                                  last ? bar_b_empty + 8 * bq.idx : 0u);
-                            fresh = false;
+                    const int nsub = stage_subs(j, kss);
+                    const uint32_t a_st = tmem + col_a + a.idx * kACols;
+                    if (!b_sub && ok)
+                        ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
+                    for (int part = 0; part < np; ++part) {
+                        const int u_lo = (np == 2) ? (part > iu_lo ? part : iu_lo) : iu_lo;
+                        const int u_hi = (np == 2) ? (part + 1 < iu_hi ? part + 1 : iu_hi) : iu_hi;
+                        // this issuer takes part in the part's barrier if it has a
+                        // unit there (always with np = 1)
+                        if (u_lo >= u_hi) continue;
+                        named_bar_sync(kBarSlot0 + a.idx * np + part, slot_cnt);  // part in TMEM
+                        for (int uu = u_lo; uu < u_hi; ++uu) {
+                            // with one B slot per sub-stage, a missing tail sub-stage
+                            // has no B slot (the loader skips it too)
+                            const bool has_b = !b_sub || uu < nsub;
+                            if (b_sub && has_b && ok)
+                                ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
+                            const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
+                            // release the part after its last block (to the team that
+                            // uses the slot next) and the B slot after its last use
+                            const bool last_u = (uu == u_hi - 1);
+                            const uint32_t rel_a = last_u ? bar_a_free + 8 * (next_team * np + part) : 0u;
+                            const bool last_b = b_sub || (part == np - 1 && uu == u_hi - 1);
+                            for (int g = ig; g < g_hi; ++g) {
+                                const bool last_g = (g == g_hi - 1);
+                                const uint32_t sub = b_sub ? (uint32_t)g
+                                                   : (KIND == 1) ? (uint32_t)uu
+                                                                 : (uint32_t)(kb_per_sub * uu + g);
+                                const uint32_t r1 = last_g ? rel_a : 0u;
+                                const uint32_t r2 =
+                                    (last_g && last_b && has_b) ? bar_b_empty + 8 * bq.idx : 0u;
+                                if (ok && uu < nsub) {
+                                    const uint64_t bd = smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
+                                    tc_fence_after();
+                                    mma_ts_f16_k64_commit(acc_col, a_st + uu * 64 + g * 32, bd, idesc,
+                                                          fresh ? 0u : 1u, r1, r2);
+                                    fresh = false;
+                                } else {
+                                    tc_commit2_elect(r1, r2);
+                                }
+                            }
+                            if (b_sub && has_b) bq.next();
                         }
-                        if (uhi <= iu_lo)  // no MMA of this issuer in the stage
-                            tc_commit2_elect(bar_a_free + 8 * next_team, bar_b_empty + 8 * bq.idx);
-                    } else {
-                        tc_commit2_elect(bar_a_free + 8 * next_team, bar_b_empty + 8 * bq.idx);
                     }
+                    if (!b_sub) bq.next();
                 }
                 tc_commit_elect(bar_acc_full + 8 * buf);
             }
@@ -523,9 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // them up once per block (these loads overlap the wait for the
                 // piece's MMAs) instead of as a dependent chain of global loads per
                 // column.  The barrier below orders these writes before the reads.
-                if (row < nr) {
-                    const int pair = p.sorted_ids[pos0 + row];
-                    col_tab[row] = make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
+                for (int col = row; col < nr; col += 128) {  // nr may exceed the 128 threads
+                    const int pair = p.sorted_ids[pos0 + col];
+                    col_tab[col] = make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
                 }
             }
             const bool u1 = !(kb1 - kb0 == 1 && stage_subs(kb0, p.KSS) == 1);
@@ -615,7 +662,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     for (int j0 = 0; j0 < nr; j0 += 16) {
                         float dv[16];
-                        if (ni == 4) {
+                        if (ni == 1) {
+                            tmem_ld_32x32b_x16_wait(tl + j0, dv);
+                        } else if (ni == 4) {
                             float d1[16];
                             tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, dv, d1);
 #pragma unroll
@@ -670,29 +719,56 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
     p.dq.c16th = 0x2C002C00u;  // fp16 1/16
     p.dq.cm72 = 0xD480D480u;   // fp16 -72
     const int BM = p.block_m;
-    if (BM < 16 || BM % 16 != 0 || BM > 128) return false;
-    // k blocks per B stage: gate/up two 64-wide blocks, down four
-    p.b_stage_bytes = (uint32_t)((kind == 1 ? 2 : 4) * BM * 128);
-    // MMA issuers (one accumulator each) and accumulator buffers: four issuers
-    // and two buffers where tensor memory still leaves two A stages, else two
-    // issuers with two buffers, else a single buffer (the issuers then wait for
-    // the epilogue at every piece end)
-    p.ni = 0;
-    const int opts[4][2] = {{4, 2}, {2, 2}, {4, 1}, {2, 1}};
-    for (int o = 0; o < 4 && !p.ni; ++o)
-        if (opts[o][0] * opts[o][1] * BM + 2 * (int)kACols <= kTmemCols) {
-            p.ni = opts[o][0];
-            p.nbuf = opts[o][1];
+    if (BM < 16 || BM % 16 != 0 || BM > 192) return false;
+    p.np = 1;
+    p.b_sub = 0;
+    int n_b;
+    if (BM <= 128) {
+        // k blocks per B stage: gate/up two 64-wide blocks, down four
+        p.b_stage_bytes = (uint32_t)((kind == 1 ? 2 : 4) * BM * 128);
+        // MMA issuers (one accumulator each) and accumulator buffers: four
+        // issuers and two buffers where tensor memory still leaves two A stages,
+        // else two issuers with two buffers, else a single buffer (the issuers
+        // then wait for the epilogue at every piece end)
+        p.ni = 0;
+        const int opts[4][2] = {{4, 2}, {2, 2}, {4, 1}, {2, 1}};
+        for (int o = 0; o < 4 && !p.ni; ++o)
+            if (opts[o][0] * opts[o][1] * BM + 2 * (int)kACols <= kTmemCols) {
+                p.ni = opts[o][0];
+                p.nbuf = opts[o][1];
+            }
+        if (!p.ni) return false;
+        p.n_a = (kTmemCols - p.nbuf * p.ni * BM) / (int)kACols;
+        if (p.n_a > 3) p.n_a = 3;            // one named barrier per A stage (ids 2..4)
+        if (p.n_a > kTeams) p.n_a = kTeams;  // a team's A-slot barrier stays within one phase
+        if (p.n_a < 2) return false;
+        n_b = (BM <= 32) ? 8 : (BM <= 64) ? 4 : 3;
+        if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;  // down stages carry four k blocks
+    } else {
+        // Wide blocks (up to 192 tokens: one pass over an expert's weights where
+        // 128-token blocks would need two).  gate/up: gate and up accumulators of
+        // BM columns leave room for one A stage, released per sub-stage half
+        // (np = 2) so the next stage's first half is written while this stage's
+        // second half is multiplied.  down: one issuer and one accumulator, two A
+        // stages, and B slots of one sub-stage (a whole 192-row stage of four
+        // k blocks would not fit in shared memory).
+        p.nbuf = 1;
+        if (kind == 1) {
+            p.ni = 2;
+            p.n_a = 1;
+            p.np = 2;
+            p.b_stage_bytes = (uint32_t)(2 * BM * 128);
+        } else {
+            p.ni = 1;
+            p.n_a = 2;
+            p.b_sub = 1;
+            p.b_stage_bytes = (uint32_t)(2 * BM * 128);
         }
-    if (!p.ni) return false;
-    p.n_a = (kTmemCols - p.nbuf * p.ni * BM) / (int)kACols;
-    if (p.n_a > 3) p.n_a = 3;            // one named barrier per A stage (ids 2..4)
-    if (p.n_a > kTeams) p.n_a = kTeams;  // a team's A-slot barrier stays within one phase
-    if (p.n_a < 2) return false;
+        if (p.nbuf * p.ni * BM + p.n_a * (int)kACols > kTmemCols) return false;
+        n_b = 3;
+    }
     const uint32_t limit = 227 * 1024 - 1024;  // opt-in maximum minus alignment slack
-    const uint32_t misc = 1024 + 16 + 128 * 8;  // barriers + words + column table
-    int n_b = (BM <= 32) ? 8 : (BM <= 64) ? 4 : 3;
-    if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;  // down stages carry four k blocks
+    const uint32_t misc = 1024 + 16 + 256 * 8;  // barriers + words + column table
     p.n_b = n_b;
     const uint32_t b_bytes = (uint32_t)n_b * p.b_stage_bytes;
     int n_w = (int)((limit - b_bytes - misc) / kStage);
@@ -708,26 +784,25 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
 
 cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_b, int grid,
                         cudaStream_t s, int *launches) {
-    static bool attr_done[64][2] = {};
+    const int wide = (p.np == 2 || p.b_sub) ? 1 : 0;
+    const int v = (kind - 1) * 2 + wide;  // instantiation index
+    static bool attr_done[64][4] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev][kind - 1]) {
-        cudaError_t e = (kind == 1)
-            ? cudaFuncSetAttribute(moe_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   227 * 1024)
-            : cudaFuncSetAttribute(moe_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   227 * 1024);
+    typedef void (*KernelFn)(const GemmParams, const CUtensorMap);
+    const KernelFn fns[4] = {moe_gemm_kernel<1, 0>, moe_gemm_kernel<1, 1>, moe_gemm_kernel<2, 0>,
+                             moe_gemm_kernel<2, 1>};
+    if (dev >= 0 && dev < 64 && !attr_done[dev][v]) {
+        cudaError_t e = cudaFuncSetAttribute(fns[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
         if (e != cudaSuccess) return e;
-        attr_done[dev][kind - 1] = true;
+        attr_done[dev][v] = true;
     }
     cudaLaunchConfig_t cfg = pdl_config((unsigned)grid, kThreads, p.smem_bytes, s);
     cudaLaunchAttribute attr;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl_attr(attr);
-    if (kind == 1)
-        cudaLaunchKernelEx(&cfg, moe_gemm_kernel<1>, p, *tmap_b);
-    else
-        cudaLaunchKernelEx(&cfg, moe_gemm_kernel<2>, p, *tmap_b);
+    cudaLaunchKernelEx(&cfg, fns[v], p, *tmap_b);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }

@@ -99,13 +99,15 @@ struct GemmParams {
     float *out_acc;            // down: fp32 accumulator [M][H]
     uint32_t *err;             // [2]
     int M, top_k, H, I, P;
-    int block_m;               // BM: routing block height (multiple of 16, <= 128)
+    int block_m;               // BM: routing block height (multiple of 16, <= 192)
     int RT;                    // row tiles per expert
     int KSS, KS;               // k sub-stages per tile (one 8 KB packed stage each) and
                                // pipeline stages per tile (two sub-stages, the last maybe one)
     int n_w, n_b, n_a;         // ring depths: weight stages, B stages, A (TMEM) stages
     int ni;                    // MMA-issuing warps (= accumulators per buffer): 4 or 2
     int nbuf;                  // accumulator buffers (pieces alternate between them)
+    int np;                    // A-slot release parts per stage: 1, or 2 (per sub-stage)
+    int b_sub;                 // 1: B ring slots hold one sub-stage (wide blocks)
     int split;                 // 1: partition k iterations evenly over CTAs
     uint32_t b_stage_bytes;
     uint32_t smem_b_off, smem_misc_off, smem_bytes;
