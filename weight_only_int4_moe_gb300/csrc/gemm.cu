@@ -218,9 +218,9 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 }  // namespace
 
-// WIDE: the wide-block configuration (blocks of 144..192 tokens): gate/up
-// releases A per sub-stage half (np = 2), down has one issuer and B slots of
-// one sub-stage.  Separate instantiations keep the common path's registers.
+// WIDE: the wide-block configuration (blocks of 144..192 tokens): A released
+// per sub-stage half (np = 2); down has one issuer and B slots of one
+// sub-stage.  Separate instantiations keep the common path's registers.
 template <int KIND, int WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_b) {
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a_free[t][part]: part `part` of the A slot of team t's next stage is free
     // (the MMAs of the stage n_a earlier on it are done); np = 2 releases each
     // sub-stage half of a slot on its own
-    constexpr int np = (WIDE && KIND == 1) ? 2 : 1;
+    constexpr int np = WIDE ? 2 : 1;
     constexpr bool b_sub = (WIDE && KIND == 2);
     const uint32_t bar_a_free = bar_b_empty + 8 * n_b;
     // acc_full[b] / acc_empty[b]: accumulator buffer b holds a finished piece /
@@ -746,23 +746,24 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
         if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;  // down stages carry four k blocks
     } else {
         // Wide blocks (up to 192 tokens: one pass over an expert's weights where
-        // 128-token blocks would need two).  gate/up: gate and up accumulators of
-        // BM columns leave room for one A stage, released per sub-stage half
-        // (np = 2) so the next stage's first half is written while this stage's
-        // second half is multiplied.  down: one issuer and one accumulator, two A
-        // stages, and B slots of one sub-stage (a whole 192-row stage of four
-        // k blocks would not fit in shared memory).
-        p.nbuf = 1;
+        // 128-token blocks would need two).  One A stage, released per sub-stage
+        // half (np = 2) so the next stage's first half is written while this
+        // stage's second half is multiplied.  gate/up: gate and up accumulators of
+        // BM columns.  down: one issuer, two buffers of one accumulator, and B
+        // slots of one sub-stage (a whole 192-row stage of four k blocks would not
+        // fit in shared memory).
+        p.n_a = 1;
+        p.np = 2;
+        p.b_stage_bytes = (uint32_t)(2 * BM * 128);
         if (kind == 1) {
             p.ni = 2;
-            p.n_a = 1;
-            p.np = 2;
-            p.b_stage_bytes = (uint32_t)(2 * BM * 128);
+            p.nbuf = 1;
         } else {
+            // one accumulator, so two buffers fit: the epilogue of one piece
+            // overlaps the MMAs of the next
             p.ni = 1;
-            p.n_a = 2;
+            p.nbuf = 2;
             p.b_sub = 1;
-            p.b_stage_bytes = (uint32_t)(2 * BM * 128);
         }
         if (p.nbuf * p.ni * BM + p.n_a * (int)kACols > kTmemCols) return false;
         n_b = 3;
