@@ -247,3 +247,27 @@ def test_bf16_output_is_rounded_fp32_output():
     assert m["rel_l1"] <= 5e-3
     # beyond the fp32 result's error, only the final rounding (half an ulp)
     assert np.all(np.abs(got - ref) <= 2e-2 * m["rms"] + 2.0 ** -8 * np.abs(ref))
+
+
+@pytest.mark.parametrize("E,k,H,I,M,seed,n_tok", [
+    # ~13 tokens per expert, block 32: gate/up 4 x ~130 tiles (one round-robin
+    # wave, then the split part), down 8 x ~130 (several waves); every token
+    (128, 8, 1024, 512, 200, 9, None),
+    # ~192 tokens per expert, wide blocks of 192: ~96 blocks, down 8 row tiles
+    # (four round-robin waves, then the split part); sampled tokens
+    (64, 8, 1024, 512, 1536, 10, 48),
+])
+def test_round_robin_waves_then_split(E, k, H, I, M, seed, n_tok):
+    """With at least two waves of tiles, whole waves go round-robin and the
+    remainder is split by stages; both parts must give the oracle's result."""
+    w, pw, t = setup(E, k, H, I, M, seed)
+    BM = _ops().moe_int4_block_m(M, pw.shape)
+    blocks = sum(-(-int(c) // BM) for c in np.bincount(t["topk_ids"].ravel(), minlength=E) if c)
+    assert blocks * (H // 128) >= 2 * 152  # the down GEMM has round-robin waves on GB300
+    got = gpu_forward(pw, t)
+    toks = None
+    if n_tok is not None:
+        toks = np.sort(np.random.default_rng(seed).choice(M, size=n_tok, replace=False))
+    ref = oracle_out(w, t, tokens=toks)
+    m = assert_parity(got if toks is None else got[toks], ref, f"E{E} M{M}")
+    print(BM, blocks, m)

@@ -367,7 +367,7 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     g.I = pl.I;
     g.P = pl.P;
     g.block_m = pl.BM;
-    g.split = 1;
+    g.round_robin = 1;
 
     GemmParams g1 = g;
     g1.wq = reinterpret_cast<const uint8_t *>(w13_packed);

@@ -32,10 +32,14 @@
 //    SiLU(g)*u in registers and writes the fp16 intermediate.  The down
 //    epilogue scales by the routing weight and adds into the fp32 [M][H]
 //    output (the top-k combine).
-//  * Work = (expert block, 128-row tile) x stages, split evenly over a persistent
-//    grid of one CTA per SM (a CTA's range may cut a tile).  A gate/up tile cut
-//    between CTAs is finished by whichever piece arrives last (partial sums in
-//    per-CTA slots + a counter); no CTA ever waits for another.
+//  * Work = (expert block, 128-row tile) x stages on a persistent grid of one
+//    CTA per SM.  Whole waves of tiles go round-robin (CTA c takes tiles c,
+//    c + G, ...), so the CTAs running at one time share a few expert blocks and
+//    re-read each block's B operand from L2 rather than from memory; the last
+//    one to two waves' worth of tiles is split evenly over the CTAs by stages
+//    (a CTA's range may cut a tile).  A gate/up tile cut between CTAs is
+//    finished by whichever piece arrives last (partial sums in per-CTA slots +
+//    a counter); no CTA ever waits for another.
 //
 // Warp roles (768 threads): 0 weight producer, 1 TMEM owner, 2 B loader,
 // 3 scale producer, 4-15 dequant (three teams), 16-19 MMA issue, 20-23
@@ -68,9 +72,15 @@ constexpr uint32_t kACols = 128;                // TMEM columns per A stage
 constexpr uint32_t kBarEpi = 1;     // the four epilogue warps
 constexpr uint32_t kBarSlot0 = 2;   // A stage s written: all dequant warps arrive, issuers wait
 
+// The schedule: tiles [0, rr) round-robin (whole tiles, CTA c takes c, c + G,
+// ...), then tiles [rr, tiles) split evenly by stages.  Stage indices of the
+// split part count from its first tile.  rr is a whole number of waves, one
+// fewer than fit, so the split part holds between G and 2G - 1 tiles and
+// balances the end; with fewer than 2G tiles everything is split.
 struct Sched {
-    long long start, end;  // stage range of this CTA (split mode)
-    int tiles, KS, G, cta, split;
+    long long start, end;  // this CTA's stage range within the split part
+    long long T;           // stages of the split part
+    int tiles, rr, KS, G, cta;
 };
 
 __device__ __forceinline__ Sched make_sched(const GemmParams &p) {
@@ -80,10 +90,11 @@ __device__ __forceinline__ Sched make_sched(const GemmParams &p) {
     s.KS = p.KS;
     s.G = gridDim.x;
     s.cta = blockIdx.x;
-    s.split = p.split;
-    const long long T = (long long)s.tiles * s.KS;
-    s.start = (T * s.cta) / s.G;
-    s.end = (T * (s.cta + 1)) / s.G;
+    const int waves = s.tiles / s.G;
+    s.rr = (p.round_robin && waves >= 2) ? (waves - 1) * s.G : 0;
+    s.T = (long long)(s.tiles - s.rr) * s.KS;
+    s.start = (s.T * s.cta) / s.G;
+    s.end = (s.T * (s.cta + 1)) / s.G;
     return s;
 }
 
@@ -95,25 +106,24 @@ struct PieceIter {
         next_tile = s.cta;
     }
     __device__ bool next(const Sched &s, int &tile, int &kb0, int &kb1) {
-        if (s.split) {
-            if (it >= s.end) return false;
-            tile = (int)(it / s.KS);
-            kb0 = (int)(it % s.KS);
-            const long long rem = s.end - it;
-            kb1 = (s.KS - kb0 <= rem) ? s.KS : kb0 + (int)rem;
-            it += kb1 - kb0;
+        if (next_tile < s.rr) {
+            tile = next_tile;
+            kb0 = 0;
+            kb1 = s.KS;
+            next_tile += s.G;
             return true;
         }
-        if (next_tile >= s.tiles) return false;
-        tile = next_tile;
-        kb0 = 0;
-        kb1 = s.KS;
-        next_tile += s.G;
+        if (it >= s.end) return false;
+        tile = s.rr + (int)(it / s.KS);
+        kb0 = (int)(it % s.KS);
+        const long long rem = s.end - it;
+        kb1 = (s.KS - kb0 <= rem) ? s.KS : kb0 + (int)rem;
+        it += kb1 - kb0;
         return true;
     }
 };
 
-// First stage index of CTA c and the CTA owning stage `it` (split mode).
+// First stage index of CTA c and the CTA owning stage `it` (split part).
 __device__ __forceinline__ long long range_start(long long T, int G, int c) {
     return (T * c) / G;
 }
@@ -557,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = wid & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const long long T = (long long)sched.tiles * sched.KS;
+        const long long T = sched.T;
         uint32_t c = 0;
         bool ok = true;
         while (pi.next(sched, tile, kb0, kb1)) {
@@ -588,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool full = (kb0 == 0 && kb1 == p.KS);
                     float *sl = nullptr;
                     if (!full) {
-                        const long long piece_start = (long long)tile * p.KS + kb0;
+                        const long long piece_start = (long long)(tile - sched.rr) * p.KS + kb0;
                         const int slot = (piece_start == sched.start) ? 0 : 1;
                         sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
                     }
@@ -640,7 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         named_bar_sync(kBarEpi, 128);
                         if (last) {
                             __threadfence();
-                            const long long ts = (long long)tile * p.KS, te = ts + p.KS;
+                            const long long ts = (long long)(tile - sched.rr) * p.KS,
+                                            te = ts + p.KS;
                             const int c_first = range_owner(T, sched.G, ts);
                             const int c_last = range_owner(T, sched.G, te - 1);
                             for (int jr = 0; jr < nr; ++jr) {

@@ -108,7 +108,8 @@ struct GemmParams {
     int nbuf;                  // accumulator buffers (pieces alternate between them)
     int np;                    // A-slot release parts per stage: 1, or 2 (per sub-stage)
     int b_sub;                 // 1: B ring slots hold one sub-stage (wide blocks)
-    int split;                 // 1: partition k iterations evenly over CTAs
+    int round_robin;           // 1: whole waves of tiles round-robin, the rest split by stages
+                               // (0: all split by stages)
     uint32_t b_stage_bytes;
     uint32_t smem_b_off, smem_misc_off, smem_bytes;
     DequantConsts dq;
