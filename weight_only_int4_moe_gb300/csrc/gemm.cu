@@ -620,14 +620,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
                         }
+                        if (full) {
+                            // all 16 SwiGLU values first (independent exp and
+                            // reciprocal chains overlap; columns past nr hold
+                            // finite or garbage values that are never stored),
+                            // then the stores of the real columns
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int jr = j0 + jj;
-                            if (jr < nr) {
-                                if (full) {
-                                    p.a_out[(size_t)(pos0 + jr) * p.I + feat] =
-                                        f16_sat(silu_mul(gv[jj], uv[jj]));
-                                } else {
+                            for (int jj = 0; jj < 16; ++jj) gv[jj] = silu_mul(gv[jj], uv[jj]);
+                            uint16_t *dst = p.a_out + (size_t)(pos0 + j0) * p.I + feat;
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj, dst += p.I)
+                                if (j0 + jj < nr) *dst = f16_sat(gv[jj]);
+                        } else {
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const int jr = j0 + jj;
+                                if (jr < nr) {
                                     sl[(size_t)jr * 128 + row] = gv[jj];
                                     sl[(size_t)(BM + jr) * 128 + row] = uv[jj];
                                 }
@@ -693,15 +701,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
                         }
+                        // the 16 columns' (token, weight) entries and products
+                        // first, then the reductions of the real columns (the
+                        // table has 256 entries, so j0 + 15 is in bounds)
+                        int tok[16];
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
-                            const int jr = j0 + jj;
-                            if (jr < nr) {
-                                const int2 tw = col_tab[jr];
-                                atomicAdd(p.out_acc + (size_t)tw.x * p.H + feat,
-                                          __int_as_float(tw.y) * dv[jj]);
-                            }
+                            const int2 tw = col_tab[j0 + jj];
+                            tok[jj] = tw.x;
+                            dv[jj] *= __int_as_float(tw.y);
                         }
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (j0 + jj < nr) atomicAdd(p.out_acc + (size_t)tok[jj] * p.H + feat, dv[jj]);
                     }
                     tc_fence_before();
                     __syncwarp();
