@@ -49,6 +49,7 @@ SMALL = [
     (32, 8, 1024, 384, 5, 6),     # many k stages per tile, stream-K splits
     (4, 2, 1024, 384, 300, 7),    # ~150 tokens per expert -> wide block 192, odd down k tail
     (8, 2, 256, 128, 500, 8),     # ~125 tokens per expert -> wide block 176
+    (4, 2, 384, 256, 300, 11),    # wide block 192, three down row tiles
 ]
 
 
