@@ -213,15 +213,15 @@ __device__ __forceinline__ uint16_t f16_sat(float v) {
     return __half_as_ushort(__float2half_rn(v));
 }
 
-// SiLU(g) * u = g / (1 + e^-g) * u.  The fast divide is within a few ulp of
-// the IEEE one (its result is rounded to fp16 next) and gives g * 0 = -0 when
-// e^-g overflows for very negative g.
 // Issuing warps that take part in (and release) one A part of a stage: with
 // four issuers (one per slab x sub-stage) a sub-stage part has two of them.
 __host__ __device__ __forceinline__ int part_issuers(int ni, int np) {
     return (ni == 4) ? 4 / np : ni;
 }
 
+// SiLU(g) * u = g / (1 + e^-g) * u.  The fast divide is within a few ulp of
+// the IEEE one (its result is rounded to fp16 next) and gives g * 0 = -0 when
+// e^-g overflows for very negative g.
 __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
