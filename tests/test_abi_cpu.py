@@ -44,6 +44,16 @@ def test_sizes_and_policy():
     sh = ops.Shape.of(384, 8, 7168, 2048)
     assert ops.moe_int4_block_m(1, sh) == 16
     assert ops.moe_int4_block_m(8192, sh) == 192  # ~170 tokens per expert: one wide block
+    mid = ops.Shape.of(64, 6, 4096, 1408)
+    # ~192 tokens per expert: two blocks per expert whether 128 or 192 rows high,
+    # so the 128-row kernel; ~768: five wide blocks instead of seven
+    assert ops.moe_int4_block_m(2048, mid) == 128
+    assert ops.moe_int4_block_m(8192, mid) == 192
+    for M in range(1, 20000, 37):  # a wide block only where it saves a pass
+        bm = ops.moe_int4_block_m(M, mid)
+        if bm > 128:
+            n = M * 6 / 64 * 1.05
+            assert -(-n // 192) < -(-n // 128)
     for M in (1, 9, 90, 256, 1024, 8192):
         bm = ops.moe_int4_block_m(M, sh)
         assert 16 <= bm <= 192 and bm % 16 == 0

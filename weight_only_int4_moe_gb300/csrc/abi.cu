@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "moe_int4.h"
@@ -42,6 +43,15 @@ int choose_block_m(long long P, int E) {
     bm = (bm + 15) / 16 * 16;
     if (bm < 16) bm = 16;
     if (bm > 192) bm = 192;
+    if (bm > 128) {
+        // A wide block (144..192 rows) pays off only where it saves a pass over
+        // an expert's weights: where a typical expert (its mean count plus a
+        // little) needs fewer 192-row blocks than 128-row ones.  Otherwise the
+        // extra blocks are short tails either way and the 128-row kernel, with
+        // its deeper A ring, is faster.
+        const double n = avg * 1.05;
+        if (std::ceil(n / 192.0) >= std::ceil(n / 128.0)) bm = 128;
+    }
     return bm;
 }
 
