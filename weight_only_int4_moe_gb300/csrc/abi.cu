@@ -337,11 +337,11 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     al.err = err;
     al.chunk_tab = reinterpret_cast<int32_t *>(ws + pl.off_chunk);
     al.n_chunks = pl.n_chunks;
+    // the align launch zeroes the gate/up split counters; the gate/up GEMM
+    // zeroes the down accumulator (off the align's critical path)
     ZeroArgs z{};
     z.ptr[0] = ws + pl.off_cnt;
     z.n16[0] = (pl.tiles1_cap * 4 + 15) / 16;
-    z.ptr[1] = acc;
-    z.n16[1] = (size_t)pl.M * pl.H * 4 / 16;
     uint16_t *x16 = reinterpret_cast<uint16_t *>(ws + pl.off_x16);
     const size_t zero_bytes = (z.n16[0] + z.n16[1]) * 16;
     int zero_ctas = (int)(zero_bytes / (64 * 1024));
@@ -380,6 +380,8 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     g.round_robin = 1;
 
     GemmParams g1 = g;
+    g1.zero_out = reinterpret_cast<float4 *>(acc);
+    g1.zero_n16 = (size_t)pl.M * pl.H * 4 / 16;
     g1.wq = reinterpret_cast<const uint8_t *>(w13_packed);
     g1.wsc = reinterpret_cast<const uint8_t *>(w13_scales);
     g1.a_out = a_buf;

@@ -354,6 +354,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(bar_w_full + 8 * (j % n_w), (j / n_w) & 1, &never, nullptr);
             }
         }
+    } else if (wid == 1) {
+        // ------------------------------------------- output zeroing (gate/up) --
+        // The tensor-memory owner has nothing to do until the end, so it clears
+        // the down GEMM's fp32 accumulator, a grid-strided share per CTA, while
+        // the weights stream.  Streaming stores: the zero lines should not push
+        // the B rows that other row tiles re-read out of L2.  The down GEMM
+        // reads the accumulator only after this grid has completed.
+        if (p.zero_out) {
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            const size_t stride = (size_t)gridDim.x * 32;
+            for (size_t i = (size_t)blockIdx.x * 32 + lane; i < p.zero_n16; i += stride)
+                __stcs(p.zero_out + i, z4);
+        }
     } else if (wid == 2) {
         // ------------------------------------------------------ B loader --
         // B rows of the block (bucketed order) by 2-D TMA tensor copies: one

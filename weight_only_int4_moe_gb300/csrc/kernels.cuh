@@ -97,6 +97,8 @@ struct GemmParams {
     float *partial;            // gate/up split slots [G][2][2][BM][128]
     int32_t *tile_cnt;         // gate/up split counters [tiles]
     float *out_acc;            // down: fp32 accumulator [M][H]
+    float4 *zero_out;          // gate/up: zeroes these zero_n16 16-byte units (the down
+    size_t zero_n16;           // GEMM's accumulator) on the side; null: nothing
     uint32_t *err;             // [2]
     int M, top_k, H, I, P;
     int block_m;               // BM: routing block height (multiple of 16, <= 192)
