@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *w_tag = reinterpret_cast<volatile uint32_t *>(smem + (misc - base) + 512);
     // down epilogue: (token, routing weight) of each column of the current block
     int2 *col_tab = reinterpret_cast<int2 *>(smem + (misc - base) + 1024);
+    // wide down epilogue: per epilogue warp, 8 columns x 32 rows of fp32 to
+    // turn into float4s of 4 rows of one column (after the column table)
+    float *epi_stage = reinterpret_cast<float *>(smem + (misc - base) + 1024 + 256 * 8);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < n_w; ++i) {
@@ -714,19 +717,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
                         }
-                        // the 16 columns' (token, weight) entries and products
-                        // first, then the reductions of the real columns (the
-                        // table has 256 entries, so j0 + 15 is in bounds)
-                        int tok[16];
+                        if (b_sub) {
+                            // Wide blocks: a lane's 16 values are one row (output
+                            // feature) of 16 columns (tokens), and a scalar add per
+                            // value is one reduction request per column per warp.
+                            // Through shared memory, each lane instead adds a float4:
+                            // 4 consecutive features of one token, a quarter of the
+                            // requests.  8 columns at a time (1 KB per warp).
+                            float *stg = epi_stage + q * 256;
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int2 tw = col_tab[j0 + jj];
-                            tok[jj] = tw.x;
-                            dv[jj] *= __int_as_float(tw.y);
+                            for (int jj = 0; jj < 16; ++jj)
+                                dv[jj] *= __int_as_float(col_tab[j0 + jj].y);
+#pragma unroll
+                            for (int h = 0; h < 16; h += 8) {
+#pragma unroll
+                                for (int jj = 0; jj < 8; ++jj) stg[jj * 32 + lane] = dv[h + jj];
+                                __syncwarp();
+#pragma unroll
+                                for (int rr = 0; rr < 2; ++rr) {
+                                    const int idx = rr * 32 + lane;  // (column, 4-row group)
+                                    const int jt = idx >> 3, f4 = idx & 7;
+                                    const int jr = j0 + h + jt;
+                                    const float4 v4 =
+                                        *reinterpret_cast<const float4 *>(stg + jt * 32 + 4 * f4);
+                                    if (jr < nr)
+                                        atomicAdd(reinterpret_cast<float4 *>(
+                                                      p.out_acc + (size_t)col_tab[jr].x * p.H +
+                                                      r * kSlabRows + q * 32 + 4 * f4),
+                                                  v4);
+                                }
+                                __syncwarp();
+                            }
+                        } else {
+                            // the 16 columns' (token, weight) entries and products
+                            // first, then the reductions of the real columns (the
+                            // table has 256 entries, so j0 + 15 is in bounds)
+                            int tok[16];
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const int2 tw = col_tab[j0 + jj];
+                                tok[jj] = tw.x;
+                                dv[jj] *= __int_as_float(tw.y);
+                            }
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (j0 + jj < nr)
+                                    atomicAdd(p.out_acc + (size_t)tok[jj] * p.H + feat, dv[jj]);
                         }
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            if (j0 + jj < nr) atomicAdd(p.out_acc + (size_t)tok[jj] * p.H + feat, dv[jj]);
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -805,7 +842,8 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
         n_b = 3;
     }
     const uint32_t limit = 227 * 1024 - 1024;  // opt-in maximum minus alignment slack
-    const uint32_t misc = 1024 + 16 + 256 * 8;  // barriers + words + column table
+    // barriers + words + column table (+ the wide down epilogue's staging)
+    const uint32_t misc = 1024 + 256 * 8 + 16 + ((kind == 2 && p.b_sub) ? 4 * 1024 : 0);
     p.n_b = n_b;
     const uint32_t b_bytes = (uint32_t)n_b * p.b_stage_bytes;
     int n_w = (int)((limit - b_bytes - misc) / kStage);
