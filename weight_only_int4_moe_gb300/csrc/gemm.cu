@@ -273,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *w_tag = reinterpret_cast<volatile uint32_t *>(smem + (misc - base) + 512);
     // down epilogue: (token, routing weight) of each column of the current block
     int2 *col_tab = reinterpret_cast<int2 *>(smem + (misc - base) + 1024);
-    // wide down epilogue: per epilogue warp, 8 columns x 32 rows of fp32 to
-    // turn into float4s of 4 rows of one column (after the column table)
+    // down epilogue (epi_f4): per epilogue warp, 8 columns x 32 rows of fp32
+    // to turn into float4s of 4 rows of one column (after the column table)
     float *epi_stage = reinterpret_cast<float *>(smem + (misc - base) + 1024 + 256 * 8);
 
     if (threadIdx.x == 0) {
@@ -717,13 +717,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
                         }
-                        if (b_sub) {
-                            // Wide blocks: a lane's 16 values are one row (output
-                            // feature) of 16 columns (tokens), and a scalar add per
-                            // value is one reduction request per column per warp.
-                            // Through shared memory, each lane instead adds a float4:
-                            // 4 consecutive features of one token, a quarter of the
-                            // requests.  8 columns at a time (1 KB per warp).
+                        if (b_sub || p.epi_f4) {
+                            // A lane's 16 values are one row (output feature) of 16
+                            // columns (tokens), and a scalar add per value is one
+                            // reduction request per column per warp.  Through shared
+                            // memory, each lane instead adds a float4: 4 consecutive
+                            // features of one token, a quarter of the requests.  8
+                            // columns at a time (1 KB per warp).
                             float *stg = epi_stage + q * 256;
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj)
@@ -842,12 +842,19 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
         n_b = 3;
     }
     const uint32_t limit = 227 * 1024 - 1024;  // opt-in maximum minus alignment slack
-    // barriers + words + column table (+ the wide down epilogue's staging)
-    const uint32_t misc = 1024 + 256 * 8 + 16 + ((kind == 2 && p.b_sub) ? 4 * 1024 : 0);
     p.n_b = n_b;
     const uint32_t b_bytes = (uint32_t)n_b * p.b_stage_bytes;
-    int n_w = (int)((limit - b_bytes - misc) / kStage);
-    if (n_w > 10) n_w = 10;
+    // barriers + words + column table, and for the down GEMM the epilogue's
+    // float4 staging (4 KB) wherever it costs no weight-ring stage (always
+    // with wide blocks, whose epilogue has no other path)
+    const uint32_t misc0 = 1024 + 256 * 8 + 16, stage_bytes = 4 * 1024;
+    auto ring = [&](uint32_t misc_bytes) {
+        const int n = (int)((limit - b_bytes - misc_bytes) / kStage);
+        return n > 10 ? 10 : n;
+    };
+    p.epi_f4 = (kind == 2 && (p.b_sub || ring(misc0 + stage_bytes) == ring(misc0))) ? 1 : 0;
+    const uint32_t misc = misc0 + (p.epi_f4 ? stage_bytes : 0u);
+    const int n_w = ring(misc);
     if (n_w < 3) return false;
     p.n_w = n_w;
     const uint32_t w_bytes = (uint32_t)n_w * kStage;

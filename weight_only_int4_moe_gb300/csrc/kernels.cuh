@@ -110,6 +110,7 @@ struct GemmParams {
     int nbuf;                  // accumulator buffers (pieces alternate between them)
     int np;                    // A-slot release parts per stage: 1, or 2 (per sub-stage)
     int b_sub;                 // 1: B ring slots hold one sub-stage (wide blocks)
+    int epi_f4;                // down: combine through shared memory as float4 adds
     int round_robin;           // 1: whole waves of tiles round-robin, the rest split by stages
                                // (0: all split by stages)
     uint32_t b_stage_bytes;
