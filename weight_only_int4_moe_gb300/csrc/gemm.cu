@@ -226,6 +226,27 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+// Gate/up epilogue of a full piece with one accumulator per slab (gate at
+// column tl, up at tl + BM): SiLU(g) * u of accumulator columns [j_lo, j_hi)
+// of this warp's lane quadrant, written as the fp16 intermediate rows
+// a_row0 + column * I (columns >= nr are not stored).
+__device__ __forceinline__ void swiglu_store(uint32_t tl, int BM, int j_lo, int j_hi, int nr,
+                                             uint16_t *a_row0, int I) {
+    for (int j0 = j_lo; j0 < j_hi; j0 += 16) {
+        float gv[16], uv[16];
+        tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
+        // all 16 SwiGLU values first (independent exp and reciprocal chains
+        // overlap; columns past nr hold finite or garbage values that are
+        // never stored), then the stores of the real columns
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) gv[jj] = silu_mul(gv[jj], uv[jj]);
+        uint16_t *dst = a_row0 + (size_t)j0 * I;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj, dst += I)
+            if (j0 + jj < nr) *dst = f16_sat(gv[jj]);
+    }
+}
+
 }  // namespace
 
 // WIDE: the wide-block configuration (blocks of 144..192 tokens): A released
@@ -258,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sub-stage half of a slot on its own
     constexpr int np = WIDE ? 2 : 1;
     constexpr bool b_sub = (WIDE && KIND == 2);
+    // Wide gate/up has one accumulator buffer, so its MMAs wait for every
+    // piece's epilogue; the four issuing warps (one per lane quadrant, idle then)
+    // take the upper half of a full piece's columns.
+    constexpr bool kHelp = (WIDE && KIND == 1);
     const uint32_t bar_a_free = bar_b_empty + 8 * n_b;
     // acc_full[b] / acc_empty[b]: accumulator buffer b holds a finished piece /
     // has been read by the epilogue (buffers alternate between pieces)
@@ -290,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < n_w; ++i) w_tag[i] = 0xFFFFFFFFu;
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_acc_full + 8 * i, ni);
-            mbar_init(bar_acc_empty + 8 * i, 4);
+            mbar_init(bar_acc_empty + 8 * i, kHelp ? 8 : 4);
         }
         mbar_init(bar_drain, ni);
         *abort_flag = 0;
@@ -569,6 +594,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit_elect(bar_acc_full + 8 * buf);
             }
+            if (kHelp) {
+                // the upper half of a full piece's columns; every issuing warp
+                // arrives on acc_empty once per piece (full or not)
+                const uint32_t buf = c % (uint32_t)nbuf;
+                const bool got = warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag,
+                                           p.err, 32);
+                if (got) {
+                    tc_fence_after();
+                    if (kb0 == 0 && kb1 == p.KS) {
+                        const int hq = wid & 3;
+                        const int half = ((nr + 31) / 32) * 16;
+                        swiglu_store(tmem + ((uint32_t)(hq * 32) << 16) + buf * acc_buf_cols, BM,
+                                     half, nr, nr,
+                                     p.a_out + (size_t)pos0 * p.I + (tile % p.RT) * kSlabRows +
+                                         hq * 32 + lane,
+                                     p.I);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
+                }
+            }
             ++c;
         }
         if (issuer) {  // every MMA of this CTA must finish before TMEM is released
@@ -618,7 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int slot = (piece_start == sched.start) ? 0 : 1;
                         sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
                     }
-                    for (int j0 = 0; j0 < nr; j0 += 16) {
+                    // wide: the issuing warps take columns [half, nr) of a full piece
+                    const int j_end = (kHelp && full) ? ((nr + 31) / 32) * 16 : nr;
+                    for (int j0 = 0; j0 < j_end; j0 += 16) {
                         float gv[16], uv[16];
                         if (ni == 4) {
                             // accumulator of (slab g, sub-stage u) is column (2g + u) * BM
