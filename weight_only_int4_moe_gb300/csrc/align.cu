@@ -123,6 +123,14 @@ __device__ void zero_regions(const ZeroArgs &z, int cta, int nctas) {
 // Rows of x in bucketed order, as the fp16 tensor-core operand of the gate/up
 // GEMM: xs[pos] = fp16(x[sorted_ids[pos] / top_k]) for every real entry (pad
 // rows are left as they are; the GEMM ignores their results).  One warp per row.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_sat(uint4 v) {
+    v.x = bf16x2_to_f16x2_sat(v.x);
+    v.y = bf16x2_to_f16x2_sat(v.y);
+    v.z = bf16x2_to_f16x2_sat(v.z);
+    v.w = bf16x2_to_f16x2_sat(v.w);
+    return v;
+}
+
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ sorted,
                                    const int32_t *__restrict__ num_post_pad, int P, int top_k, int H,
                                    uint16_t *__restrict__ xs) {
@@ -137,14 +145,16 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t
         if (pair >= P) continue;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(pair / top_k) * H);
         uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)pos * H);
-        for (int c = lane; c < n8; c += 32) {
-            uint4 v = src[c];
-            v.x = bf16x2_to_f16x2_sat(v.x);
-            v.y = bf16x2_to_f16x2_sat(v.y);
-            v.z = bf16x2_to_f16x2_sat(v.z);
-            v.w = bf16x2_to_f16x2_sat(v.w);
-            dst[c] = v;
+        // four 16-byte loads in flight per lane (a row is H / 256 of them per lane)
+        int c = lane;
+        for (; c + 96 < n8; c += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = src[c + 32 * u];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dst[c + 32 * u] = bf16x8_to_f16x8_sat(v[u]);
         }
+        for (; c < n8; c += 32) dst[c] = bf16x8_to_f16x8_sat(src[c]);
     }
 }
 
