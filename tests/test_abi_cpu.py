@@ -44,6 +44,9 @@ def test_sizes_and_policy():
     sh = ops.Shape.of(384, 8, 7168, 2048)
     assert ops.moe_int4_block_m(1, sh) == 16
     assert ops.moe_int4_block_m(8192, sh) == 192  # ~170 tokens per expert: one wide block
+    # 2 x mean + 8: the verify batches' busier experts (skewed routing, ~2.5x the
+    # mean) fit one block
+    assert [ops.moe_int4_block_m(M, sh) for M in (90, 256, 512, 1024)] == [16, 32, 32, 64]
     mid = ops.Shape.of(64, 6, 4096, 1408)
     # ~192 tokens per expert: two blocks per expert whether 128 or 192 rows high,
     # so the 128-row kernel; ~768: five wide blocks instead of seven

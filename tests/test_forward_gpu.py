@@ -48,8 +48,14 @@ SMALL = [
     (64, 6, 512, 256, 700, 5),    # P = 4200 -> multi-block align
     (32, 8, 1024, 384, 5, 6),     # many k stages per tile, stream-K splits
     (4, 2, 1024, 384, 300, 7),    # ~150 tokens per expert -> wide block 192, odd down k tail
-    (8, 2, 256, 128, 500, 8),     # ~125 tokens per expert -> wide block 176
+    (8, 2, 256, 128, 500, 8),     # ~125 tokens per expert -> wide block 192
     (4, 2, 384, 256, 300, 11),    # wide block 192, three down row tiles
+    # narrow block heights 48..112: each tensor-memory plan, scalar and float4 combines
+    (16, 4, 384, 256, 64, 12),    # block 48
+    (16, 4, 384, 256, 96, 13),    # block 64 (scalar combine)
+    (8, 2, 256, 128, 128, 14),    # block 80
+    (8, 2, 256, 128, 160, 15),    # block 96 (scalar combine)
+    (8, 2, 512, 256, 192, 16),    # block 112 (scalar combine)
 ]
 
 
