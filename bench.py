@@ -211,6 +211,12 @@ def allreduce_max(dist, value, use_gpu):
     return float(t.item())
 
 
+def job_rate(world, units_per_step, step_seconds_max):
+    """Whole-job throughput of `world` replicas that each process units_per_step
+    per step: every rank's units over the slowest rank's step time."""
+    return world * units_per_step / step_seconds_max
+
+
 # ------------------------------------------------------------ CPU oracle --
 def time_oracle(w, cfg, Ms, target_s, threads, state=None):
     """Times the oracle on a bounded sample: rounds of `threads` tokens (one per
@@ -367,7 +373,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
     ms_per_step = sum(r["ms"] for r in rec) / args.steps
     ms_per_step_max = allreduce_max(dist, ms_per_step, True)
     tokens_per_step = sum(Ms)
-    value = world * tokens_per_step / (ms_per_step_max / 1e3)
+    value = job_rate(world, tokens_per_step, ms_per_step_max / 1e3)
 
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -458,7 +464,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
                                           shape, ws_io)
                 e2e_s += time.perf_counter() - t0
         e2e_step = allreduce_max(dist, e2e_s / args.steps, True)
-        e2e = {"value": world * tokens_per_step / e2e_step, "unit": "tokens/s",
+        e2e = {"value": job_rate(world, tokens_per_step, e2e_step), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_step * 1e3}
 
