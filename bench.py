@@ -76,21 +76,32 @@ def expert_bytes(H, I):
 GEMM_SOURCES = ("gemm.cu", "kernels.cuh", "common.cuh")
 
 
+def kernel_source_hash():
+    """sha256 of the GEMM kernel sources without their // comments and blank
+    lines: a code change invalidates a stored ncu capture, a comment edit does
+    not (the sources have no block comments and no // inside strings)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "weight_only_int4_moe_gb300", "csrc", name)) as f:
+            for line in f:
+                code = re.sub(r"//.*$", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
+    return h.hexdigest()
+
+
 def kernel_traffic(kernel, workload, bytes_per_launch):
     """DRAM traffic per launch of `kernel`, from the committed ncu summary of a
     smaller case of the same kernel, scaled by algorithmic bytes.  None when no
     summary exists or the kernel's source changed since it was captured."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.json")
     if not os.path.exists(path):
         return None, "no ncu summary for this kernel and workload"
     with open(path) as f:
         d = json.load(f)
-    h = hashlib.sha256()
-    for name in GEMM_SOURCES:
-        with open(os.path.join(ROOT, "weight_only_int4_moe_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != d.get("kernel_source_sha256"):
+    if kernel_source_hash() != d.get("kernel_source_sha256"):
         return None, "kernel changed since the ncu capture"
     ratio = float(d["traffic_per_algorithmic_byte"])
     return ratio * bytes_per_launch, (f"ncu dram bytes of {d['captured_case']}: "

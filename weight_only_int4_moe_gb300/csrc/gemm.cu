@@ -31,7 +31,11 @@
 //    128 intermediate features in the same lanes, so the epilogue forms
 //    SiLU(g)*u in registers and writes the fp16 intermediate.  The down
 //    epilogue scales by the routing weight and adds into the fp32 [M][H]
-//    output (the top-k combine).
+//    output (the top-k combine), through shared memory as float4 adds (four
+//    features of one token per lane) where there is room: a lane holds one
+//    feature of many tokens, and scalar adds would cost one reduction request
+//    per token.  Wide gate/up (one accumulator buffer) has the idle issuing
+//    warps take half of each full piece's SwiGLU columns.
 //  * Work = (expert block, 128-row tile) x stages on a persistent grid of one
 //    CTA per SM.  Whole waves of tiles go round-robin (CTA c takes tiles c,
 //    c + G, ...), so the CTAs running at one time share a few expert blocks and
@@ -41,9 +45,9 @@
 //    finished by whichever piece arrives last (partial sums in per-CTA slots +
 //    a counter); no CTA ever waits for another.
 //
-// Warp roles (768 threads): 0 weight producer, 1 TMEM owner, 2 B loader,
-// 3 scale producer, 4-15 dequant (three teams), 16-19 MMA issue, 20-23
-// epilogue.  Each (slab, sub-stage) has its own issuing warp and accumulator
+// Warp roles (768 threads): 0 weight producer, 1 TMEM owner (in gate/up it
+// also zeroes the down GEMM's fp32 accumulator), 2 B loader, 3 scale producer,
+// 4-15 dequant (three teams), 16-19 MMA issue, 20-23 epilogue.  Each (slab, sub-stage) has its own issuing warp and accumulator
 // (the epilogue sums them): one thread issuing tcgen05.mma waits tens of
 // cycles per instruction while MMAs from several warps overlap.  Every
 // mbarrier wait is bounded (MOE_DEVERR_TIMEOUT).
