@@ -62,6 +62,9 @@ enum {
 /* Device-side error flags (bit set), read with moe_int4_get_errors. */
 #define MOE_DEVERR_BAD_EXPERT_ID 0x1u /* a topk_ids entry outside [0, E) was dropped */
 #define MOE_DEVERR_TIMEOUT 0x2u       /* a pipeline wait gave up (kernel bug guard) */
+#define MOE_DEVERR_BOUNDS 0x4u        /* debug-bounds builds only (-DMOE_DEBUG_BOUNDS): an index
+                                         read back from a routing buffer was out of range; the
+                                         access was kept in bounds and the result is invalid */
 
 /* Output element types (moe_int4_shape.out_dtype). */
 #define MOE_OUT_BF16 0 /* bf16, rounded to nearest even from the fp32 combine */

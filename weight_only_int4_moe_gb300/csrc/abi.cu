@@ -366,7 +366,7 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     } else if (launch_align(al, z, zero_ctas, s, &launches) != cudaSuccess) {
         return MOE_ERR_CUDA;
     }
-    if (launch_gather_rows(x, sorted, npp, pl.P, pl.k, pl.H, x16, pl.cap, sms, s, &launches) !=
+    if (launch_gather_rows(x, sorted, npp, pl.P, pl.k, pl.H, x16, pl.cap, err, sms, s, &launches) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     prof_record(1, s);
@@ -382,6 +382,8 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     g.H = pl.H;
     g.I = pl.I;
     g.P = pl.P;
+    g.E = pl.E;
+    g.cap = pl.cap > (size_t)INT32_MAX ? INT32_MAX : (int)pl.cap;
     g.block_m = pl.BM;
     g.round_robin = 1;
 

@@ -133,16 +133,18 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8_sat(uint4 v) {
 
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ sorted,
                                    const int32_t *__restrict__ num_post_pad, int P, int top_k, int H,
-                                   uint16_t *__restrict__ xs) {
+                                   uint16_t *__restrict__ xs, int cap, uint32_t *err) {
     pdl_wait();  // sorted_ids and num_post_pad come from the align launch
     pdl_launch_dependents();
-    const int npp = *num_post_pad;
+    int npp = *num_post_pad;
+    if (!bounds_ok(npp >= 0 && npp <= cap, err)) npp = 0;
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     const int n8 = H / 8;
     for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < npp; pos += warps) {
         const int pair = sorted[pos];
-        if (pair >= P) continue;
+        if (pair >= P) continue;  // a pad
+        if (!bounds_ok(pair >= 0, err)) continue;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(pair / top_k) * H);
         uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)pos * H);
         // four 16-byte loads in flight per lane (a row is H / 256 of them per lane)
@@ -159,8 +161,8 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t
 }
 
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const int32_t *npp, int P,
-                               int top_k, int H, uint16_t *xs, size_t cap_rows, int sms,
-                               cudaStream_t s, int *launches) {
+                               int top_k, int H, uint16_t *xs, size_t cap_rows, uint32_t *err,
+                               int sms, cudaStream_t s, int *launches) {
     size_t blocks = (cap_rows + 7) / 8;  // 8 warps (rows) per block
     if (blocks > (size_t)sms * 8) blocks = (size_t)sms * 8;
     if (blocks < 1) blocks = 1;
@@ -168,7 +170,8 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const i
     cudaLaunchAttribute attr;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl_attr(attr);
-    cudaLaunchKernelEx(&cfg, gather_rows_kernel, x, sorted, npp, P, top_k, H, xs);
+    const int cap = cap_rows > (size_t)INT32_MAX ? INT32_MAX : (int)cap_rows;
+    cudaLaunchKernelEx(&cfg, gather_rows_kernel, x, sorted, npp, P, top_k, H, xs, cap, err);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }

@@ -14,11 +14,29 @@ namespace moe {
 // Error word layout inside the workspace (uint32[2]): flags, dropped-pair count.
 constexpr uint32_t kErrBadExpert = 0x1u;
 constexpr uint32_t kErrTimeout = 0x2u;
+constexpr uint32_t kErrBounds = 0x4u;
+
+// Debug-bounds builds (-DMOE_DEBUG_BOUNDS) check the indices that kernels read
+// back from the routing buffers (block count, expert ids, pair ids) before using
+// them: a failed check records kErrBounds and the caller substitutes an
+// in-range index, so no access leaves its buffer and no pipeline wait is left
+// unanswered.  Other builds compile the checks away (bounds_ok is true).
+#ifdef MOE_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
 
 // A pipeline wait that takes longer than this many SM cycles (about 2 s at the
 // GB300's 2.07 GHz maximum clock) is treated as a kernel bug: the waiting role
 // records kErrTimeout and the CTA winds down.
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
+
+MOE_DEV bool bounds_ok(bool in_range, uint32_t *err) {
+    if (!kDebugBounds) return true;
+    if (!in_range && err) atomicOr(err, kErrBounds);
+    return in_range;
+}
 
 MOE_DEV uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

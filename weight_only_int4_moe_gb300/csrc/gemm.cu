@@ -89,7 +89,8 @@ struct Sched {
 
 __device__ __forceinline__ Sched make_sched(const GemmParams &p) {
     Sched s;
-    const int npp = *p.num_post_pad;
+    int npp = *p.num_post_pad;
+    if (!bounds_ok(npp >= 0 && npp <= p.cap && npp % p.block_m == 0, p.err)) npp = 0;
     s.tiles = (npp / p.block_m) * p.RT;
     s.KS = p.KS;
     s.G = gridDim.x;
@@ -386,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             while (ok && pi.next(sched, tile, kb0, kb1)) {
                 const int b = tile / p.RT, r = tile % p.RT;
-                const int e = p.expert_ids[b];
+                int e = p.expert_ids[b];
+                if (!bounds_ok(e >= 0 && e < p.E, p.err)) e = 0;
                 const size_t sub0 = ((size_t)e * p.RT + r) * kss;  // first sub-stage of the tile
                 for (int j = kb0; j < kb1; ++j, ++i, w.next()) {
                     if (!mbar_wait(bar_w_empty + 8 * w.idx, w.ph ^ 1, abort_flag, p.err, 128)) {
@@ -684,7 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // piece's MMAs) instead of as a dependent chain of global loads per
                 // column.  The barrier below orders these writes before the reads.
                 for (int col = row; col < nr; col += 128) {  // nr may exceed the 128 threads
-                    const int pair = p.sorted_ids[pos0 + col];
+                    int pair = p.sorted_ids[pos0 + col];
+                    if (!bounds_ok(pair >= 0 && pair < p.P, p.err)) pair = 0;
                     col_tab[col] = make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
                 }
             }

@@ -61,8 +61,8 @@ cudaError_t launch_route_align(const RouteArgs &r, const AlignArgs &a, const Zer
 cudaError_t launch_align(const AlignArgs &a, const ZeroArgs &z, int zero_ctas, cudaStream_t s,
                          int *launches);
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const int32_t *npp, int P,
-                               int top_k, int H, uint16_t *xs, size_t cap_rows, int sms,
-                               cudaStream_t s, int *launches);
+                               int top_k, int H, uint16_t *xs, size_t cap_rows, uint32_t *err,
+                               int sms, cudaStream_t s, int *launches);
 cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, cudaStream_t s,
                             int *launches);
 cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
@@ -100,7 +100,8 @@ struct GemmParams {
     float4 *zero_out;          // gate/up: zeroes these zero_n16 16-byte units (the down
     size_t zero_n16;           // GEMM's accumulator) on the side; null: nothing
     uint32_t *err;             // [2]
-    int M, top_k, H, I, P;
+    int M, top_k, H, I, P, E;
+    int cap;                   // rows of sorted_ids, of the gathered x and of a_out
     int block_m;               // BM: routing block height (multiple of 16, <= 192)
     int RT;                    // row tiles per expert
     int KSS, KS;               // k sub-stages per tile (one 8 KB packed stage each) and

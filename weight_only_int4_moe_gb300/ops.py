@@ -8,6 +8,7 @@ there is no other implementation to fall back to.
 from __future__ import annotations
 
 import ctypes
+import os
 import threading
 
 import numpy as np
@@ -21,6 +22,7 @@ MOE_OUT_BF16 = 0
 MOE_OUT_F32 = 1
 MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_TIMEOUT = 0x2
+MOE_DEVERR_BOUNDS = 0x4  # debug-bounds builds only
 
 EXPORTED = [
     "moe_int4_packed_bytes", "moe_int4_packed_scale_bytes", "moe_int4_pack",
@@ -51,8 +53,15 @@ _lib = None
 _lock = threading.Lock()
 
 
+def debug_bounds() -> bool:
+    """MOE_INT4_DEBUG_BOUNDS=1 selects the debug-bounds build of the library
+    (index checks on routing buffers, MOE_DEVERR_BOUNDS); read once, when the
+    library is first loaded."""
+    return os.environ.get("MOE_INT4_DEBUG_BOUNDS", "0") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.DEBUG_LIB if debug_bounds() else _build.LIB
 
 
 def load_library(build_if_missing: bool = True):
@@ -61,7 +70,8 @@ def load_library(build_if_missing: bool = True):
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.build() if build_if_missing else _build.LIB
+        dbg = debug_bounds()
+        path = _build.build(debug_bounds=dbg) if build_if_missing else library_path()
         lib = ctypes.CDLL(path)
         p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         sp = ctypes.POINTER(Shape)
