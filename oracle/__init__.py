@@ -68,8 +68,20 @@ def _load():
         lib.oracle_weight.restype = ctypes.c_double
         lib.oracle_moe_forward_tokens.argtypes = [p] * 7 + [i64] * 5 + [p, i64, p, p]
         lib.oracle_moe_forward_tokens.restype = i64
+        lib.oracle_moe_forward_tokens_fmt.argtypes = ([ctypes.c_int] + [p] * 7 + [i64] * 5
+                                                      + [p, i64, p, p])
+        lib.oracle_moe_forward_tokens_fmt.restype = i64
+        lib.oracle_e2m1.argtypes = [ctypes.c_int]
+        lib.oracle_e2m1.restype = ctypes.c_double
+        lib.oracle_e8m0.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0.restype = ctypes.c_double
+        lib.oracle_weight_fmt.argtypes = [ctypes.c_int, p, p, i64, i64, i64, i64, i64]
+        lib.oracle_weight_fmt.restype = ctypes.c_double
         lib.oracle_moe_intermediate_pairs.argtypes = [p] * 4 + [i64] * 5 + [p, i64, p]
         lib.oracle_moe_intermediate_pairs.restype = None
+        lib.oracle_moe_intermediate_pairs_fmt.argtypes = ([ctypes.c_int] + [p] * 4 + [i64] * 5
+                                                          + [p, i64, p])
+        lib.oracle_moe_intermediate_pairs_fmt.restype = None
         lib.oracle_align.argtypes = [p, i64, i64, i64, i64, p, i64, p, i64, p]
         lib.oracle_route.argtypes = [p, i64, i64, i64, p, p]
         lib.oracle_route.restype = None
@@ -105,24 +117,49 @@ def weight(q: np.ndarray, s: np.ndarray, e: int, n: int, k: int) -> float:
     return _load().oracle_weight(_ptr(q), _ptr(s), N, 2 * K2, e, n, k)
 
 
+# Weight formats: INT4 (q - 8) * bf16 scale; MXFP4 e2m1(q) * 2^(e8m0 - 127).
+FORMATS = {"int4": (0, np.uint16), "mxfp4": (1, np.uint8)}
+
+
+def e2m1(code: int) -> float:
+    """Value of one FP4 E2M1 code (OCP Microscaling v1.0 element type)."""
+    return _load().oracle_e2m1(int(code))
+
+
+def e8m0(bits: int) -> float:
+    """Value of one E8M0 scale: 2^(bits - 127); 255 is NaN."""
+    return _load().oracle_e8m0(int(bits))
+
+
+def weight_fmt(fmt: str, q: np.ndarray, s: np.ndarray, e: int, n: int, k: int) -> float:
+    """Dequantised weight W[e, n, k] of a [E, N, K] matrix in format fmt."""
+    code, sdt = FORMATS[fmt]
+    q = _c(q, np.uint8)
+    s = _c(s, sdt)
+    E, N, K2 = q.shape
+    return _load().oracle_weight_fmt(code, _ptr(q), _ptr(s), N, 2 * K2, e, n, k)
+
+
 def _default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
 def moe_forward(x, q13, s13, q2, s2, topk_ids, topk_weights, tokens=None,
-                threads: int | None = None):
+                threads: int | None = None, fmt: str = "int4"):
     """Layer output in fp64 for the given tokens (all tokens by default).
 
-    x: uint16 bf16 bits [M, H]; q13 uint8 [E, 2I, H/2]; s13 uint16 [E, 2I, H/32];
-    q2 uint8 [E, H, I/2]; s2 uint16 [E, H, I/32]; topk_ids int32 [M, k];
-    topk_weights float32 [M, k].  Returns (out float64 [n, H], n_dropped).
+    x: uint16 bf16 bits [M, H]; q13 uint8 [E, 2I, H/2]; s13 [E, 2I, H/32];
+    q2 uint8 [E, H, I/2]; s2 [E, H, I/32]; topk_ids int32 [M, k];
+    topk_weights float32 [M, k].  Scales: uint16 bf16 bits (fmt "int4") or
+    uint8 E8M0 (fmt "mxfp4").  Returns (out float64 [n, H], n_dropped).
     """
     lib = _load()
+    fcode, sdt = FORMATS[fmt]
     x = _c(x, np.uint16)
     q13 = _c(q13, np.uint8)
-    s13 = _c(s13, np.uint16)
+    s13 = _c(s13, sdt)
     q2 = _c(q2, np.uint8)
-    s2 = _c(s2, np.uint16)
+    s2 = _c(s2, sdt)
     ids = _c(topk_ids, np.int32)
     w = _c(topk_weights, np.float32)
     M, H = x.shape
@@ -141,8 +178,8 @@ def moe_forward(x, q13, s13, q2, s2, topk_ids, topk_weights, tokens=None,
         sub = _c(toks[idx], np.int64)
         o = np.zeros((len(sub), H), dtype=np.float64)
         scratch = np.zeros(I + H, dtype=np.float64)
-        d = lib.oracle_moe_forward_tokens(
-            _ptr(x), _ptr(q13), _ptr(s13), _ptr(q2), _ptr(s2), _ptr(ids), _ptr(w),
+        d = lib.oracle_moe_forward_tokens_fmt(
+            fcode, _ptr(x), _ptr(q13), _ptr(s13), _ptr(q2), _ptr(s2), _ptr(ids), _ptr(w),
             M, E, k, H, I, _ptr(sub), len(sub), _ptr(scratch), _ptr(o))
         out[idx] = o
         return d
@@ -155,12 +192,14 @@ def moe_forward(x, q13, s13, q2, s2, topk_ids, topk_weights, tokens=None,
     return out, int(dropped)
 
 
-def moe_intermediate(x, q13, s13, topk_ids, pairs, threads: int | None = None):
+def moe_intermediate(x, q13, s13, topk_ids, pairs, threads: int | None = None,
+                     fmt: str = "int4"):
     """SwiGLU intermediate a [n, I] (fp64) of routing pairs (flat index t*k+j)."""
     lib = _load()
+    fcode, sdt = FORMATS[fmt]
     x = _c(x, np.uint16)
     q13 = _c(q13, np.uint8)
-    s13 = _c(s13, np.uint16)
+    s13 = _c(s13, sdt)
     ids = _c(topk_ids, np.int32)
     M, H = x.shape
     E, twoI, _ = q13.shape
@@ -174,8 +213,8 @@ def moe_intermediate(x, q13, s13, topk_ids, pairs, threads: int | None = None):
     def run(idx):
         sub = _c(pairs[idx], np.int64)
         o = np.zeros((len(sub), I), dtype=np.float64)
-        lib.oracle_moe_intermediate_pairs(_ptr(x), _ptr(q13), _ptr(s13), _ptr(ids),
-                                          M, E, k, H, I, _ptr(sub), len(sub), _ptr(o))
+        lib.oracle_moe_intermediate_pairs_fmt(fcode, _ptr(x), _ptr(q13), _ptr(s13), _ptr(ids),
+                                              M, E, k, H, I, _ptr(sub), len(sub), _ptr(o))
         out[idx] = o
 
     if len(chunks) == 1:

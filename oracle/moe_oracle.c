@@ -24,6 +24,13 @@
  *        y_h = sum_i W2[e, h, i] a_i
  *        out[t, h] += w[t, j] * y_h                     (top-k weighted combine)
  *  - Routing pairs whose expert id is outside [0, E) are dropped and counted.
+ *  - The MXFP4 variant ("From 1,060 to 4,016 tok/s on one B300", whose model
+ *    has MXFP4 experts, and its section "Finding 2: the MoE autotuner only saw
+ *    decode shapes") changes only the weight: value = e2m1(q) * 2^(e - 127),
+ *    the OCP Microscaling v1.0 FP4 element (sign, 2-bit exponent with bias 1, one
+ *    mantissa bit; exponent 0 subnormal) with one E8M0 power-of-two scale per 32
+ *    along the reduction axis.  The pages name the format without defining it;
+ *    this is the published definition.  Exact in fp64.
  *
  * Canonical storage read here (not a device layout):
  *  - q bytes [E][N][K/2]: logical element k of a row sits in byte k/2, in the
@@ -56,40 +63,74 @@ int oracle_nibble(const uint8_t *row, int64_t k) {
     return (k % 2 == 0) ? (b & 0x0F) : (b >> 4);
 }
 
-/* Dequantised weight W[e, n, k] = (q - 8) * s[e, n, k / 32] for a matrix of
- * N rows and K columns per expert, exact in fp64. */
-double oracle_weight(const uint8_t *q, const uint16_t *s, int64_t N, int64_t K,
-                     int64_t e, int64_t n, int64_t k) {
+/* Weight formats. */
+enum { ORACLE_INT4 = 0, ORACLE_MXFP4 = 1 };
+
+/* FP4 E2M1 element: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
+ * exponent 0 is subnormal (0 or 0.5). */
+double oracle_e2m1(int code) {
+    int sign = (code >> 3) & 1, ex = (code >> 1) & 3, man = code & 1;
+    double mag = (ex == 0) ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);
+    return sign ? -mag : mag;
+}
+
+/* E8M0 scale: 2^(bits - 127); the code 255 is NaN. */
+double oracle_e8m0(uint8_t bits) {
+    return bits == 255 ? NAN : ldexp(1.0, (int)bits - 127);
+}
+
+/* Dequantised weight W[e, n, k] of a matrix of N rows and K columns per expert,
+ * exact in fp64.  INT4: (q - 8) * s[e, n, k / 32] with s bf16 (uint16 bit
+ * patterns).  MXFP4: e2m1(q) * e8m0(s[e, n, k / 32]) with s one byte. */
+double oracle_weight_fmt(int fmt, const uint8_t *q, const void *s, int64_t N, int64_t K,
+                         int64_t e, int64_t n, int64_t k) {
     const uint8_t *row = q + (e * N + n) * (K / 2);
     int nib = oracle_nibble(row, k);
-    double scale = oracle_bf16_to_double(s[(e * N + n) * (K / 32) + k / 32]);
-    return (double)(nib - 8) * scale;
+    int64_t g = (e * N + n) * (K / 32) + k / 32;
+    if (fmt == ORACLE_MXFP4) return oracle_e2m1(nib) * oracle_e8m0(((const uint8_t *)s)[g]);
+    return (double)(nib - 8) * oracle_bf16_to_double(((const uint16_t *)s)[g]);
+}
+
+double oracle_weight(const uint8_t *q, const uint16_t *s, int64_t N, int64_t K,
+                     int64_t e, int64_t n, int64_t k) {
+    return oracle_weight_fmt(ORACLE_INT4, q, s, N, K, e, n, k);
 }
 
 /* SwiGLU intermediate a[0..I) of one (token, expert) pair. */
-void oracle_pair_intermediate(const uint16_t *x_row, const uint8_t *q13,
-                              const uint16_t *s13, int64_t e, int64_t H,
-                              int64_t I, double *a) {
+void oracle_pair_intermediate_fmt(int fmt, const uint16_t *x_row, const uint8_t *q13,
+                                  const void *s13, int64_t e, int64_t H, int64_t I,
+                                  double *a) {
     for (int64_t i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int64_t h = 0; h < H; ++h) {
             double xv = oracle_bf16_to_double(x_row[h]);
-            g += oracle_weight(q13, s13, 2 * I, H, e, i, h) * xv;
-            u += oracle_weight(q13, s13, 2 * I, H, e, I + i, h) * xv;
+            g += oracle_weight_fmt(fmt, q13, s13, 2 * I, H, e, i, h) * xv;
+            u += oracle_weight_fmt(fmt, q13, s13, 2 * I, H, e, I + i, h) * xv;
         }
         a[i] = g / (1.0 + exp(-g)) * u;
     }
 }
 
+void oracle_pair_intermediate(const uint16_t *x_row, const uint8_t *q13,
+                              const uint16_t *s13, int64_t e, int64_t H,
+                              int64_t I, double *a) {
+    oracle_pair_intermediate_fmt(ORACLE_INT4, x_row, q13, s13, e, H, I, a);
+}
+
 /* Expert output y[0..H) = W2[e] a for one pair. */
-void oracle_pair_down(const double *a, const uint8_t *q2, const uint16_t *s2,
-                      int64_t e, int64_t H, int64_t I, double *y) {
+void oracle_pair_down_fmt(int fmt, const double *a, const uint8_t *q2, const void *s2,
+                          int64_t e, int64_t H, int64_t I, double *y) {
     for (int64_t h = 0; h < H; ++h) {
         double acc = 0.0;
         for (int64_t i = 0; i < I; ++i)
-            acc += oracle_weight(q2, s2, H, I, e, h, i) * a[i];
+            acc += oracle_weight_fmt(fmt, q2, s2, H, I, e, h, i) * a[i];
         y[h] = acc;
     }
+}
+
+void oracle_pair_down(const double *a, const uint8_t *q2, const uint16_t *s2,
+                      int64_t e, int64_t H, int64_t I, double *y) {
+    oracle_pair_down_fmt(ORACLE_INT4, a, q2, s2, e, H, I, y);
 }
 
 /*
@@ -97,13 +138,12 @@ void oracle_pair_down(const double *a, const uint8_t *q2, const uint16_t *s2,
  * r in [0, n_tokens).  scratch must hold I + H doubles.  Returns the number of
  * routing pairs of those tokens that were dropped (expert id outside [0, E)).
  */
-int64_t oracle_moe_forward_tokens(const uint16_t *x, const uint8_t *q13,
-                                  const uint16_t *s13, const uint8_t *q2,
-                                  const uint16_t *s2, const int32_t *topk_ids,
-                                  const float *topk_weights, int64_t M, int64_t E,
-                                  int64_t top_k, int64_t H, int64_t I,
-                                  const int64_t *tokens, int64_t n_tokens,
-                                  double *scratch, double *out) {
+int64_t oracle_moe_forward_tokens_fmt(int fmt, const uint16_t *x, const uint8_t *q13,
+                                      const void *s13, const uint8_t *q2, const void *s2,
+                                      const int32_t *topk_ids, const float *topk_weights,
+                                      int64_t M, int64_t E, int64_t top_k, int64_t H,
+                                      int64_t I, const int64_t *tokens, int64_t n_tokens,
+                                      double *scratch, double *out) {
     int64_t dropped = 0;
     double *a = scratch;
     double *y = scratch + I;
@@ -119,23 +159,34 @@ int64_t oracle_moe_forward_tokens(const uint16_t *x, const uint8_t *q13,
                 continue;
             }
             double w = (double)topk_weights[t * top_k + j];
-            oracle_pair_intermediate(x + t * H, q13, s13, e, H, I, a);
-            oracle_pair_down(a, q2, s2, e, H, I, y);
+            oracle_pair_intermediate_fmt(fmt, x + t * H, q13, s13, e, H, I, a);
+            oracle_pair_down_fmt(fmt, a, q2, s2, e, H, I, y);
             for (int64_t h = 0; h < H; ++h) o[h] += w * y[h];
         }
     }
     return dropped;
 }
 
+int64_t oracle_moe_forward_tokens(const uint16_t *x, const uint8_t *q13,
+                                  const uint16_t *s13, const uint8_t *q2,
+                                  const uint16_t *s2, const int32_t *topk_ids,
+                                  const float *topk_weights, int64_t M, int64_t E,
+                                  int64_t top_k, int64_t H, int64_t I,
+                                  const int64_t *tokens, int64_t n_tokens,
+                                  double *scratch, double *out) {
+    return oracle_moe_forward_tokens_fmt(ORACLE_INT4, x, q13, s13, q2, s2, topk_ids,
+                                         topk_weights, M, E, top_k, H, I, tokens, n_tokens,
+                                         scratch, out);
+}
+
 /*
  * Intermediate a for a list of routing pairs (flat index t*k+j): out[r, i].
  * Pairs with an out-of-range expert give a row of zeros.
  */
-void oracle_moe_intermediate_pairs(const uint16_t *x, const uint8_t *q13,
-                                   const uint16_t *s13, const int32_t *topk_ids,
-                                   int64_t M, int64_t E, int64_t top_k, int64_t H,
-                                   int64_t I, const int64_t *pairs, int64_t n_pairs,
-                                   double *out) {
+void oracle_moe_intermediate_pairs_fmt(int fmt, const uint16_t *x, const uint8_t *q13,
+                                       const void *s13, const int32_t *topk_ids, int64_t M,
+                                       int64_t E, int64_t top_k, int64_t H, int64_t I,
+                                       const int64_t *pairs, int64_t n_pairs, double *out) {
     for (int64_t r = 0; r < n_pairs; ++r) {
         int64_t p = pairs[r];
         double *o = out + r * I;
@@ -144,8 +195,17 @@ void oracle_moe_intermediate_pairs(const uint16_t *x, const uint8_t *q13,
             for (int64_t i = 0; i < I; ++i) o[i] = 0.0;
             continue;
         }
-        oracle_pair_intermediate(x + (p / top_k) * H, q13, s13, e, H, I, o);
+        oracle_pair_intermediate_fmt(fmt, x + (p / top_k) * H, q13, s13, e, H, I, o);
     }
+}
+
+void oracle_moe_intermediate_pairs(const uint16_t *x, const uint8_t *q13,
+                                   const uint16_t *s13, const int32_t *topk_ids,
+                                   int64_t M, int64_t E, int64_t top_k, int64_t H,
+                                   int64_t I, const int64_t *pairs, int64_t n_pairs,
+                                   double *out) {
+    oracle_moe_intermediate_pairs_fmt(ORACLE_INT4, x, q13, s13, topk_ids, M, E, top_k, H, I,
+                                      pairs, n_pairs, out);
 }
 
 /*

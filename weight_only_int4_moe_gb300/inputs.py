@@ -95,6 +95,28 @@ def make_weights(E: int, H: int, I: int, seed: int) -> dict:
     return {"q13": q13, "s13": s13, "q2": q2, "s2": s2}
 
 
+# MXFP4 weights: E8M0 scale codes are drawn from [119, 123] (2^-8 .. 2^-4), so
+# weights e2m1(q) * scale span about the same range as the INT4 ones.
+MXFP4_SCALE_CODES = (119, 123)
+
+
+def make_weights_mxfp4(E: int, H: int, I: int, seed: int) -> dict:
+    """Canonical MXFP4 weights for w13 [E, 2I, H] and w2 [E, H, I]: E2M1 codes
+    in the INT4 nibble order (uniform over the 16 codes) and E8M0 scale bytes."""
+    assert H % GROUP == 0 and I % GROUP == 0
+    rng = np.random.default_rng([1, seed])
+    lo, hi = MXFP4_SCALE_CODES
+
+    def scales(shape):
+        return rng.integers(lo, hi + 1, size=shape, dtype=np.uint8)
+
+    q13 = _random_nibble_bytes(rng, (E, 2 * I, H // 2))
+    s13 = scales((E, 2 * I, H // GROUP))
+    q2 = _random_nibble_bytes(rng, (E, H, I // 2))
+    s2 = scales((E, H, I // GROUP))
+    return {"q13": q13, "s13": s13, "q2": q2, "s2": s2}
+
+
 def _softmax(logits: np.ndarray) -> np.ndarray:
     z = logits - logits.max(axis=1, keepdims=True)
     p = np.exp(z)
