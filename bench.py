@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--routed", action="store_true",
                     help="time moe_int4_forward_routed: routing from router logits in the call")
+    ap.add_argument("--format", choices=["int4", "mxfp4"], default="int4",
+                    help="expert weight format (mxfp4: E2M1 codes, E8M0 scale per 32)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (a smaller case of the same kernels, for ncu captures)")
     return ap.parse_args()
@@ -67,10 +69,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def expert_bytes(H, I):
-    w13 = 2 * I * H // 2 + 2 * I * (H // 32) * 2
-    w2 = H * I // 2 + H * (I // 32) * 2
+def expert_bytes(H, I, fmt="int4"):
+    """Algorithmic bytes of one expert: 4-bit codes plus one scale per 32
+    (bf16 for INT4, one E8M0 byte for MXFP4)."""
+    sb = 2 if fmt == "int4" else 1
+    w13 = 2 * I * H // 2 + 2 * I * (H // 32) * sb
+    w2 = H * I // 2 + H * (I // 32) * sb
     return w13, w2
+
+
+def make_weights(cfg, fmt):
+    if fmt == "mxfp4":
+        return inputs.make_weights_mxfp4(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
+    return inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
 
 
 GEMM_SOURCES = ("gemm.cu", "kernels.cuh", "common.cuh")
@@ -229,7 +240,7 @@ def job_rate(world, units_per_step, step_seconds_max):
 
 
 # ------------------------------------------------------------ CPU oracle --
-def time_oracle(w, cfg, Ms, target_s, threads, state=None):
+def time_oracle(w, cfg, Ms, target_s, threads, state=None, fmt="int4"):
     """Times the oracle on a bounded sample: rounds of `threads` tokens (one per
     thread) taken in turn from the largest call of the sweep, until about
     target_s seconds have passed.  Returns (tokens, seconds, M sampled)."""
@@ -245,7 +256,7 @@ def time_oracle(w, cfg, Ms, target_s, threads, state=None):
         state["next"] = (state["next"] + n) % M
         t0 = time.perf_counter()
         oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
-                           t["topk_weights"], tokens=tk, threads=threads)
+                           t["topk_weights"], tokens=tk, threads=threads, fmt=fmt)
         t_total += time.perf_counter() - t0
         toks_done += len(tk)
         rounds += 1
@@ -256,15 +267,15 @@ def run_reference(args, cfg, Ms, world, rank):
     if rank != 0:
         return
     threads = host_threads()
-    w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
+    w = make_weights(cfg, args.format)
     per_step_s = max(0.5, args.cpu_seconds / max(1, args.steps))
     state = {"next": 0}
     for _ in range(args.warmup):
-        time_oracle(w, cfg, Ms, 0.0, threads, state)
+        time_oracle(w, cfg, Ms, 0.0, threads, state, fmt=args.format)
     toks, secs = 0, 0.0
     step_ms = []
     for _ in range(args.steps):
-        n, s, Msamp = time_oracle(w, cfg, Ms, per_step_s, threads, state)
+        n, s, Msamp = time_oracle(w, cfg, Ms, per_step_s, threads, state, fmt=args.format)
         toks += n
         secs += s
         step_ms.append(s * 1e3)
@@ -275,7 +286,7 @@ def run_reference(args, cfg, Ms, world, rank):
         "ms_per_step": statistics.mean(step_ms), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "E": cfg.E, "top_k": cfg.top_k, "hidden": cfg.H,
-                   "inter": cfg.I, "Ms": list(Ms)},
+                   "inter": cfg.I, "weight_format": args.format, "Ms": list(Ms)},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{toks} tokens of the M={Msamp} call ({args.steps} "
                                    f"steps of rounds of {threads} tokens), fp64 oracle, "
@@ -297,8 +308,9 @@ def run_ours(args, cfg, Ms, world, rank, local):
     peaks, peak_src = load_peaks()
     out_dtype = ops.MOE_OUT_F32 if args.out_dtype == "f32" else ops.MOE_OUT_BF16
 
-    w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
-    pw = ops.PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k, device=dev, out_dtype=out_dtype)
+    w = make_weights(cfg, args.format)
+    pw = ops.PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k, device=dev, out_dtype=out_dtype,
+                           fmt=args.format)
     shape = pw.shape
     Mmax = max(Ms)
     ws = ops.alloc_workspace(Mmax, shape, device=dev)
@@ -306,7 +318,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
     if ws.numel() < ws_bytes_max:
         ws = torch.empty(ws_bytes_max, dtype=torch.uint8, device=dev)
     flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
-    w13_b, w2_b = expert_bytes(cfg.H, cfg.I)
+    w13_b, w2_b = expert_bytes(cfg.H, cfg.I, args.format)
 
     data = {}
     for M in Ms:
@@ -482,7 +494,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         threads = host_threads()
-        n, secs, Msamp = time_oracle(w, cfg, Ms, args.cpu_seconds, threads)
+        n, secs, Msamp = time_oracle(w, cfg, Ms, args.cpu_seconds, threads, fmt=args.format)
         cpu = {"value": n / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} tokens of the M={Msamp} call, fp64 oracle, {threads} threads, "
                          f"{secs:.1f} s"}
@@ -494,7 +506,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
             "config": {"workload": cfg.name, "E": cfg.E, "top_k": cfg.top_k, "hidden": cfg.H,
-                       "inter": cfg.I, "group": 32, "Ms": list(Ms),
+                       "inter": cfg.I, "group": 32, "weight_format": args.format, "Ms": list(Ms),
                        "step": "one moe_int4_forward per M",
                        "l2": f"flushed by a {args.flush_mb} MB device write before every call; "
                              f"routing rotates over {args.pool} seeded routings per M",
@@ -516,6 +528,8 @@ def main():
     cfg = inputs.CONFIGS[args.config]
     if args.experts:
         cfg = dataclasses.replace(cfg, E=args.experts, name=f"{cfg.name}_E{args.experts}")
+    if args.format != "int4":
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_{args.format}")
     Ms = tuple(int(m) for m in args.ms.split(",")) if args.ms else cfg.Ms
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -70,15 +70,28 @@ enum {
 #define MOE_OUT_BF16 0 /* bf16, rounded to nearest even from the fp32 combine */
 #define MOE_OUT_F32 1  /* the fp32 combine itself */
 
+/* Expert weight formats (moe_int4_shape.weight_format), both with one scale per
+ * 32 consecutive elements along the reduction axis:
+ *   MOE_W_INT4   value = (q - 8) * scale, q in 0..15, scale bf16 (moe_int4_pack).
+ *   MOE_W_MXFP4  value = e2m1(q) * 2^(e - 127): q an FP4 E2M1 code (bit 3 sign,
+ *                bits 2..1 exponent with bias 1, bit 0 mantissa, exponent 0
+ *                subnormal: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives), e an
+ *                E8M0 scale byte (OCP Microscaling v1.0; "From 1,060 to 4,016
+ *                tok/s on one B300": MXFP4 experts) -- moe_mxfp4_pack. */
+#define MOE_W_INT4 0
+#define MOE_W_MXFP4 1
+
 /* Layer shape.  Supported: 1 <= E <= 1024, 1 <= top_k <= min(E, 32),
- * hidden % 128 == 0, inter % 128 == 0, group == 32. */
+ * hidden % 128 == 0, inter % 128 == 0, group == 32, weight_format one of
+ * MOE_W_*.  A zero-initialised weight_format is INT4. */
 typedef struct {
-    int32_t E;         /* number of experts */
-    int32_t top_k;     /* routing slots per token */
-    int32_t hidden;    /* H: model width (K of the gate/up GEMM, N of the down GEMM) */
-    int32_t inter;     /* I: expert intermediate width */
-    int32_t group;     /* quantisation group along K; must be 32 */
-    int32_t out_dtype; /* MOE_OUT_BF16 or MOE_OUT_F32 */
+    int32_t E;             /* number of experts */
+    int32_t top_k;         /* routing slots per token */
+    int32_t hidden;        /* H: model width (K of the gate/up GEMM, N of the down GEMM) */
+    int32_t inter;         /* I: expert intermediate width */
+    int32_t group;         /* quantisation group along K; must be 32 */
+    int32_t out_dtype;     /* MOE_OUT_BF16 or MOE_OUT_F32 */
+    int32_t weight_format; /* MOE_W_INT4 or MOE_W_MXFP4 (how the weights were packed) */
 } moe_int4_shape;
 
 /* ------------------------------------------------------------------------- */
@@ -122,6 +135,31 @@ size_t moe_int4_packed_scale_bytes(int E, int N, int K);
  */
 int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
                   int is_w13, void *packed, void *packed_scales, moe_stream_t stream);
+
+/*
+ * moe_mxfp4_pack: canonical MXFP4 weights -> the same device layout (forward
+ * with shape.weight_format = MOE_W_MXFP4).
+ *
+ * In:  q       uint8 [E][N][K/2], FP4 E2M1 codes in the nibble order of
+ *              moe_int4_pack.
+ *      scales  uint8 E8M0 [E][N][K/32] (2^(e - 127)); one per 32 consecutive k.
+ *      is_w13  as for moe_int4_pack.
+ * Out: packed (moe_int4_packed_bytes) and packed_scales
+ *      (moe_int4_packed_scale_bytes), caller-allocated, 16-byte aligned, laid
+ *      out as for moe_int4_pack.  Each scale is stored as the fp16 factor the
+ *      kernels multiply by, 2^(e - 113) (the dequant's fp16 bit pattern of a
+ *      code is its value times 2^-14), representable for e in [89, 128], i.e.
+ *      scales 2^-38 .. 2; codes outside that range (and 255, NaN) are clamped to
+ *      its ends and counted.  The dequantised fp16 weights are exact for e in
+ *      [104, 128]; below, magnitudes under 2^-24 round in fp16.
+ *      bad_scales  optional (NULL: not counted): device uint32, incremented
+ *              (atomically, on the stream) once per clamped scale; the caller
+ *              zeroes it first.
+ * Errors: as moe_int4_pack.
+ */
+int moe_mxfp4_pack(const uint8_t *q, const uint8_t *scales, int E, int N, int K, int is_w13,
+                   void *packed, void *packed_scales, uint32_t *bad_scales,
+                   moe_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Align: bucket routing pairs by expert and pad each bucket to block_m       */

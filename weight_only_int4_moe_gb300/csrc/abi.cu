@@ -33,6 +33,7 @@ int check_shape(const moe_int4_shape *sh) {
     if (sh->inter < 128 || sh->inter % 128) return MOE_ERR_SHAPE;
     if (sh->group != 32) return MOE_ERR_SHAPE;
     if (sh->out_dtype != MOE_OUT_BF16 && sh->out_dtype != MOE_OUT_F32) return MOE_ERR_SHAPE;
+    if (sh->weight_format != MOE_W_INT4 && sh->weight_format != MOE_W_MXFP4) return MOE_ERR_SHAPE;
     return MOE_OK;
 }
 
@@ -204,6 +205,23 @@ int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
         return MOE_ERR_ALIGN;
     cudaError_t e = launch_pack(q, scales, E, N, K, is_w13, packed, packed_scales,
                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_mxfp4_pack(const uint8_t *q, const uint8_t *scales, int E, int N, int K, int is_w13,
+                   void *packed, void *packed_scales, uint32_t *bad_scales,
+                   moe_stream_t stream) {
+    if (!q || !scales || !packed || !packed_scales) return MOE_ERR_NULL;
+    if (E < 1 || N < 1 || K < 1) return MOE_ERR_SHAPE;
+    if (is_w13) {
+        if (N % 256 || K % 64) return MOE_ERR_SHAPE;
+    } else {
+        if (N % 128 || K % 128) return MOE_ERR_SHAPE;
+    }
+    if (!aligned16(q) || !aligned16(scales) || !aligned16(packed) || !aligned16(packed_scales))
+        return MOE_ERR_ALIGN;
+    cudaError_t e = launch_pack_mxfp4(q, scales, E, N, K, is_w13, packed, packed_scales,
+                                      bad_scales, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -386,6 +404,7 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     g.cap = pl.cap > (size_t)INT32_MAX ? INT32_MAX : (int)pl.cap;
     g.block_m = pl.BM;
     g.round_robin = 1;
+    g.fmt = shape->weight_format;
 
     GemmParams g1 = g;
     g1.zero_out = reinterpret_cast<float4 *>(acc);

@@ -233,6 +233,30 @@ __device__ __forceinline__ void dequant_row(const uint4 lo, const uint4 hi, uint
     }
 }
 
+// MXFP4: the same 32 pairs from FP4 E2M1 codes in the same nibble order,
+// e2m1(q) * 2^(e - 127).  With the code's magnitude bits (exponent, mantissa)
+// moved to fp16 bits 11..9 and its sign to bit 15, the fp16 value is exactly the
+// code's value times 2^-14 -- codes of exponent 0 (0 and 0.5) land on fp16 zero
+// and subnormals, the others on normals with the right exponent -- so the
+// packed scale carries 2^(e - 127 + 14) and one multiply finishes the weight.
+// Two shifts, two logic operations and a multiply per two weights.
+__device__ __forceinline__ void dequant_row_fp4(const uint4 lo, const uint4 hi, uint32_t sc,
+                                                uint32_t out[32]) {
+    const __half2 s0 = as_h2(__byte_perm(sc, 0, 0x1010));
+    const __half2 s1 = as_h2(__byte_perm(sc, 0, 0x3232));
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        const __half2 s2 = (v < 4) ? s0 : s1;
+#pragma unroll
+        for (int b = 0; b < 16; b += 4) {  // nibbles at bits b.. and 16 + b..
+            const uint32_t mag = ((b <= 9) ? (w[v] << (9 - b)) : (w[v] >> (b - 9))) & 0x0E000E00u;
+            const uint32_t sgn = (w[v] << (12 - b)) & 0x80008000u;
+            out[4 * v + b / 4] = as_u32(__hmul2(as_h2(mag | sgn), s2));
+        }
+    }
+}
+
 // fp32 -> fp16, saturating at the largest finite fp16 value.
 __device__ __forceinline__ uint16_t f16_sat(float v) {
     v = fminf(fmaxf(v, -65504.0f), 65504.0f);
@@ -278,7 +302,8 @@ __device__ __forceinline__ void swiglu_store(uint32_t tl, int BM, int j_lo, int 
 // WIDE: the wide-block configuration (blocks of 144..192 tokens): A released
 // per sub-stage half (np = 2); down has one issuer and B slots of one
 // sub-stage.  Separate instantiations keep the common path's registers.
-template <int KIND, int WIDE>
+// FMT: the weight format (0 INT4, 1 MXFP4); it changes only the dequant.
+template <int KIND, int WIDE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_b) {
     extern __shared__ uint8_t smem_raw[];
@@ -525,6 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
                             }
                             uint32_t v[32];
+                            if (FMT == 1)
+                            dequant_row_fp4(lo, hi, sc, v);
+                        else
                             dequant_row(lo, hi, sc, dqc, v);
                             tc_fence_after();
                             tmem_st_32x32b_x32_wait(st + uu * 64 + g * 32, v);
@@ -961,13 +989,16 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
 cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_b, int grid,
                         cudaStream_t s, int *launches) {
     const int wide = (p.np == 2 || p.b_sub) ? 1 : 0;
-    const int v = (kind - 1) * 2 + wide;  // instantiation index
-    static bool attr_done[64][4] = {};
+    const int fmt = (p.fmt == 1) ? 1 : 0;  // MOE_W_MXFP4
+    const int v = (fmt * 2 + (kind - 1)) * 2 + wide;  // instantiation index
+    static bool attr_done[64][8] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     typedef void (*KernelFn)(const GemmParams, const CUtensorMap);
-    const KernelFn fns[4] = {moe_gemm_kernel<1, 0>, moe_gemm_kernel<1, 1>, moe_gemm_kernel<2, 0>,
-                             moe_gemm_kernel<2, 1>};
+    const KernelFn fns[8] = {moe_gemm_kernel<1, 0, 0>, moe_gemm_kernel<1, 1, 0>,
+                             moe_gemm_kernel<2, 0, 0>, moe_gemm_kernel<2, 1, 0>,
+                             moe_gemm_kernel<1, 0, 1>, moe_gemm_kernel<1, 1, 1>,
+                             moe_gemm_kernel<2, 0, 1>, moe_gemm_kernel<2, 1, 1>};
     if (dev >= 0 && dev < 64 && !attr_done[dev][v]) {
         cudaError_t e = cudaFuncSetAttribute(fns[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);

@@ -67,6 +67,9 @@ cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, 
                             int *launches);
 cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
                         int is_w13, void *packed, void *packed_scales, cudaStream_t s);
+cudaError_t launch_pack_mxfp4(const uint8_t *q, const uint8_t *scales, int E, int N, int K,
+                              int is_w13, void *packed, void *packed_scales, uint32_t *bad,
+                              cudaStream_t s);
 
 // Packed weight geometry shared by the pack kernel and the GEMMs.
 constexpr int kSlabRows = 128;
@@ -112,6 +115,7 @@ struct GemmParams {
     int np;                    // A-slot release parts per stage: 1, or 2 (per sub-stage)
     int b_sub;                 // 1: B ring slots hold one sub-stage (wide blocks)
     int epi_f4;                // down: combine through shared memory as float4 adds
+    int fmt;                   // weight format: MOE_W_INT4 or MOE_W_MXFP4 (picks the kernel)
     int round_robin;           // 1: whole waves of tiles round-robin, the rest split by stages
                                // (0: all split by stages)
     uint32_t b_stage_bytes;

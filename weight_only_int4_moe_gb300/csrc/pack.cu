@@ -5,7 +5,9 @@
 // "Building the Benchmark"); this layout is designed for the sm_103a kernels:
 // each stage is contiguous, each dequantising thread reads its row's 32 bytes
 // as two conflict-free 16-byte shared-memory loads, and the nibble order lets
-// one mask/OR produce two bf16 values at once.
+// one mask/OR produce two fp16 values at once.  MXFP4 weights use the same
+// nibble layout (their codes are E2M1, not integers) with E8M0 scales converted
+// to the fp16 factor their dequant multiplies by.
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
@@ -58,8 +60,35 @@ __device__ __forceinline__ uint16_t bf16_bits_to_f16_sat(uint16_t b) {
     return __half_as_ushort(__float2half_rn(v));
 }
 
-__global__ void pack_scales_kernel(const uint16_t *__restrict__ s, uint32_t *__restrict__ out,
-                                   int N, int K, int is_w13, size_t n_words) {
+// E8M0 scale byte -> the fp16 factor of the MXFP4 dequant, 2^(e - 113): the
+// scale 2^(e - 127) times 2^14, since the dequant's fp16 bit pattern of an E2M1
+// code is the code's value times 2^-14.  Exact for e in [89, 128] (fp16 normal
+// or subnormal powers of two); other codes, 255 (NaN) included, are clamped to
+// that range and counted in *bad.
+__device__ __forceinline__ uint16_t e8m0_to_f16_factor(uint8_t e, uint32_t *bad) {
+    int x = (int)e - 113;
+    if (x < -24 || x > 15) {
+        if (bad) atomicAdd(bad, 1u);
+        x = x < -24 ? -24 : 15;
+    }
+    return x >= -14 ? (uint16_t)((x + 15) << 10) : (uint16_t)(1u << (x + 24));
+}
+
+struct Bf16Scale {
+    using T = uint16_t;
+    __device__ uint16_t operator()(uint16_t b) const { return bf16_bits_to_f16_sat(b); }
+};
+struct E8m0Scale {
+    using T = uint8_t;
+    uint32_t *bad;
+    __device__ uint16_t operator()(uint8_t e) const { return e8m0_to_f16_factor(e, bad); }
+};
+
+// Scales [E][N][K/32] (bf16 bits or E8M0 bytes) -> per stage [slab][row][2] fp16.
+template <class Conv>
+__global__ void pack_scales_kernel(const typename Conv::T *__restrict__ s,
+                                   uint32_t *__restrict__ out, int N, int K, int is_w13,
+                                   size_t n_words, Conv conv) {
     const int KS = is_w13 ? K / kSlabK : K / (2 * kSlabK);
     const int RT = is_w13 ? (N / 2) / kSlabRows : N / kSlabRows;
     const int G = K / 32;
@@ -80,14 +109,15 @@ __global__ void pack_scales_kernel(const uint16_t *__restrict__ s, uint32_t *__r
             n = kSlabRows * r + row;
             kb = 2 * kk + slab;
         }
-        const uint16_t *src = s + (e * N + n) * (size_t)G + 2 * kb;
-        out[idx] = (uint32_t)bf16_bits_to_f16_sat(src[0]) |
-                   ((uint32_t)bf16_bits_to_f16_sat(src[1]) << 16);
+        const typename Conv::T *src = s + (e * N + n) * (size_t)G + 2 * kb;
+        out[idx] = (uint32_t)conv(src[0]) | ((uint32_t)conv(src[1]) << 16);
     }
 }
 
-cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
-                        int is_w13, void *packed, void *packed_scales, cudaStream_t s) {
+template <class Conv>
+cudaError_t launch_pack_impl(const uint8_t *q, const typename Conv::T *scales, Conv conv, int E,
+                             int N, int K, int is_w13, void *packed, void *packed_scales,
+                             cudaStream_t s) {
     const size_t n_words = (size_t)E * N * (K / 2) / 4;
     const size_t n_swords = (size_t)E * N * (K / 32) / 2;
     const int threads = 256;
@@ -97,9 +127,21 @@ cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, 
         q, reinterpret_cast<uint32_t *>(packed), N, K, is_w13, n_words);
     size_t sblocks = (n_swords + threads - 1) / threads;
     if (sblocks > 65535 * 8) sblocks = 65535 * 8;
-    pack_scales_kernel<<<(unsigned)sblocks, threads, 0, s>>>(
-        scales, reinterpret_cast<uint32_t *>(packed_scales), N, K, is_w13, n_swords);
+    pack_scales_kernel<Conv><<<(unsigned)sblocks, threads, 0, s>>>(
+        scales, reinterpret_cast<uint32_t *>(packed_scales), N, K, is_w13, n_swords, conv);
     return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
+                        int is_w13, void *packed, void *packed_scales, cudaStream_t s) {
+    return launch_pack_impl(q, scales, Bf16Scale{}, E, N, K, is_w13, packed, packed_scales, s);
+}
+
+cudaError_t launch_pack_mxfp4(const uint8_t *q, const uint8_t *scales, int E, int N, int K,
+                              int is_w13, void *packed, void *packed_scales, uint32_t *bad,
+                              cudaStream_t s) {
+    return launch_pack_impl(q, scales, E8m0Scale{bad}, E, N, K, is_w13, packed, packed_scales,
+                            s);
 }
 
 }  // namespace moe

@@ -23,9 +23,11 @@ MOE_OUT_F32 = 1
 MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_TIMEOUT = 0x2
 MOE_DEVERR_BOUNDS = 0x4  # debug-bounds builds only
+MOE_W_INT4 = 0
+MOE_W_MXFP4 = 1
 
 EXPORTED = [
-    "moe_int4_packed_bytes", "moe_int4_packed_scale_bytes", "moe_int4_pack",
+    "moe_int4_packed_bytes", "moe_int4_packed_scale_bytes", "moe_int4_pack", "moe_mxfp4_pack",
     "moe_align_capacity", "moe_align_scratch_bytes", "moe_align",
     "moe_int4_workspace_bytes", "moe_int4_block_m", "moe_int4_workspace_layout",
     "moe_int4_forward",
@@ -38,11 +40,11 @@ EXPORTED = [
 class Shape(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("inter", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("weight_format", ctypes.c_int32)]
 
     @classmethod
-    def of(cls, E, top_k, hidden, inter, out_dtype=MOE_OUT_F32):
-        return cls(E, top_k, hidden, inter, 32, out_dtype)
+    def of(cls, E, top_k, hidden, inter, out_dtype=MOE_OUT_F32, weight_format=0):
+        return cls(E, top_k, hidden, inter, 32, out_dtype, weight_format)
 
     @property
     def torch_out_dtype(self):
@@ -79,6 +81,7 @@ def load_library(build_if_missing: bool = True):
             "moe_int4_packed_bytes": ([i, i, i], sz),
             "moe_int4_packed_scale_bytes": ([i, i, i], sz),
             "moe_int4_pack": ([p, p, i, i, i, i, p, p, p], i),
+            "moe_mxfp4_pack": ([p, p, i, i, i, i, p, p, p, p], i),
             "moe_align_capacity": ([i, i, i, i], sz),
             "moe_align_scratch_bytes": ([i, i, i], sz),
             "moe_align": ([p, i, i, i, i, p, p, p, p, p, sz, p], i),
@@ -156,6 +159,23 @@ def moe_int4_pack(q: torch.Tensor, scales: torch.Tensor, is_w13: bool, stream=No
                            _dptr(packed), _dptr(pscales), _stream(stream))
     _check(rc, "moe_int4_pack")
     return packed, pscales
+
+
+def moe_mxfp4_pack(q: torch.Tensor, scales: torch.Tensor, is_w13: bool, stream=None):
+    """Canonical MXFP4 (E2M1 codes, uint8 [E, N, K/2]) + E8M0 scales (uint8
+    [E, N, K/32]) -> packed (uint8) and packed scales (uint8) device tensors,
+    plus the device count of scales clamped to the supported range (int32 [1])."""
+    lib = load_library()
+    E, N, K2 = q.shape
+    K = 2 * K2
+    packed = torch.empty(lib.moe_int4_packed_bytes(E, N, K), dtype=torch.uint8, device=q.device)
+    pscales = torch.empty(lib.moe_int4_packed_scale_bytes(E, N, K), dtype=torch.uint8,
+                          device=q.device)
+    bad = torch.zeros(1, dtype=torch.int32, device=q.device)
+    rc = lib.moe_mxfp4_pack(_dptr(q), _dptr(scales.contiguous()), E, N, K, int(bool(is_w13)),
+                            _dptr(packed), _dptr(pscales), _dptr(bad), _stream(stream))
+    _check(rc, "moe_mxfp4_pack")
+    return packed, pscales, bad
 
 
 # ------------------------------------------------------------------- align --
@@ -335,20 +355,35 @@ def moe_int4_last_launch_count() -> int:
 
 # --------------------------------------------------------------- helpers --
 class PackedWeights:
-    """Device copies of one weight set in the kernels' packed layout."""
+    """Device copies of one weight set in the kernels' packed layout.  fmt "int4":
+    w holds q13/q2 nibble bytes and bf16 scales s13/s2; "mxfp4": E2M1 codes and
+    E8M0 scale bytes (the weights' canonical forms in inputs.make_weights*).
+    An MXFP4 set with a scale outside the supported range raises."""
 
     def __init__(self, w: dict, E: int, H: int, I: int, top_k: int, device="cuda",
-                 keep_canonical: bool = False, out_dtype: int = MOE_OUT_F32):
-        self.shape = Shape.of(E, top_k, H, I, out_dtype)
-        q13 = torch.from_numpy(np.ascontiguousarray(w["q13"])).to(device)
-        s13 = torch.from_numpy(np.ascontiguousarray(w["s13"]).view(np.int16)).to(device)
-        self.w13, self.w13_scales = moe_int4_pack(q13, s13, True)
-        if not keep_canonical:
-            del q13, s13
-        q2 = torch.from_numpy(np.ascontiguousarray(w["q2"])).to(device)
-        s2 = torch.from_numpy(np.ascontiguousarray(w["s2"]).view(np.int16)).to(device)
-        self.w2, self.w2_scales = moe_int4_pack(q2, s2, False)
+                 keep_canonical: bool = False, out_dtype: int = MOE_OUT_F32, fmt: str = "int4"):
+        if fmt not in ("int4", "mxfp4"):
+            raise ValueError(f"unknown weight format {fmt!r}")
+        mx = fmt == "mxfp4"
+        self.shape = Shape.of(E, top_k, H, I, out_dtype, MOE_W_MXFP4 if mx else MOE_W_INT4)
+        bad = []
+
+        def pack(q_np, s_np, is_w13):
+            q = torch.from_numpy(np.ascontiguousarray(q_np)).to(device)
+            if mx:
+                sc = torch.from_numpy(np.ascontiguousarray(s_np, dtype=np.uint8)).to(device)
+                packed, pscales, nbad = moe_mxfp4_pack(q, sc, is_w13)
+                bad.append(nbad)
+                return packed, pscales
+            sc = torch.from_numpy(np.ascontiguousarray(s_np).view(np.int16)).to(device)
+            return moe_int4_pack(q, sc, is_w13)
+
+        self.w13, self.w13_scales = pack(w["q13"], w["s13"], True)
+        self.w2, self.w2_scales = pack(w["q2"], w["s2"], False)
         torch.cuda.synchronize()
+        n_bad = sum(int(t.item()) for t in bad)
+        if n_bad:
+            raise ValueError(f"{n_bad} E8M0 scales outside the supported range [89, 128]")
 
     def forward(self, x, topk_ids, topk_weights, out=None, workspace=None, stream=None):
         return moe_int4_forward(x, self.w13, self.w13_scales, self.w2, self.w2_scales, topk_ids,
