@@ -107,3 +107,21 @@ def test_the_two_formats_agree_on_weights_both_hold():
     of = gpu_forward(ops.PackedWeights(wf, E, H, I, k, fmt="mxfp4"), t)
     scale = np.abs(oi).max()
     np.testing.assert_allclose(of, oi, rtol=0, atol=1e-5 * scale)
+
+
+@pytest.mark.slow
+def test_mxfp4_k26_shapes_sampled():
+    """The K2.6 layer shapes (hidden 7168, inter 2048, top-8) with 48 MXFP4
+    experts at M = 90, in the forward's own launch configuration: every output
+    finite, sampled tokens against the oracle."""
+    ops = _ops()
+    E, k, H, I, M = 48, 8, 7168, 2048, 90
+    w = inputs.make_weights_mxfp4(E, H, I, 123)
+    pw = ops.PackedWeights(w, E, H, I, k, fmt="mxfp4")
+    t = inputs.make_tokens(inputs.MoEConfig("mx", E, k, H, I, (M,), "uniform", 0, 124), M)
+    got = gpu_forward(pw, t)
+    assert np.all(np.isfinite(got))
+    toks = np.sort(np.random.default_rng(5).choice(M, size=4, replace=False))
+    ref, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
+                                t["topk_weights"], tokens=toks, fmt="mxfp4")
+    print(assert_parity(got[toks], ref, "mxfp4 K2.6 shapes E48 M90"))

@@ -920,13 +920,15 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
         // k blocks per B stage: gate/up two 64-wide blocks, down four
         p.b_stage_bytes = (uint32_t)((kind == 1 ? 2 : 4) * BM * 128);
         // MMA issuers (one accumulator each), accumulator buffers and the A
-        // stages that tensor memory then leaves, in order of preference: four
-        // issuers with three A stages (two buffers, else one: measured faster at
-        // 32-row blocks than two buffers with two A stages), then two A stages
-        // with four or two issuers and two buffers, then a single buffer (the
-        // issuers then wait for the epilogue at every piece end)
+        // stages that tensor memory then leaves, in order of preference: more A
+        // stages first, then more issuers, then more buffers -- four issuers
+        // with three A stages (two buffers, else one: measured faster at 32-row
+        // blocks than two buffers with two A stages), then two A stages (four
+        // issuers with one buffer measured faster at 64-row blocks than two with
+        // two), then two issuers.  With one buffer the issuers wait for the
+        // epilogue at every piece end.
         p.ni = 0;
-        const int opts[6][3] = {{4, 2, 3}, {4, 1, 3}, {4, 2, 2}, {2, 2, 2}, {4, 1, 2}, {2, 1, 2}};
+        const int opts[6][3] = {{4, 2, 3}, {4, 1, 3}, {4, 2, 2}, {4, 1, 2}, {2, 2, 2}, {2, 1, 2}};
         for (int o = 0; o < 6 && !p.ni; ++o)
             if (opts[o][0] * opts[o][1] * BM + opts[o][2] * (int)kACols <= kTmemCols) {
                 p.ni = opts[o][0];
