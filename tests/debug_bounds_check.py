@@ -2,7 +2,7 @@
 MOE_INT4_DEBUG_BOUNDS=1: the forward through the debug-bounds build of the
 library (index checks on every routing buffer read back by a kernel) on shapes
 that cover each block-height regime, a multi-block align, the routed entry
-point and dropped invalid ids.  Each output must match the oracle and no check
+point, dropped invalid ids and MXFP4 weights.  Each output must match the oracle and no check
 may fire (MOE_DEVERR_BOUNDS clear).  Prints one line per case; exits non-zero on
 the first failure."""
 import os
@@ -100,6 +100,27 @@ def run_routed():
     print("routed: ok", flush=True)
 
 
+def run_mxfp4():
+    """The MXFP4 kernels (the same pipeline with the other dequant) under the
+    same checks."""
+    import torch
+    E, k, H, I, M = 8, 2, 512, 256, 1000
+    w = inputs.make_weights_mxfp4(E, H, I, 996)
+    pw = ops.PackedWeights(w, E, H, I, k, fmt="mxfp4")
+    t = inputs.make_tokens(inputs.MoEConfig("dbg", E, k, H, I, (M,), "uniform", 0, 997), M)
+    x = torch.from_numpy(t["x"].view(np.int16)).cuda().view(torch.bfloat16)
+    ws = ops.alloc_workspace(M, pw.shape)
+    out = pw.forward(x, torch.from_numpy(t["topk_ids"]).cuda(),
+                     torch.from_numpy(t["topk_weights"]).cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    flags, dropped = ops.moe_int4_get_errors(ws)
+    assert flags == 0 and dropped == 0, hex(flags)
+    ref, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
+                                t["topk_weights"], fmt="mxfp4")
+    assert_parity(out.cpu().numpy(), ref, "mxfp4")
+    print("mxfp4: ok", flush=True)
+
+
 def main():
     assert ops.debug_bounds(), "run with MOE_INT4_DEBUG_BOUNDS=1"
     ops.load_library()
@@ -108,6 +129,7 @@ def main():
         run_case(*case, seed=i)
     run_invalid_ids()
     run_routed()
+    run_mxfp4()
     print("debug-bounds: all cases clean", flush=True)
 
 

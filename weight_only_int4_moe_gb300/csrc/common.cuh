@@ -1,7 +1,6 @@
 // Device helpers shared by the kernels of the INT4 MoE library: inline-PTX
-// wrappers for mbarriers, bulk/tensor async copies (TMA), cp.async, and the
-// tcgen05 tensor-memory / MMA instructions of sm_100-family GPUs (built for
-// sm_103a).
+// wrappers for mbarriers, bulk/tensor async copies (TMA) and the tcgen05
+// tensor-memory / MMA instructions of sm_100-family GPUs (built for sm_103a).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -40,12 +39,6 @@ MOE_DEV bool bounds_ok(bool in_range, uint32_t *err) {
 
 MOE_DEV uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-MOE_DEV uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 // ---------------------------------------------------------------- mbarrier --
@@ -197,33 +190,6 @@ MOE_DEV void tma_load_2d(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
         : "memory");
 }
 
-MOE_DEV void cp_async_16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src)
-                 : "memory");
-}
-MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-MOE_DEV void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-MOE_DEV void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-// Wait until at most `depth` (1..7) of this thread's cp.async groups are pending.
-MOE_DEV void cp_async_wait_depth(uint32_t depth) {
-    switch (depth) {
-        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
-        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
-        case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
-        default: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    }
-}
-
-// Make generic-proxy writes to shared memory visible to the async proxy
-// (TMA, tensor-core operand reads).
-MOE_DEV void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 MOE_DEV void named_bar_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -264,28 +230,12 @@ MOE_DEV void tc_fence_before() {
 MOE_DEV void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Arrive on `bar` once every tcgen05 async operation issued so far by this
-// thread has completed.
-MOE_DEV void tc_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            bar)
-        : "memory");
-}
 
 // Warp-collective forms: every lane of the warp executes them with the same
 // operands and elect.sync picks the one lane that issues.  (Issuing from
 // warp-uniform code keeps the operands in uniform registers.)
-MOE_DEV void mma_ts_f16_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
+// Arrive on `bar` once every tcgen05 async operation issued so far by the
+// elected thread has completed.
 MOE_DEV void tc_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -335,17 +285,6 @@ MOE_DEV void tc_commit2_elect(uint32_t bar1, uint32_t bar2) {
         "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(
             bar1),
         "r"(bar2)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (fp16 in, fp32 accumulate).
-MOE_DEV void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
