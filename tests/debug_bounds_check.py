@@ -2,9 +2,9 @@
 MOE_INT4_DEBUG_BOUNDS=1: the forward through the debug-bounds build of the
 library (index checks on every routing buffer read back by a kernel) on shapes
 that cover each block-height regime, a multi-block align, the routed entry
-point, dropped invalid ids and MXFP4 weights.  Each output must match the oracle and no check
-may fire (MOE_DEVERR_BOUNDS clear).  Prints one line per case; exits non-zero on
-the first failure."""
+point, dropped invalid ids and MXFP4 weights.  Each output must match the
+oracle and no check may fire (MOE_DEVERR_BOUNDS clear).  Prints one line per
+case; exits non-zero on the first failure."""
 import os
 import sys
 
