@@ -551,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             uint32_t v[32];
                             if (FMT == 1)
-                            dequant_row_fp4(lo, hi, sc, v);
-                        else
-                            dequant_row(lo, hi, sc, dqc, v);
+                                dequant_row_fp4(lo, hi, sc, v);
+                            else
+                                dequant_row(lo, hi, sc, dqc, v);
                             tc_fence_after();
                             tmem_st_32x32b_x32_wait(st + uu * 64 + g * 32, v);
                         }
@@ -603,7 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (pa.next(sched, tile_a, kb0_a, kb1_a))
                     rows_load(ahead, p.sorted_ids, (tile_a / p.RT) * BM, BM);
             } else {
-                nr = block_rows(p.sorted_ids, pos0, BM, p.P);
+                // 16-row blocks issue 16-column MMAs whatever their row count, so
+                // they skip the dependent load of the block's entries (measured
+                // 2 % faster for the down GEMM at decode)
+                nr = (BM == 16) ? 16 : block_rows(p.sorted_ids, pos0, BM, p.P);
             }
             // ---- issue (every stage is visited, see the dequant role)
             if (issuer) {
