@@ -42,7 +42,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--workload", choices=sorted(inputs.WORKLOADS), default="k26_decode")
     ap.add_argument("--ms", type=str, default=None, help="comma-separated token counts")
     ap.add_argument("--pool", type=int, default=8, help="routings per M")
     ap.add_argument("--flush-mb", type=int, default=512)
@@ -525,7 +525,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
 
 def main():
     args = parse_args()
-    cfg = inputs.CONFIGS[args.config]
+    cfg = inputs.WORKLOADS[args.workload]
     if args.experts:
         cfg = dataclasses.replace(cfg, E=args.experts, name=f"{cfg.name}_E{args.experts}")
     if args.format != "int4":

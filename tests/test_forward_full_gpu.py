@@ -21,7 +21,7 @@ def _ops():
 
 @pytest.fixture(scope="module")
 def k26():
-    cfg = inputs.CONFIGS[1]
+    cfg = inputs.WORKLOADS["k26_decode"]
     w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
     pw = _ops().PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k)
     yield w, pw
@@ -30,7 +30,7 @@ def k26():
 
 @pytest.fixture(scope="module")
 def mid():
-    cfg = inputs.CONFIGS[4]
+    cfg = inputs.WORKLOADS["mid"]
     w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
     pw = _ops().PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k)
     yield w, pw
@@ -51,14 +51,15 @@ def _check(w, pw, cfg, M, n_samples=SAMPLES):
     return assert_parity(got[toks], ref, f"{cfg.name} M={M}")
 
 
-@pytest.mark.parametrize("cfg_idx,M", [(1, 1), (1, 9), (1, 90), (2, 256), (2, 512), (2, 1024),
-                                       (3, 8192)])
-def test_k26_workloads(k26, cfg_idx, M):
+@pytest.mark.parametrize("workload,M", [("k26_decode", 1), ("k26_decode", 9), ("k26_decode", 90),
+                                        ("k26_verify", 256), ("k26_verify", 512),
+                                        ("k26_verify", 1024), ("k26_prefill", 8192)])
+def test_k26_workloads(k26, workload, M):
     w, pw = k26
-    print(_check(w, pw, inputs.CONFIGS[cfg_idx], M))
+    print(_check(w, pw, inputs.WORKLOADS[workload], M))
 
 
 @pytest.mark.parametrize("M", [1, 32, 128, 2048, 8192])
 def test_mid_workload(mid, M):
     w, pw = mid
-    print(_check(w, pw, inputs.CONFIGS[4], M, n_samples=M if M <= 32 else SAMPLES))
+    print(_check(w, pw, inputs.WORKLOADS["mid"], M, n_samples=M if M <= 32 else SAMPLES))

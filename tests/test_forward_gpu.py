@@ -69,7 +69,7 @@ def test_forward_matches_oracle(E, k, H, I, M, seed):
 
 
 def test_tiny_workload_seed():
-    cfg = inputs.CONFIGS[0]
+    cfg = inputs.WORKLOADS["tiny"]
     w = inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
     pw = _ops().PackedWeights(w, cfg.E, cfg.H, cfg.I, cfg.top_k)
     t = inputs.make_tokens(cfg, 16)

@@ -30,7 +30,7 @@ def test_weights_shapes_ranges_and_determinism():
 
 
 def test_routing_uniform():
-    cfg = inputs.CONFIGS[0]
+    cfg = inputs.WORKLOADS["tiny"]
     t = inputs.make_tokens(cfg, 16)
     ids, w = t["topk_ids"], t["topk_weights"]
     assert ids.shape == (16, 2) and w.shape == (16, 2)
@@ -40,7 +40,7 @@ def test_routing_uniform():
 
 
 def test_routing_skewed_share():
-    cfg = inputs.CONFIGS[2]
+    cfg = inputs.WORKLOADS["k26_verify"]
     small = inputs.MoEConfig("s", 384, 8, 64, 64, (256,), "skewed", 1, 2)
     t = inputs.make_tokens(small, 256)
     assert abs(t["hot_share"] - 0.5) <= 0.011
@@ -51,7 +51,7 @@ def test_routing_skewed_share():
 def test_router_logits_reproduce_the_routings():
     """Routing the generated router logits gives the generator's routings
     (uniform and skewed recipes)."""
-    for cfg, M in ((inputs.CONFIGS[0], 16), (inputs.MoEConfig("s", 64, 8, 128, 128, (40,), "skewed", 2, 9), 40)):
+    for cfg, M in ((inputs.WORKLOADS["tiny"], 16), (inputs.MoEConfig("s", 64, 8, 128, 128, (40,), "skewed", 2, 9), 40)):
         pool = [inputs.make_tokens(cfg, M)["topk_ids"]] + [ids for ids, _ in inputs.routing_pool(cfg, M, 2)]
         for ids, lg in zip(pool, inputs.router_logits_pool(cfg, M, 2)):
             rid, _ = inputs.route(lg, cfg.top_k)

@@ -46,19 +46,19 @@ class MoEConfig:
     Ms: tuple
     routing: str = "uniform"
     weight_seed: int = 0
-    index: int = 0
+    seed_id: int = 0  # stream id of the token and routing draws
     extra: dict = field(default_factory=dict)
 
 
-# The five workloads: tiny, K2.6-shaped decode, K2.6-shaped verify batch (skewed
-# routing), K2.6-shaped prefill chunk, mid-size MoE.
-CONFIGS = {
-    0: MoEConfig("tiny", 8, 2, 256, 128, (16,), "uniform", 0, 0),
-    1: MoEConfig("k26_decode", 384, 8, 7168, 2048, (1, 9, 90), "uniform", 1, 1),
-    2: MoEConfig("k26_verify", 384, 8, 7168, 2048, (256, 512, 1024), "skewed", 1, 2),
-    3: MoEConfig("k26_prefill", 384, 8, 7168, 2048, (8192,), "uniform", 1, 3),
-    4: MoEConfig("mid", 64, 6, 4096, 1408, (1, 32, 128, 2048, 8192), "uniform", 4, 4),
-}
+# The five workloads, by name: tiny, K2.6-shaped decode, K2.6-shaped verify batch
+# (skewed routing), K2.6-shaped prefill chunk, mid-size MoE.
+WORKLOADS = {c.name: c for c in (
+    MoEConfig("tiny", 8, 2, 256, 128, (16,), "uniform", 0, 0),
+    MoEConfig("k26_decode", 384, 8, 7168, 2048, (1, 9, 90), "uniform", 1, 1),
+    MoEConfig("k26_verify", 384, 8, 7168, 2048, (256, 512, 1024), "skewed", 1, 2),
+    MoEConfig("k26_prefill", 384, 8, 7168, 2048, (8192,), "uniform", 1, 3),
+    MoEConfig("mid", 64, 6, 4096, 1408, (1, 32, 128, 2048, 8192), "uniform", 4, 4),
+)}
 
 
 def bf16_bits_from_f32(a) -> np.ndarray:
@@ -163,7 +163,7 @@ def route_skewed(logits: np.ndarray, k: int, hot: np.ndarray, share=0.5, tol=0.0
 
 def make_tokens(cfg: MoEConfig, M: int) -> dict:
     """x (bf16 bits [M, H]), topk_ids int32 [M, k], topk_weights fp32 [M, k]."""
-    rng = np.random.default_rng([0, cfg.index, M])
+    rng = np.random.default_rng([0, cfg.seed_id, M])
     x = bf16_bits_from_f32(rng.standard_normal((M, cfg.H), dtype=np.float32))
     logits = rng.standard_normal((M, cfg.E), dtype=np.float32)
     out = {"x": x}
@@ -189,7 +189,7 @@ def routing_pool(cfg: MoEConfig, M: int, n: int, base_seed: int = 1000):
     used to rotate the touched expert set between timed calls."""
     pool = []
     for r in range(n):
-        rng = np.random.default_rng([0, cfg.index, M, base_seed + r])
+        rng = np.random.default_rng([0, cfg.seed_id, M, base_seed + r])
         logits = rng.standard_normal((M, cfg.E), dtype=np.float32)
         if cfg.routing == "skewed":
             perm = rng.permutation(cfg.E)
@@ -206,12 +206,12 @@ def router_logits_pool(cfg: MoEConfig, M: int, n: int, base_seed: int = 1000):
     routings of routing_pool(cfg, M, n): the same draws, with the hot-expert
     bias of the skewed recipe added, so that routing them gives those routings."""
     out = []
-    rng = np.random.default_rng([0, cfg.index, M])
+    rng = np.random.default_rng([0, cfg.seed_id, M])
     rng.standard_normal((M, cfg.H), dtype=np.float32)  # x
     seeds = [None] + [base_seed + r for r in range(n)]
     for sd in seeds:
         if sd is not None:
-            rng = np.random.default_rng([0, cfg.index, M, sd])
+            rng = np.random.default_rng([0, cfg.seed_id, M, sd])
         logits = rng.standard_normal((M, cfg.E), dtype=np.float32)
         if cfg.routing == "skewed":
             perm = rng.permutation(cfg.E)
