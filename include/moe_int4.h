@@ -16,8 +16,9 @@
  * value = (q - 8) * scale, q in {0..15}, scale bf16 ("Building the Benchmark":
  * INT4, group size 32).  Activations are bf16 and the output bf16 or fp32.  The
  * tensor cores multiply fp16 operands with fp32 accumulation: each dequantised
- * weight (q - 8) * scale is rounded once to fp16 (11 significant bits, where
- * bf16 would keep 8), x is converted to fp16 (exact for |x| in [2^-14, 65504];
+ * weight (q - 8) * scale is formed in fp16 with one rounding (11 significant
+ * bits, where bf16 would keep 8; it is exact for scales in [2^-14, 8188], since
+ * a bf16 scale's 8 significant bits times |q - 8| <= 8 fit in 11), x is converted to fp16 (exact for |x| in [2^-14, 65504];
  * larger magnitudes saturate to +-65504, smaller ones lose precision as fp16
  * subnormals), and the SwiGLU intermediate is stored as fp16 saturated to
  * +-65504.
@@ -255,7 +256,7 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
  *                    overwritten (tokens whose pairs were all dropped get 0).
  * workspace: >= moe_int4_workspace_bytes(M, shape, 0) bytes of device memory,
  *   16-byte aligned; no initial contents are required.  It holds the align
- *   buffers, the bf16 intermediate, fp32 accumulators and the error words; two
+ *   buffers, the gathered fp16 x rows, the fp16 intermediate, fp32 accumulators and the error words; two
  *   calls in flight at once must not share it.
  * M == 0 returns MOE_OK without touching out.  Every pointer must be 16-byte
  * aligned.  The call launches only kernels (no host sync, no allocation).
