@@ -56,3 +56,19 @@ def test_router_logits_reproduce_the_routings():
         for ids, lg in zip(pool, inputs.router_logits_pool(cfg, M, 2)):
             rid, _ = inputs.route(lg, cfg.top_k)
             np.testing.assert_array_equal(rid, ids)
+
+
+def test_dequantised_int4_weights_are_exact_in_fp16():
+    """The kernels form (q - 8) * scale in fp16.  For a bf16 scale s in
+    [2^-14, 8188] that product needs at most 8 + 3 significant bits and stays in
+    fp16's normal range, so it is exact: checked here over every positive bf16
+    value of that range and every q."""
+    bits = np.arange(0x3880, 0x4600, dtype=np.uint16)        # 2^-14 .. 8192 (exclusive)
+    s = inputs.f32_from_bf16_bits(bits).astype(np.float64)
+    s = s[(s >= 2.0 ** -14) & (s <= 8188.0)]
+    assert s.min() == 2.0 ** -14 and s.max() > 8000.0
+    prod = np.arange(-8, 8, dtype=np.float64)[:, None] * s[None, :]
+    np.testing.assert_array_equal(prod.astype(np.float16).astype(np.float64), prod)
+    # the next bf16 value, 8192, overflows fp16 at q = 0: -8 * 8192 = -65536
+    with np.errstate(over="ignore"):
+        assert not np.isfinite(np.float16(-8.0 * 8192.0))
