@@ -131,6 +131,11 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8_sat(uint4 v) {
     return v;
 }
 
+// U: 16-byte loads in flight per lane.  A warp copies a row in ceil(H / (256 U))
+// dependent memory round trips; where the rows are few (decode) that latency is
+// the kernel's duration, so U = 16 (2 round trips at H = 7168); where there are
+// many, U = 4 keeps the registers low enough for every block to be resident.
+template <int U>
 __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ sorted,
                                    const int32_t *__restrict__ num_post_pad, int P, int top_k, int H,
                                    uint16_t *__restrict__ xs, int cap, uint32_t *err) {
@@ -147,16 +152,15 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t
         if (!bounds_ok(pair >= 0, err)) continue;
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(pair / top_k) * H);
         uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)pos * H);
-        // four 16-byte loads in flight per lane (a row is H / 256 of them per lane)
-        int c = lane;
-        for (; c + 96 < n8; c += 128) {
-            uint4 v[4];
+        for (int c0 = lane; c0 < n8; c0 += 32 * U) {
+            uint4 v[U];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = src[c + 32 * u];
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * u < n8) v[u] = src[c0 + 32 * u];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) dst[c + 32 * u] = bf16x8_to_f16x8_sat(v[u]);
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * u < n8) dst[c0 + 32 * u] = bf16x8_to_f16x8_sat(v[u]);
         }
-        for (; c < n8; c += 32) dst[c] = bf16x8_to_f16x8_sat(src[c]);
     }
 }
 
@@ -171,7 +175,12 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const i
     cfg.attrs = &attr;
     cfg.numAttrs = pdl_attr(attr);
     const int cap = cap_rows > (size_t)INT32_MAX ? INT32_MAX : (int)cap_rows;
-    cudaLaunchKernelEx(&cfg, gather_rows_kernel, x, sorted, npp, P, top_k, H, xs, cap, err);
+    // the U = 16 kernel keeps two 256-thread blocks per SM resident: use it
+    // where the whole grid fits in that
+    if (blocks <= (size_t)sms * 2)
+        cudaLaunchKernelEx(&cfg, gather_rows_kernel<16>, x, sorted, npp, P, top_k, H, xs, cap, err);
+    else
+        cudaLaunchKernelEx(&cfg, gather_rows_kernel<4>, x, sorted, npp, P, top_k, H, xs, cap, err);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }
