@@ -47,10 +47,11 @@
 //
 // Warp roles (768 threads): 0 weight producer, 1 TMEM owner (in gate/up it
 // also zeroes the down GEMM's fp32 accumulator), 2 B loader, 3 scale producer,
-// 4-15 dequant (three teams), 16-19 MMA issue, 20-23 epilogue.  Each (slab, sub-stage) has its own issuing warp and accumulator
-// (the epilogue sums them): one thread issuing tcgen05.mma waits tens of
-// cycles per instruction while MMAs from several warps overlap.  Every
-// mbarrier wait is bounded (MOE_DEVERR_TIMEOUT).
+// 4-15 dequant (three teams), 16-19 MMA issue, 20-23 epilogue.  Each (slab,
+// sub-stage) has its own issuing warp and accumulator (the epilogue sums them):
+// one thread issuing tcgen05.mma waits tens of cycles per instruction while
+// MMAs from several warps overlap.  Every mbarrier wait is bounded
+// (MOE_DEVERR_TIMEOUT).
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
