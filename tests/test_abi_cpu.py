@@ -113,3 +113,57 @@ def test_null_and_alignment_rejected_on_host():
     assert lib.moe_int4_pack(good, good, 1, 128, 64, 1, good, good, None) == -2
     assert lib.moe_int4_pack(good, good, 1, 128, 64, 0, good, good, None) == -2
     assert ops.moe_int4_strerror(-4) == "workspace too small"
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_int4.h"
+
+int main(void) {
+    moe_int4_shape sh;
+    memset(&sh, 0, sizeof sh);
+    sh.E = 384; sh.top_k = 8; sh.hidden = 7168; sh.inter = 2048; sh.group = 32;
+    sh.out_dtype = MOE_OUT_F32;
+    printf("%zu\n", moe_int4_packed_bytes(384, 4096, 7168));
+    printf("%zu\n", moe_int4_workspace_bytes(90, &sh, 0));
+    printf("%d\n", moe_int4_block_m(90, &sh));
+    printf("%zu\n", moe_align_capacity(90, 8, 384, 16));
+    printf("%d\n", moe_int4_forward(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, &sh,
+                                    NULL, 0, NULL));
+    sh.hidden = 7200;
+    printf("%zu\n", moe_int4_workspace_bytes(90, &sh, 0));
+    printf("%s\n", moe_int4_strerror(MOE_ERR_SHAPE));
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
+    """The boundary is a C ABI: a C11 program (pedantic, warnings as errors)
+    includes the header, links the library and calls its host-side entry points,
+    which agree with the Python binding."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    ops.load_library()
+    lib = ops.library_path()
+    src = tmp_path / "use_abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_abi"
+    r = subprocess.run([gcc, "-std=c11", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), lib,
+                        "-Wl,-rpath," + os.path.dirname(lib), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    sh = ops.Shape.of(384, 8, 7168, 2048)
+    assert int(out[0]) == ops.moe_int4_packed_bytes(384, 4096, 7168)
+    assert int(out[1]) == ops.moe_int4_workspace_bytes(90, sh)
+    assert int(out[2]) == ops.moe_int4_block_m(90, sh) == 16
+    assert int(out[3]) == ops.moe_align_capacity(90, 8, 384, 16) == 720 + 384 * 15
+    assert int(out[4]) == 0          # M == 0: a no-op
+    assert int(out[5]) == 0          # a rejected shape needs no workspace
+    assert out[6] == ops.moe_int4_strerror(-2)
