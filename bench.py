@@ -57,6 +57,10 @@ def parse_args():
                     help="expert weight format (mxfp4: E2M1 codes, E8M0 scale per 32)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (a smaller case of the same kernels, for ncu captures)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the verify, prefill and mid-size blocks of the default run")
+    ap.add_argument("--extra-calls", type=int, default=20,
+                    help="timed calls per M of each extra workload")
     return ap.parse_args()
 
 
@@ -298,6 +302,162 @@ def run_reference(args, cfg, Ms, world, rank):
 
 
 # --------------------------------------------------------------- GPU arm --
+def roofline_of(recs, w13_b, w2_b, top_k, H, I, hbm_peak, tc_peak, peak_src, workload):
+    """Roofline position of the dominant kernel over profiled calls: the fused
+    decode kernel where the forward ran it (both GEMMs in one launch), else the
+    GEMM with the larger share of the per-kernel event time.  Algorithmic bytes
+    (touched experts x packed weights + scales) or FLOPs (2 x pairs x the
+    GEMM's weights) per launch over its CUDA-event duration, whichever bound is
+    the slower at the peaks."""
+    g1_ms = [r["stages"][1] for r in recs]
+    g2_ms = [r["stages"][2] for r in recs]
+    if all(r["fused"] for r in recs):
+        dominant, k_ms = "fused", g1_ms
+        k_bytes = [r["touched"] * (w13_b + w2_b) for r in recs]
+        k_flops = [2.0 * r["M"] * top_k * H * I * 3 for r in recs]
+    else:
+        dominant = "gate_up" if sum(g1_ms) >= sum(g2_ms) else "down"
+        k_ms = g1_ms if dominant == "gate_up" else g2_ms
+        k_bytes = [r["touched"] * (w13_b if dominant == "gate_up" else w2_b) for r in recs]
+        k_flops = [2.0 * r["M"] * top_k * H * I * (2 if dominant == "gate_up" else 1)
+                   for r in recs]
+    t_hbm = sum(k_bytes) / (hbm_peak * 1e9)
+    t_tc = sum(k_flops) / (tc_peak * 1e12)
+    bytes_mean = statistics.mean(k_bytes)
+    traffic, traffic_src = kernel_traffic(dominant, workload, bytes_mean)
+    if t_hbm >= t_tc:  # weight streaming bound
+        ach = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                "frac": ach / hbm_peak, "peak_source": f"{peak_src} (hbm_gbs)"}
+    else:  # tensor bound; fp16 operands run at the bf16 dense rate
+        ach = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": ach / tc_peak,
+                "peak_source": f"{peak_src} (bf16_tflops; fp16 has the same dense rate)"}
+    roof.update({"traffic": traffic, "kernel": dominant, "traffic_source": traffic_src,
+                 "bytes_per_launch_mean": bytes_mean,
+                 "flops_per_launch_mean": statistics.mean(k_flops),
+                 "launch_ms_mean": statistics.mean(k_ms)})
+    return roof
+
+
+class Workload:
+    """Device inputs of one workload: a routing pool per M, x, the output and a
+    shared workspace; one_call() runs one timed forward after an L2 flush."""
+
+    def __init__(self, args, cfg, Ms, pw, dev, flush):
+        import torch
+        from weight_only_int4_moe_gb300 import ops
+        self.args, self.cfg, self.Ms, self.pw, self.flush = args, cfg, Ms, pw, flush
+        shape = pw.shape
+        self.shape = shape
+        ws_bytes = max(ops.moe_int4_workspace_bytes(M, shape) for M in Ms)
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        self.data = {}
+        for M in Ms:
+            t = inputs.make_tokens(cfg, M)
+            pool = ([(t["topk_ids"], t["topk_weights"])]
+                    + inputs.routing_pool(cfg, M, args.pool - 1))
+            x = torch.from_numpy(t["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+            routes = []
+            for ids, tw in pool:
+                n = len(inputs.touched_experts(ids, cfg.E))
+                routes.append((torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev), n))
+            out = torch.empty((M, cfg.H), dtype=shape.torch_out_dtype, device=dev)
+            d = {"x": x, "routes": routes, "out": out, "host": t}
+            if args.routed:
+                d["logits"] = [torch.from_numpy(lg).to(dev)
+                               for lg in inputs.router_logits_pool(cfg, M, args.pool - 1)]
+                d["rids"] = torch.empty((M, cfg.top_k), dtype=torch.int32, device=dev)
+                d["rw"] = torch.empty((M, cfg.top_k), dtype=torch.float32, device=dev)
+            self.data[M] = d
+
+    def one_call(self, M, r, rec, stream, profiled=False):
+        import torch
+        from weight_only_int4_moe_gb300 import ops
+        d = self.data[M]
+        pw, shape = self.pw, self.shape
+        ids, tw, n_touched = d["routes"][r % len(d["routes"])]
+        self.flush.zero_()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        if self.args.routed:
+            ops.moe_int4_forward_routed(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales,
+                                        d["logits"][r % len(d["logits"])], shape, out=d["out"],
+                                        topk_ids=d["rids"], topk_weights=d["rw"],
+                                        workspace=self.ws, stream=stream)
+        else:
+            ops.moe_int4_forward(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales, ids, tw,
+                                 shape, out=d["out"], workspace=self.ws, stream=stream)
+        ev1.record(stream)
+        launches = ops.moe_int4_last_launch_count()
+        if rec is not None:
+            stages = ops.moe_int4_profile_read() if profiled else None  # waits for the events
+            ev1.synchronize()
+            rec.append({"M": M, "ms": ev0.elapsed_time(ev1), "stages": stages,
+                        "touched": n_touched, "launches": launches,
+                        "fused": ops.moe_int4_fused(M, shape)})
+
+    def profiled(self, steps, first, stream):
+        """The same calls again with CUDA events between the kernels, on the
+        launching stream (for the stage split and the roofline)."""
+        import torch
+        from weight_only_int4_moe_gb300 import ops
+        ops.moe_int4_profile_enable(True)
+        prec = []
+        for s in range(steps):
+            for M in self.Ms:
+                self.one_call(M, first + s, prec, stream, profiled=True)
+        torch.cuda.synchronize()
+        ops.moe_int4_profile_enable(False)
+        return prec
+
+    def per_m(self, rec, prec, hbm_peak, tc_peak, fmt):
+        cfg = self.cfg
+        w13_b, w2_b = expert_bytes(cfg.H, cfg.I, fmt)
+        out = {}
+        for M in self.Ms:
+            rs = [r for r in rec if r["M"] == M]
+            us = [r["ms"] * 1e3 for r in rs]
+            touched = statistics.mean(r["touched"] for r in rs)
+            bytes_w = touched * (w13_b + w2_b)
+            flops = 2.0 * M * cfg.top_k * 3 * cfg.H * cfg.I
+            t_med = statistics.median(us)
+            t_hbm = bytes_w / (hbm_peak * 1e9) * 1e6
+            t_tc = flops / (tc_peak * 1e12) * 1e6
+            st = np.mean([r["stages"] for r in prec if r["M"] == M], axis=0)
+            fused = all(r["fused"] for r in rs)
+            out[str(M)] = {
+                "us_per_call": t_med, "us_mean": statistics.mean(us), "calls": len(us),
+                "tokens_per_s": M / (t_med / 1e6),
+                "touched_experts": touched,
+                "weight_bytes": bytes_w,
+                "hbm_gbs": bytes_w / (t_med / 1e6) / 1e9,
+                "frac_hbm": bytes_w / (t_med / 1e6) / 1e9 / hbm_peak,
+                "tflops": flops / (t_med / 1e6) / 1e12,
+                "frac_tensor": flops / (t_med / 1e6) / 1e12 / tc_peak,
+                "ideal_us": {"hbm": t_hbm, "tensor": t_tc},
+                "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                "roofline_frac": max(t_hbm, t_tc) / t_med,
+                "kernels": "fused" if fused else "separate",
+                "stage_us": ({"align": st[0] * 1e3, "fused": st[1] * 1e3, "finalize": st[3] * 1e3}
+                             if fused else
+                             {"align+gather": st[0] * 1e3, "gate_up": st[1] * 1e3,
+                              "down": st[2] * 1e3, "finalize": st[3] * 1e3}),
+            }
+        return out
+
+
+def extra_workloads(args, base_cfg):
+    """The other workloads of the default run, each measured in a few calls per M
+    (their own per-M numbers and roofline position): verify and prefill on the
+    decode workload's weights, the mid-size MoE on its own."""
+    if args.no_extra or args.workload != "k26_decode" or args.experts or args.ms:
+        return []
+    return [(inputs.WORKLOADS[n], n != "mid") for n in ("k26_verify", "k26_prefill", "mid")]
+
+
 def run_ours(args, cfg, Ms, world, rank, local):
     import torch
     from weight_only_int4_moe_gb300 import ops
@@ -306,6 +466,8 @@ def run_ours(args, cfg, Ms, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     out_dtype = ops.MOE_OUT_F32 if args.out_dtype == "f32" else ops.MOE_OUT_BF16
 
     w = make_weights(cfg, args.format)
@@ -313,59 +475,16 @@ def run_ours(args, cfg, Ms, world, rank, local):
                            fmt=args.format)
     shape = pw.shape
     Mmax = max(Ms)
-    ws = ops.alloc_workspace(Mmax, shape, device=dev)
-    ws_bytes_max = max(ops.moe_int4_workspace_bytes(M, shape) for M in Ms)
-    if ws.numel() < ws_bytes_max:
-        ws = torch.empty(ws_bytes_max, dtype=torch.uint8, device=dev)
     flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
     w13_b, w2_b = expert_bytes(cfg.H, cfg.I, args.format)
-
-    data = {}
-    for M in Ms:
-        t = inputs.make_tokens(cfg, M)
-        pool = [(t["topk_ids"], t["topk_weights"])] + inputs.routing_pool(cfg, M, args.pool - 1)
-        x = torch.from_numpy(t["x"].view(np.int16)).to(dev).view(torch.bfloat16)
-        routes = []
-        for ids, tw in pool:
-            n = len(inputs.touched_experts(ids, cfg.E))
-            routes.append((torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev), n))
-        out = torch.empty((M, cfg.H), dtype=shape.torch_out_dtype, device=dev)
-        data[M] = {"x": x, "routes": routes, "out": out, "host": t, "pool": pool}
-        if args.routed:
-            data[M]["logits"] = [torch.from_numpy(lg).to(dev)
-                                 for lg in inputs.router_logits_pool(cfg, M, args.pool - 1)]
-            data[M]["rids"] = torch.empty((M, cfg.top_k), dtype=torch.int32, device=dev)
-            data[M]["rw"] = torch.empty((M, cfg.top_k), dtype=torch.float32, device=dev)
+    wl = Workload(args, cfg, Ms, pw, dev, flush)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-
-    def one_call(M, r, rec, profiled=False):
-        d = data[M]
-        ids, tw, n_touched = d["routes"][r % len(d["routes"])]
-        flush.zero_()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        if args.routed:
-            ops.moe_int4_forward_routed(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales,
-                                        d["logits"][r % len(d["logits"])], shape, out=d["out"],
-                                        topk_ids=d["rids"], topk_weights=d["rw"], workspace=ws,
-                                        stream=stream)
-        else:
-            ops.moe_int4_forward(d["x"], pw.w13, pw.w13_scales, pw.w2, pw.w2_scales, ids, tw,
-                                 shape, out=d["out"], workspace=ws, stream=stream)
-        ev1.record(stream)
-        launches = ops.moe_int4_last_launch_count()
-        if rec is not None:
-            stages = ops.moe_int4_profile_read() if profiled else None  # waits for the events
-            ev1.synchronize()
-            rec.append({"M": M, "ms": ev0.elapsed_time(ev1), "stages": stages,
-                        "touched": n_touched, "launches": launches})
 
     # warm-up
     for s in range(args.warmup):
         for M in Ms:
-            one_call(M, s, None)
+            wl.one_call(M, s, None, stream)
     torch.cuda.synchronize()
 
     # timed region: whole calls, no events between the kernels (they would
@@ -378,82 +497,56 @@ def run_ours(args, cfg, Ms, world, rank, local):
     wall0 = time.perf_counter()
     for s in range(args.steps):
         for M in Ms:
-            one_call(M, args.warmup + s, rec)
+            wl.one_call(M, args.warmup + s, rec, stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(dist, True)
     clk = clocks.stop()
-    # per-kernel times: the same calls again with CUDA events between the
-    # kernels, on the launching stream (for the stage split and the roofline)
-    ops.moe_int4_profile_enable(True)
-    prec = []
-    for s in range(args.steps):
-        for M in Ms:
-            one_call(M, args.warmup + s, prec, profiled=True)
-    torch.cuda.synchronize()
-    ops.moe_int4_profile_enable(False)
+    prec = wl.profiled(args.steps, args.warmup, stream)
 
     ms_per_step = sum(r["ms"] for r in rec) / args.steps
     ms_per_step_max = allreduce_max(dist, ms_per_step, True)
     tokens_per_step = sum(Ms)
     value = job_rate(world, tokens_per_step, ms_per_step_max / 1e3)
+    per_m = wl.per_m(rec, prec, hbm_peak, tc_peak, args.format)
+    roofline = roofline_of(prec, w13_b, w2_b, cfg.top_k, cfg.H, cfg.I, hbm_peak, tc_peak,
+                           peak_src, cfg.name)
 
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    per_m = {}
-    for M in Ms:
-        rs = [r for r in rec if r["M"] == M]
-        us = [r["ms"] * 1e3 for r in rs]
-        touched = statistics.mean(r["touched"] for r in rs)
-        bytes_w = touched * (w13_b + w2_b)
-        flops = 2.0 * M * cfg.top_k * 3 * cfg.H * cfg.I
-        t_med = statistics.median(us)
-        t_hbm = bytes_w / (hbm_peak * 1e9) * 1e6
-        t_tc = flops / (tc_peak * 1e12) * 1e6
-        st = np.mean([r["stages"] for r in prec if r["M"] == M], axis=0)
-        per_m[str(M)] = {
-            "us_per_call": t_med, "us_mean": statistics.mean(us),
-            "tokens_per_s": M / (t_med / 1e6),
-            "touched_experts": touched,
-            "weight_bytes": bytes_w,
-            "hbm_gbs": bytes_w / (t_med / 1e6) / 1e9,
-            "frac_hbm": bytes_w / (t_med / 1e6) / 1e9 / hbm_peak,
-            "tflops": flops / (t_med / 1e6) / 1e12,
-            "frac_tensor": flops / (t_med / 1e6) / 1e12 / tc_peak,
-            "ideal_us": {"hbm": t_hbm, "tensor": t_tc},
-            "roofline_frac": max(t_hbm, t_tc) / t_med,
-            "stage_us": {"align": st[0] * 1e3, "gate_up": st[1] * 1e3, "down": st[2] * 1e3,
-                         "finalize": st[3] * 1e3},
+    # the other workloads: a few calls per M each, same timing rules
+    workloads = {}
+    for xcfg, shared in extra_workloads(args, cfg):
+        if shared:
+            xpw = pw
+        else:
+            xw = make_weights(xcfg, args.format)
+            xpw = ops.PackedWeights(xw, xcfg.E, xcfg.H, xcfg.I, xcfg.top_k, device=dev,
+                                    out_dtype=out_dtype, fmt=args.format)
+            del xw
+        xpw.shape.top_k = xcfg.top_k
+        xl = Workload(args, xcfg, xcfg.Ms, xpw, dev, flush)
+        for s in range(3):
+            for M in xcfg.Ms:
+                xl.one_call(M, s, None, stream)
+        xrec = []
+        for s in range(args.extra_calls):
+            for M in xcfg.Ms:
+                xl.one_call(M, 3 + s, xrec, stream)
+        torch.cuda.synchronize()
+        xprec = xl.profiled(max(3, args.extra_calls // 2), 3, stream)
+        xb13, xb2 = expert_bytes(xcfg.H, xcfg.I, args.format)
+        workloads[xcfg.name] = {
+            "config": {"E": xcfg.E, "top_k": xcfg.top_k, "hidden": xcfg.H, "inter": xcfg.I,
+                       "Ms": list(xcfg.Ms), "routing": xcfg.routing,
+                       "block_m": {str(M): ops.moe_int4_block_m(M, xpw.shape)
+                                   for M in xcfg.Ms}},
+            "per_m": xl.per_m(xrec, xprec, hbm_peak, tc_peak, args.format),
+            "roofline": roofline_of(xprec, xb13, xb2, xcfg.top_k, xcfg.H, xcfg.I, hbm_peak,
+                                    tc_peak, peak_src, xcfg.name),
         }
-
-    # dominant kernel: the gate/up GEMM (largest stage share); algorithmic bytes
-    # = touched experts x (w13 int4 + scales) per launch
-    g1_ms = [r["stages"][1] for r in prec]
-    g1_bytes = [r["touched"] * w13_b for r in prec]
-    g2_ms = [r["stages"][2] for r in prec]
-    dominant = "gate_up" if sum(g1_ms) >= sum(g2_ms) else "down"
-    k_ms = g1_ms if dominant == "gate_up" else g2_ms
-    k_bytes = g1_bytes if dominant == "gate_up" else [r["touched"] * w2_b for r in prec]
-    # algorithmic FLOPs of the launch: 2 x pairs x (2I x H for gate/up, H x I for down)
-    k_flops = [2.0 * r["M"] * cfg.top_k * cfg.H * cfg.I * (2 if dominant == "gate_up" else 1)
-               for r in prec]
-    t_hbm = sum(k_bytes) / (hbm_peak * 1e9)
-    t_tc = sum(k_flops) / (tc_peak * 1e12)
-    bytes_mean = statistics.mean(k_bytes)
-    traffic, traffic_src = kernel_traffic(dominant, cfg.name, bytes_mean)
-    if t_hbm >= t_tc:  # weight streaming bound
-        ach = sum(k_bytes) / (sum(k_ms) / 1e3) / 1e9
-        roofline = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": ach / hbm_peak, "peak_source": f"{peak_src} (hbm_gbs)"}
-    else:  # tensor bound; fp16 operands run at the bf16 dense rate
-        ach = sum(k_flops) / (sum(k_ms) / 1e3) / 1e12
-        roofline = {"bound": "tensor", "achieved": ach, "peak": tc_peak, "unit": "TFLOP/s",
-                    "frac": ach / tc_peak,
-                    "peak_source": f"{peak_src} (bf16_tflops; fp16 has the same dense rate)"}
-    roofline.update({"traffic": traffic, "kernel": dominant, "traffic_source": traffic_src,
-                     "bytes_per_launch_mean": bytes_mean,
-                     "flops_per_launch_mean": statistics.mean(k_flops),
-                     "launch_ms_mean": statistics.mean(k_ms)})
+        del xl
+        if not shared:
+            del xpw
+        torch.cuda.empty_cache()
 
     # end to end through the host-buffer entry point
     e2e = None
@@ -462,7 +555,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
         hosts = {}
         h2d = d2h = 0
         for M in Ms:
-            t = data[M]["host"]
+            t = wl.data[M]["host"]
             hx = torch.from_numpy(t["x"].view(np.int16)).pin_memory()
             hids = torch.from_numpy(t["topk_ids"]).pin_memory()
             htw = torch.from_numpy(t["topk_weights"]).pin_memory()
@@ -517,6 +610,7 @@ def run_ours(args, cfg, Ms, world, rank, local):
             "per_m": per_m, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(sum(r["launches"] for r in rec)),
             "clocks": clk, "wall_s_timed": wall,
+            "workloads": workloads,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -18,10 +18,12 @@
  * tensor cores multiply fp16 operands with fp32 accumulation: each dequantised
  * weight (q - 8) * scale is formed in fp16 with one rounding (11 significant
  * bits, where bf16 would keep 8; it is exact for scales in [2^-14, 8188], since
- * a bf16 scale's 8 significant bits times |q - 8| <= 8 fit in 11), x is converted to fp16 (exact for |x| in [2^-14, 65504];
- * larger magnitudes saturate to +-65504, smaller ones lose precision as fp16
- * subnormals), and the SwiGLU intermediate is stored as fp16 saturated to
- * +-65504.
+ * a bf16 scale's 8 significant bits times |q - 8| <= 8 fit in 11, and
+ * moe_int4_pack counts the scales outside that range), x is converted to fp16
+ * (exact for |x| in [2^-14, 65504]; below, fp16 subnormals are within 2^-25 of
+ * x), and the SwiGLU intermediate is stored as fp16.  An x element or an
+ * intermediate beyond +-65504 (or not finite) is saturated to +-65504 and
+ * raises the device flag MOE_DEVERR_RANGE: such a call's output is not valid.
  *
  * Conventions for every entry point:
  *  - All array pointers are DEVICE pointers owned by the caller, except those of
@@ -66,6 +68,10 @@ enum {
 #define MOE_DEVERR_BOUNDS 0x4u        /* debug-bounds builds only (-DMOE_DEBUG_BOUNDS): an index
                                          read back from a routing buffer was out of range; the
                                          access was kept in bounds and the result is invalid */
+#define MOE_DEVERR_RANGE 0x8u         /* a value outside fp16's finite range reached an fp16
+                                         tensor-core operand and was saturated to +-65504: an x
+                                         element or a SwiGLU intermediate beyond +-65504,
+                                         infinite or NaN; the output is not valid */
 
 /* Output element types (moe_int4_shape.out_dtype). */
 #define MOE_OUT_BF16 0 /* bf16, rounded to nearest even from the fp32 combine */
@@ -82,9 +88,14 @@ enum {
 #define MOE_W_INT4 0
 #define MOE_W_MXFP4 1
 
+/* Forward flags (moe_int4_shape.flags). */
+#define MOE_FLAG_UNFUSED 0x1 /* run the gather, gate/up and down steps as separate kernels
+                                even where the fused decode kernel applies (same results) */
+
 /* Layer shape.  Supported: 1 <= E <= 1024, 1 <= top_k <= min(E, 32),
  * hidden % 128 == 0, inter % 128 == 0, group == 32, weight_format one of
- * MOE_W_*.  A zero-initialised weight_format is INT4. */
+ * MOE_W_*, flags a combination of MOE_FLAG_*.  Zero-initialised weight_format and
+ * flags mean INT4 and the default launch plan. */
 typedef struct {
     int32_t E;             /* number of experts */
     int32_t top_k;         /* routing slots per token */
@@ -93,6 +104,7 @@ typedef struct {
     int32_t group;         /* quantisation group along K; must be 32 */
     int32_t out_dtype;     /* MOE_OUT_BF16 or MOE_OUT_F32 */
     int32_t weight_format; /* MOE_W_INT4 or MOE_W_MXFP4 (how the weights were packed) */
+    int32_t flags;         /* MOE_FLAG_* */
 } moe_int4_shape;
 
 /* ------------------------------------------------------------------------- */
@@ -131,11 +143,17 @@ size_t moe_int4_packed_scale_bytes(int E, int N, int K);
  *   Scales: per stage 1024 bytes, [slab][row][2] fp16, groups 2kb and 2kb+1 of
  *   the slab's k block; each bf16 scale is converted to fp16 (exact for
  *   magnitudes in [2^-14, 65504], saturating above, fp16 subnormal below).
+ * inexact_scales  optional (NULL: not counted): device uint32, incremented
+ *   (atomically, on the stream) once per non-zero scale whose magnitude lies
+ *   outside [2^-14, 8188] or that is not finite.  When it stays 0, every
+ *   dequantised weight (q - 8) * scale the kernels form is exact in fp16.  The
+ *   caller zeroes it first.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE (N or K not multiples as above),
  *   MOE_ERR_ALIGN, MOE_ERR_CUDA.
  */
 int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
-                  int is_w13, void *packed, void *packed_scales, moe_stream_t stream);
+                  int is_w13, void *packed, void *packed_scales, uint32_t *inexact_scales,
+                  moe_stream_t stream);
 
 /*
  * moe_mxfp4_pack: canonical MXFP4 weights -> the same device layout (forward
@@ -183,8 +201,11 @@ size_t moe_align_scratch_bytes(int M, int top_k, int E);
  *        space).  Entries past num_post_pad are not written.
  *      expert_ids int32: the expert of each block of block_m entries.
  *      num_post_pad int32 [1]: total entries written.
- *      Pairs whose id is outside [0, E) are dropped and flagged (needs
- *      err_flags, may be NULL to skip the flag: uint32 [2] = flags, count).
+ *      Pairs whose id is outside [0, E) are dropped and reported in
+ *      err_flags (uint32 [2] = flags, count; NULL: not reported): the call ORs
+ *      MOE_DEVERR_BAD_EXPERT_ID into the flags and adds the number dropped to
+ *      the count, so the caller zeroes both words first (a clean call leaves
+ *      them as they were).
  * block_m: 1..256.  scratch: moe_align_scratch_bytes bytes (NULL if 0).
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
  */
@@ -206,9 +227,12 @@ int moe_align(const int32_t *topk_ids, int M, int top_k, int E, int block_m,
  * Limit: moe_align_scratch_bytes(M, top_k, E) <= 1 MiB (E = 384: up to
  * 698,368 pairs; E = 1024: 262,144), else MOE_ERR_NOALLOC_LIMIT and nothing
  * is launched.
- * The first call on each device looks up the array's device address on the
- * current device (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Nothing in the array needs to start at zero (each call
+ * Routings of up to 4096 pairs need no table and touch neither the array nor
+ * any set-up.  The first larger call on each device looks up the array's
+ * device address on the current device (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  The address is cached per device and
+ * does not survive cudaDeviceReset: after a reset, do not call this entry
+ * point again in the same process.  Nothing in the array needs to start at zero (each call
  * writes every entry it reads), but all calls share it: calls whose kernels
  * overlap on the GPU (different streams, or host threads) race and give wrong
  * results; serialise them, e.g. on one stream.
@@ -233,6 +257,11 @@ size_t moe_int4_workspace_bytes(int M, const moe_int4_shape *shape, int flags);
 /* The routing block height the forward uses for M tokens (16..192). */
 int moe_int4_block_m(int M, const moe_int4_shape *shape);
 
+/* 1 if a forward of M tokens runs the fused decode kernel (gather, gate/up and
+ * down GEMMs in one launch; see moe_int4_forward), 0 if it runs them as separate
+ * kernels (or M or the shape is invalid). */
+int moe_int4_fused(int M, const moe_int4_shape *shape);
+
 /*
  * moe_int4_workspace_layout: byte offsets inside the workspace of a forward of
  * M tokens, for inspecting a finished call: offsets[0] error words (uint32 flags,
@@ -255,11 +284,19 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
  * Out: out           [M][hidden] of shape->out_dtype (bf16 bits or fp32),
  *                    overwritten (tokens whose pairs were all dropped get 0).
  * workspace: >= moe_int4_workspace_bytes(M, shape, 0) bytes of device memory,
- *   16-byte aligned; no initial contents are required.  It holds the align
- *   buffers, the gathered fp16 x rows, the fp16 intermediate, fp32 accumulators and the error words; two
- *   calls in flight at once must not share it.
+ *   16-byte aligned.  It holds the align buffers, the gathered fp16 x rows, the
+ *   fp16 intermediate, fp32 accumulators and the error words; two calls in
+ *   flight at once must not share it.  No initial contents are required except
+ *   for the error words (its first 8 bytes), which accumulate over calls: clear
+ *   them (moe_int4_clear_errors) once after allocating the workspace.
  * M == 0 returns MOE_OK without touching out.  Every pointer must be 16-byte
  * aligned.  The call launches only kernels (no host sync, no allocation).
+ * Launch plan: the align kernel, then, for routings of at most 4096 pairs
+ * whose block height is at most 128 (decode-sized batches), one persistent
+ * kernel that gathers x, runs the gate/up GEMM and then the down GEMM (its
+ * CTAs hand work to each other through counters in the workspace, with bounded
+ * waits; it expects to get every SM within about two seconds); otherwise a
+ * gather kernel and one kernel per GEMM.  bf16 output adds a conversion kernel.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,
  *   MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  */
@@ -320,7 +357,11 @@ int moe_int4_forward_host(const uint16_t *x_host, const void *w13_packed,
 /*
  * moe_int4_get_errors: read (synchronously on `stream`) the device error flags
  * (MOE_DEVERR_*) and the count of dropped routing pairs accumulated in the
- * workspace since the last moe_int4_clear_errors.  Either output may be NULL.
+ * workspace since the last moe_int4_clear_errors.  Every forward on the
+ * workspace ORs its flags into the first word and adds its dropped pairs to
+ * the second; nothing resets them but moe_int4_clear_errors, so a flag raised
+ * by one call (a timeout, a bad id) is still there after later clean calls.
+ * Either output may be NULL.
  */
 int moe_int4_get_errors(const void *workspace, uint32_t *flags, uint32_t *count,
                         moe_stream_t stream);

@@ -26,6 +26,20 @@ def test_header_declares_the_entry_points():
     assert set(names) == set(ops.EXPORTED)
 
 
+def test_header_constants_match_the_binding():
+    """The device error flags, output types and weight formats of the header
+    are the values the Python binding uses."""
+    text = open(HEADER).read()
+    defs = dict(re.findall(r"^#define\s+(MOE_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text,
+                           flags=re.M))
+    for name in ("MOE_DEVERR_BAD_EXPERT_ID", "MOE_DEVERR_TIMEOUT", "MOE_DEVERR_BOUNDS",
+                 "MOE_DEVERR_RANGE", "MOE_OUT_BF16", "MOE_OUT_F32", "MOE_W_INT4", "MOE_W_MXFP4",
+                 "MOE_WS_HOST_IO", "MOE_FLAG_UNFUSED"):
+        assert int(defs[name], 0) == getattr(ops, name), name
+    flags = [int(v, 0) for k, v in defs.items() if k.startswith("MOE_DEVERR_")]
+    assert all(f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)
+
+
 def test_library_exports_every_declared_symbol():
     lib = ops.load_library()
     assert os.path.exists(ops.library_path())
@@ -109,9 +123,9 @@ def test_null_and_alignment_rejected_on_host():
     rc = lib.moe_int4_forward(None, None, None, None, None, None, None, None, 0, ctypes.byref(sh),
                               None, 0, None)
     assert rc == 0
-    assert lib.moe_int4_pack(None, good, 1, 256, 64, 1, good, good, None) == -1
-    assert lib.moe_int4_pack(good, good, 1, 128, 64, 1, good, good, None) == -2
-    assert lib.moe_int4_pack(good, good, 1, 128, 64, 0, good, good, None) == -2
+    assert lib.moe_int4_pack(None, good, 1, 256, 64, 1, good, good, None, None) == -1
+    assert lib.moe_int4_pack(good, good, 1, 128, 64, 1, good, good, None, None) == -2
+    assert lib.moe_int4_pack(good, good, 1, 128, 64, 0, good, good, None, None) == -2
     assert ops.moe_int4_strerror(-4) == "workspace too small"
 
 

@@ -2,6 +2,8 @@
 configuration the benchmark times (moe_int4_forward with its own plan), checked
 against the oracle on sampled tokens (the oracle computes each token's output
 one by one), plus checks that hold for every output at any size."""
+import copy
+
 import numpy as np
 import pytest
 
@@ -39,7 +41,7 @@ def mid():
 
 def _check(w, pw, cfg, M, n_samples=SAMPLES):
     t = inputs.make_tokens(cfg, M)
-    got = gpu_forward(pw, t)
+    got = gpu_forward(pw, t).astype(np.float64)
     assert np.all(np.isfinite(got))
     # tokens whose every slot went to experts... all tokens have k valid slots here,
     # so no output row may be identically zero
@@ -63,3 +65,42 @@ def test_k26_workloads(k26, workload, M):
 def test_mid_workload(mid, M):
     w, pw = mid
     print(_check(w, pw, inputs.WORKLOADS["mid"], M, n_samples=M if M <= 32 else SAMPLES))
+
+
+def _bf16_view(pw):
+    """The same packed weights with bf16 output (the fp32 combine rounded to
+    nearest even by the finalize kernel)."""
+    ops = _ops()
+    b = copy.copy(pw)
+    sh = pw.shape
+    b.shape = ops.Shape.of(sh.E, sh.top_k, sh.hidden, sh.inter, ops.MOE_OUT_BF16, sh.weight_format,
+                           sh.flags)
+    return b
+
+
+@pytest.mark.parametrize("workload,M", [("k26_decode", 1), ("k26_decode", 90),
+                                        ("k26_verify", 1024), ("k26_prefill", 8192)])
+def test_k26_bf16_output(k26, workload, M):
+    """bf16 output at full size, held to the same bound as fp32 output."""
+    w, pw = k26
+    print(_check(w, _bf16_view(pw), inputs.WORKLOADS[workload], M))
+
+
+@pytest.mark.parametrize("M", [128, 2048])
+def test_mid_bf16_output(mid, M):
+    w, pw = mid
+    print(_check(w, _bf16_view(pw), inputs.WORKLOADS["mid"], M))
+
+
+@pytest.mark.parametrize("workload,M", [("k26_decode", 1), ("k26_decode", 90), ("k26_verify", 512)])
+def test_k26_separate_kernels(k26, workload, M):
+    """The same decode-sized calls through the separate gather / gate/up / down
+    kernels (where the default plan runs the fused decode kernel)."""
+    ops = _ops()
+    w, pw = k26
+    b = copy.copy(pw)
+    sh = pw.shape
+    b.shape = ops.Shape.of(sh.E, sh.top_k, sh.hidden, sh.inter, sh.out_dtype, sh.weight_format,
+                           ops.MOE_FLAG_UNFUSED)
+    assert ops.moe_int4_fused(M, pw.shape) and not ops.moe_int4_fused(M, b.shape)
+    print(_check(w, b, inputs.WORKLOADS[workload], M))

@@ -34,6 +34,7 @@ int check_shape(const moe_int4_shape *sh) {
     if (sh->group != 32) return MOE_ERR_SHAPE;
     if (sh->out_dtype != MOE_OUT_BF16 && sh->out_dtype != MOE_OUT_F32) return MOE_ERR_SHAPE;
     if (sh->weight_format != MOE_W_INT4 && sh->weight_format != MOE_W_MXFP4) return MOE_ERR_SHAPE;
+    if (sh->flags & ~MOE_FLAG_UNFUSED) return MOE_ERR_SHAPE;
     return MOE_OK;
 }
 
@@ -64,6 +65,7 @@ int choose_block_m(long long P, int E) {
 
 struct Plan {
     int M, E, k, H, I, P, BM, RT1, RT2, n_chunks, out_f32;
+    bool fused;  // the fused decode kernel (gather + gate/up + down in one launch)
     size_t cap, blocks_cap, tiles1_cap;
     size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_cnt, off_partial, off_a,
         off_x16, off_acc, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
@@ -86,13 +88,17 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.cap = (size_t)p.P + touched * (size_t)(p.BM - 1);
     p.blocks_cap = p.cap / p.BM + 1;
     p.tiles1_cap = p.blocks_cap * p.RT1;
+    p.fused = !(sh->flags & MOE_FLAG_UNFUSED) && p.n_chunks == 0 && p.BM <= 128;
     size_t o = 0;
     p.off_err = o; o += 256;
     p.off_npp = o; o += 256;
     p.off_sorted = o; o = rup(o + p.cap * 4, 256);
     p.off_expert = o; o = rup(o + p.blocks_cap * 4, 256);
     p.off_chunk = o; o = rup(o + (size_t)p.n_chunks * p.E * 4, 256);
-    p.off_cnt = o; o = rup(o + p.tiles1_cap * 4, 256);
+    // counters zeroed by the align launch: gate/up split counters, then (fused
+    // kernel) per-block finished gate/up tiles and the CTAs done with their
+    // gather and zeroing share
+    p.off_cnt = o; o = rup(o + (p.tiles1_cap + p.blocks_cap + 1) * 4, 256);
     p.off_partial = o; o = rup(o + (size_t)kMaxGrid * 4 * p.BM * 128 * 4, 256);
     p.off_a = o; o = rup(o + p.cap * (size_t)p.I * 2, 256);
     p.off_x16 = o; o = rup(o + p.cap * (size_t)p.H * 2, 256);  // x rows, bucketed, fp16
@@ -193,7 +199,8 @@ size_t moe_int4_packed_scale_bytes(int E, int N, int K) {
 }
 
 int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K, int is_w13,
-                  void *packed, void *packed_scales, moe_stream_t stream) {
+                  void *packed, void *packed_scales, uint32_t *inexact_scales,
+                  moe_stream_t stream) {
     if (!q || !scales || !packed || !packed_scales) return MOE_ERR_NULL;
     if (E < 1 || N < 1 || K < 1) return MOE_ERR_SHAPE;
     if (is_w13) {
@@ -204,7 +211,7 @@ int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
     if (!aligned16(q) || !aligned16(scales) || !aligned16(packed) || !aligned16(packed_scales))
         return MOE_ERR_ALIGN;
     cudaError_t e = launch_pack(q, scales, E, N, K, is_w13, packed, packed_scales,
-                                reinterpret_cast<cudaStream_t>(stream));
+                                inexact_scales, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -270,6 +277,11 @@ size_t moe_int4_workspace_bytes(int M, const moe_int4_shape *shape, int flags) {
     if (M == 0) return 256;
     Plan p = make_plan(M, shape);
     return (flags & MOE_WS_HOST_IO) ? p.total_io : p.total;
+}
+
+int moe_int4_fused(int M, const moe_int4_shape *shape) {
+    if (check_shape(shape) != MOE_OK || M < 1 || M > (1 << 20)) return 0;
+    return make_plan(M, shape).fused ? 1 : 0;
 }
 
 int moe_int4_block_m(int M, const moe_int4_shape *shape) {
@@ -361,11 +373,11 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     al.err = err;
     al.chunk_tab = reinterpret_cast<int32_t *>(ws + pl.off_chunk);
     al.n_chunks = pl.n_chunks;
-    // the align launch zeroes the gate/up split counters; the gate/up GEMM
-    // zeroes the down accumulator (off the align's critical path)
+    // the align launch zeroes the counters; the gate/up GEMM (or the fused
+    // kernel) zeroes the down accumulator (off the align's critical path)
     ZeroArgs z{};
     z.ptr[0] = ws + pl.off_cnt;
-    z.n16[0] = (pl.tiles1_cap * 4 + 15) / 16;
+    z.n16[0] = ((pl.tiles1_cap + pl.blocks_cap + 1) * 4 + 15) / 16;
     uint16_t *x16 = reinterpret_cast<uint16_t *>(ws + pl.off_x16);
     const size_t zero_bytes = (z.n16[0] + z.n16[1]) * 16;
     int zero_ctas = (int)(zero_bytes / (64 * 1024));
@@ -384,8 +396,8 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     } else if (launch_align(al, z, zero_ctas, s, &launches) != cudaSuccess) {
         return MOE_ERR_CUDA;
     }
-    if (launch_gather_rows(x, sorted, npp, pl.P, pl.k, pl.H, x16, pl.cap, err, sms, s, &launches) !=
-        cudaSuccess)
+    if (!pl.fused && launch_gather_rows(x, sorted, npp, pl.P, pl.k, pl.H, x16, pl.cap, err, sms,
+                                        s, &launches) != cudaSuccess)
         return MOE_ERR_CUDA;
     prof_record(1, s);
 
@@ -406,35 +418,54 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     g.round_robin = 1;
     g.fmt = shape->weight_format;
 
-    GemmParams g1 = g;
-    g1.zero_out = reinterpret_cast<float4 *>(acc);
-    g1.zero_n16 = (size_t)pl.M * pl.H * 4 / 16;
-    g1.wq = reinterpret_cast<const uint8_t *>(w13_packed);
-    g1.wsc = reinterpret_cast<const uint8_t *>(w13_scales);
-    g1.a_out = a_buf;
-    g1.partial = reinterpret_cast<float *>(ws + pl.off_partial);
-    g1.tile_cnt = reinterpret_cast<int32_t *>(ws + pl.off_cnt);
-    g1.RT = pl.RT1;
-    g1.KSS = pl.H / 64;
-    g1.KS = (g1.KSS + 1) / 2;
-    if (!plan_gemm_smem(1, g1)) return MOE_ERR_SHAPE;
-    CUtensorMap tmap_x;
-    if (!encode_rows_map(&tmap_x, x16, pl.cap, pl.H, pl.BM)) return MOE_ERR_CUDA;
-    if (launch_gemm(1, g1, &tmap_x, grid, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
-    prof_record(2, s);
+    int32_t *cnt = reinterpret_cast<int32_t *>(ws + pl.off_cnt);
+    g.g[0].wq = reinterpret_cast<const uint8_t *>(w13_packed);
+    g.g[0].wsc = reinterpret_cast<const uint8_t *>(w13_scales);
+    g.g[0].RT = pl.RT1;
+    g.g[0].KSS = pl.H / 64;
+    g.g[0].KS = (g.g[0].KSS + 1) / 2;
+    g.g[1].wq = reinterpret_cast<const uint8_t *>(w2_packed);
+    g.g[1].wsc = reinterpret_cast<const uint8_t *>(w2_scales);
+    g.g[1].RT = pl.RT2;
+    g.g[1].KSS = pl.I / 128;
+    g.g[1].KS = (g.g[1].KSS + 1) / 2;
+    g.a_out = a_buf;
+    g.partial = reinterpret_cast<float *>(ws + pl.off_partial);
+    g.tile_cnt = cnt;
+    g.out_acc = acc;
+    CUtensorMap tmap_x, tmap_a;
+    if (!encode_rows_map(&tmap_x, x16, pl.cap, pl.H, pl.BM) ||
+        !encode_rows_map(&tmap_a, a_buf, pl.cap, pl.I, pl.BM))
+        return MOE_ERR_CUDA;
 
-    GemmParams g2 = g;
-    g2.wq = reinterpret_cast<const uint8_t *>(w2_packed);
-    g2.wsc = reinterpret_cast<const uint8_t *>(w2_scales);
-    g2.out_acc = acc;
-    g2.RT = pl.RT2;
-    g2.KSS = pl.I / 128;
-    g2.KS = (g2.KSS + 1) / 2;
-    if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
-    CUtensorMap tmap;
-    if (!encode_rows_map(&tmap, a_buf, pl.cap, pl.I, pl.BM)) return MOE_ERR_CUDA;
-    if (launch_gemm(2, g2, &tmap, grid, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
-    prof_record(3, s);
+    if (pl.fused) {
+        // one persistent kernel: gather, gate/up + SwiGLU, down + combine
+        GemmParams gf = g;
+        gf.zero_out = reinterpret_cast<float4 *>(acc);
+        gf.zero_n16 = (size_t)pl.M * pl.H * 4 / 16;
+        gf.x = x;
+        gf.x16 = x16;
+        gf.blk_done = cnt + pl.tiles1_cap;
+        gf.prep_done = cnt + pl.tiles1_cap + pl.blocks_cap;
+        if (!plan_gemm_smem(3, gf)) return MOE_ERR_SHAPE;
+        if (launch_gemm(3, gf, &tmap_x, &tmap_a, grid, s, &launches) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        prof_record(2, s);
+        prof_record(3, s);
+    } else {
+        GemmParams g1 = g;
+        g1.zero_out = reinterpret_cast<float4 *>(acc);
+        g1.zero_n16 = (size_t)pl.M * pl.H * 4 / 16;
+        if (!plan_gemm_smem(1, g1)) return MOE_ERR_SHAPE;
+        if (launch_gemm(1, g1, &tmap_x, &tmap_a, grid, s, &launches) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        prof_record(2, s);
+        GemmParams g2 = g;
+        if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
+        if (launch_gemm(2, g2, &tmap_x, &tmap_a, grid, s, &launches) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        prof_record(3, s);
+    }
 
     if (!pl.out_f32 && launch_finalize(acc, reinterpret_cast<uint16_t *>(out),
                                        (size_t)pl.M * pl.H, sms, s, &launches) != cudaSuccess)

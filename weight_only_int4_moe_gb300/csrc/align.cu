@@ -10,6 +10,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -49,8 +51,9 @@ __device__ int block_exclusive_scan(int v, int *warp_tot, int *total) {
 }
 
 // Given per-expert counts cnt[0..E) (shared), compute padded bucket offsets
-// into off[0..E) (shared), write expert_ids, pad entries, num_post_pad and the
-// error words.  One 1024-thread block; E <= 1024.
+// into off[0..E) (shared), write expert_ids, pad entries and num_post_pad, and
+// add the dropped pairs to the error words (which accumulate until the caller
+// clears them).  One 1024-thread block; E <= 1024.
 __device__ void align_layout(const AlignArgs &a, const int *cnt, int *off, int *scan_tmp) {
     const int e = threadIdx.x;
     const int c = (e < a.E) ? cnt[e] : 0;
@@ -68,8 +71,10 @@ __device__ void align_layout(const AlignArgs &a, const int *cnt, int *off, int *
         *a.num_post_pad = total;
         if (a.err) {
             const uint32_t dropped = (uint32_t)(a.P - valid_total);
-            a.err[0] = dropped ? kErrBadExpert : 0u;
-            a.err[1] = dropped;
+            if (dropped) {
+                atomicOr(&a.err[0], kErrBadExpert);
+                atomicAdd(&a.err[1], dropped);
+            }
         }
     }
 }
@@ -101,14 +106,6 @@ __device__ void align_place_round(const AlignArgs &a, int i0, int *base, int *wt
     __syncthreads();
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
-    float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
-    lo = fminf(fmaxf(lo, -65504.0f), 65504.0f);
-    hi = fminf(fmaxf(hi, -65504.0f), 65504.0f);
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
 __device__ void zero_regions(const ZeroArgs &z, int cta, int nctas) {
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
     const size_t stride = (size_t)nctas * blockDim.x;
@@ -123,14 +120,6 @@ __device__ void zero_regions(const ZeroArgs &z, int cta, int nctas) {
 // Rows of x in bucketed order, as the fp16 tensor-core operand of the gate/up
 // GEMM: xs[pos] = fp16(x[sorted_ids[pos] / top_k]) for every real entry (pad
 // rows are left as they are; the GEMM ignores their results).  One warp per row.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8_sat(uint4 v) {
-    v.x = bf16x2_to_f16x2_sat(v.x);
-    v.y = bf16x2_to_f16x2_sat(v.y);
-    v.z = bf16x2_to_f16x2_sat(v.z);
-    v.w = bf16x2_to_f16x2_sat(v.w);
-    return v;
-}
-
 // U: 16-byte loads in flight per lane.  A warp copies a row in ceil(H / (256 U))
 // dependent memory round trips; where the rows are few (decode) that latency is
 // the kernel's duration, so U = 16 (2 round trips at H = 7168); where there are
@@ -140,28 +129,21 @@ __global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t
                                    const int32_t *__restrict__ num_post_pad, int P, int top_k, int H,
                                    uint16_t *__restrict__ xs, int cap, uint32_t *err) {
     pdl_wait();  // sorted_ids and num_post_pad come from the align launch
+    // Only now may the gate/up GEMM start: its weight stream reads the align's
+    // outputs without waiting for this kernel (it waits only before it reads
+    // the gathered rows).
     pdl_launch_dependents();
     int npp = *num_post_pad;
     if (!bounds_ok(npp >= 0 && npp <= cap, err)) npp = 0;
-    const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
-    const int n8 = H / 8;
+    bool bad = false;
     for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < npp; pos += warps) {
         const int pair = sorted[pos];
         if (pair >= P) continue;  // a pad
         if (!bounds_ok(pair >= 0, err)) continue;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(pair / top_k) * H);
-        uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)pos * H);
-        for (int c0 = lane; c0 < n8; c0 += 32 * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (c0 + 32 * u < n8) v[u] = src[c0 + 32 * u];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (c0 + 32 * u < n8) dst[c0 + 32 * u] = bf16x8_to_f16x8_sat(v[u]);
-        }
+        gather_row<U>(x + (size_t)(pair / top_k) * H, xs + (size_t)pos * H, H, bad);
     }
+    report_range(bad, err);
 }
 
 cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const int32_t *npp, int P,
@@ -371,20 +353,27 @@ size_t align_smem_fused(int E) { return (size_t)(2 * E + 64 + kAlignWarps * E) *
 size_t align_smem_scan(int E) { return (size_t)(2 * E + 64) * sizeof(int); }
 size_t align_smem_scatter(int E) { return (size_t)(E + kAlignWarps * E) * sizeof(int); }
 
+// Raises the dynamic shared-memory limit of the align kernels, once per device
+// (under a lock: concurrent first calls from several host threads); a failure
+// is returned, and not recorded as done.
 static cudaError_t launch_align_attrs() {
+    static std::mutex mu;
     static bool attr_done[64] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        const int maxs = (int)align_smem_fused(1024);
-        cudaFuncSetAttribute(align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
-        cudaFuncSetAttribute(align_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
-        cudaFuncSetAttribute(align_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
-        cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
-        cudaFuncSetAttribute(route_align_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             maxs);
-        attr_done[dev] = true;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (attr_done[dev]) return cudaSuccess;
+    const int maxs = (int)align_smem_fused(1024);
+    const void *fns[] = {(const void *)align_fused_kernel, (const void *)align_hist_kernel,
+                         (const void *)align_scan_kernel, (const void *)align_scatter_kernel,
+                         (const void *)route_align_fused_kernel};
+    for (const void *f : fns) {
+        e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, maxs);
+        if (e != cudaSuccess) return e;
     }
+    attr_done[dev] = true;
     return cudaSuccess;
 }
 

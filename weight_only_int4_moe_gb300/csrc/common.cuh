@@ -14,6 +14,73 @@ namespace moe {
 constexpr uint32_t kErrBadExpert = 0x1u;
 constexpr uint32_t kErrTimeout = 0x2u;
 constexpr uint32_t kErrBounds = 0x4u;
+// A value left fp16's finite range on its way to an fp16 tensor-core operand
+// (an x element or a SwiGLU intermediate beyond +-65504, infinite or NaN): it
+// was saturated and the result is not valid.
+constexpr uint32_t kErrRange = 0x8u;
+
+// Records kErrRange once per warp if any lane saw an out-of-range value
+// (whole-warp call).
+MOE_DEV void report_range(bool bad, uint32_t *err) {
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && err) atomicOr(err, kErrRange);
+}
+
+// Two bf16 -> two fp16 (exact for magnitudes in [2^-14, 65504]; fp16
+// subnormals below, within 2^-25); `bad` records a value beyond +-65504,
+// infinite or NaN, which is saturated.
+MOE_DEV uint32_t bf16x2_to_f16x2_sat(uint32_t v, bool &bad) {
+    float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
+    bad |= !(fabsf(lo) <= 65504.0f) || !(fabsf(hi) <= 65504.0f);
+    lo = fminf(fmaxf(lo, -65504.0f), 65504.0f);
+    hi = fminf(fmaxf(hi, -65504.0f), 65504.0f);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+MOE_DEV uint4 bf16x8_to_f16x8_sat(uint4 v, bool &bad) {
+    v.x = bf16x2_to_f16x2_sat(v.x, bad);
+    v.y = bf16x2_to_f16x2_sat(v.y, bad);
+    v.z = bf16x2_to_f16x2_sat(v.z, bad);
+    v.w = bf16x2_to_f16x2_sat(v.w, bad);
+    return v;
+}
+
+// One row of H bf16 values to fp16 (the gate/up GEMM's B operand), copied by
+// one warp with U 16-byte loads in flight per lane: a row takes
+// ceil(H / (256 U)) dependent memory round trips.
+template <int U>
+MOE_DEV void gather_row(const uint16_t *src_row, uint16_t *dst_row, int H, bool &bad) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+    const int n8 = H / 8, lane = threadIdx.x & 31;
+    for (int c0 = lane; c0 < n8; c0 += 32 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (c0 + 32 * u < n8) v[u] = src[c0 + 32 * u];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (c0 + 32 * u < n8) dst[c0 + 32 * u] = bf16x8_to_f16x8_sat(v[u], bad);
+    }
+}
+
+// ------------------------------------------------- hand-offs between CTAs --
+// Acquire load at GPU scope (a counter that other CTAs release).
+MOE_DEV int ld_acquire_gpu(const int32_t *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Release add at GPU scope.
+MOE_DEV void red_release_gpu(int32_t *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy global accesses with the async proxy's
+// (TMA) accesses to global memory.
+MOE_DEV void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // Debug-bounds builds (-DMOE_DEBUG_BOUNDS) check the indices that kernels read
 // back from the routing buffers (block count, expert ids, pair ids) before using

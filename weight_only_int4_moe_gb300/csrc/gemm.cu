@@ -54,6 +54,8 @@
 // (MOE_DEVERR_TIMEOUT).
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -76,6 +78,9 @@ constexpr uint32_t kACols = 128;                // TMEM columns per A stage
 // hardware named barriers (0 is __syncthreads)
 constexpr uint32_t kBarEpi = 1;     // the four epilogue warps
 constexpr uint32_t kBarSlot0 = 2;   // A stage s written: all dequant warps arrive, issuers wait
+                                    // (ids 2..4: one per A stage or stage half)
+constexpr uint32_t kBarPrep = 5;    // fused kernel: the gather and zeroing warps (1, 20..23)
+constexpr uint32_t kPrepThreads = 5 * 32;
 
 // The schedule: tiles [0, rr) round-robin (whole tiles, CTA c takes c, c + G,
 // ...), then tiles [rr, tiles) split evenly by stages.  Stage indices of the
@@ -88,12 +93,12 @@ struct Sched {
     int tiles, rr, KS, G, cta;
 };
 
-__device__ __forceinline__ Sched make_sched(const GemmParams &p) {
+__device__ __forceinline__ Sched make_sched(const GemmParams &p, const GemmPhase &g) {
     Sched s;
-    int npp = *p.num_post_pad;
+    int npp = __ldcg(p.num_post_pad);
     if (!bounds_ok(npp >= 0 && npp <= p.cap && npp % p.block_m == 0, p.err)) npp = 0;
-    s.tiles = (npp / p.block_m) * p.RT;
-    s.KS = p.KS;
+    s.tiles = (npp / p.block_m) * g.RT;
+    s.KS = g.KS;
     s.G = gridDim.x;
     s.cta = blockIdx.x;
     const int waves = s.tiles / s.G;
@@ -141,7 +146,7 @@ __device__ __forceinline__ int range_owner(long long T, int G, long long it) {
 __device__ __forceinline__ int block_rows(const int32_t *sorted, int pos0, int BM, int P) {
     const int lane = threadIdx.x & 31;
     int cnt = 0;
-    for (int j = lane; j < BM; j += 32) cnt += (sorted[pos0 + j] < P) ? 1 : 0;
+    for (int j = lane; j < BM; j += 32) cnt += (__ldcg(sorted + pos0 + j) < P) ? 1 : 0;
     return __reduce_add_sync(0xffffffffu, cnt);
 }
 
@@ -156,7 +161,7 @@ __device__ __forceinline__ void rows_load(RowsAhead &r, const int32_t *sorted, i
 #pragma unroll
     for (int k = 0; k < 6; ++k) {
         const int j = lane + 32 * k;
-        r.v[k] = (j < BM) ? sorted[pos0 + j] : 0x7FFFFFFF;
+        r.v[k] = (j < BM) ? __ldcg(sorted + pos0 + j) : 0x7FFFFFFF;
     }
 }
 __device__ __forceinline__ int rows_count(const RowsAhead &r, int P) {
@@ -186,6 +191,26 @@ __device__ __forceinline__ bool wait_stage(uint32_t bar, uint32_t parity,
     while (true) {
         if (!warp_wait(bar, parity, abort, err)) return false;
         if (__all_sync(0xffffffffu, *tag == stage)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitTimeoutCycles) {
+            *abort = 1;
+            if (err) atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Bounded wait (one thread) until the counter *ctr, which other CTAs increment
+// with a release, reaches `target`: an acquire load, then polls with a short
+// sleep.  Gives up (false: the CTA's abort flag and MOE_DEVERR_TIMEOUT) after
+// kWaitTimeoutCycles or when another role of the CTA has aborted.
+__device__ bool wait_counter(const int32_t *ctr, int target, volatile int *abort, uint32_t *err) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    const long long t0 = clock64();
+#pragma unroll 1
+    while (true) {
+        __nanosleep(128);
+        if (ld_acquire_gpu(ctr) >= target) return true;
         if (*abort) return false;
         if (clock64() - t0 > kWaitTimeoutCycles) {
             *abort = 1;
@@ -258,8 +283,10 @@ __device__ __forceinline__ void dequant_row_fp4(const uint4 lo, const uint4 hi, 
     }
 }
 
-// fp32 -> fp16, saturating at the largest finite fp16 value.
-__device__ __forceinline__ uint16_t f16_sat(float v) {
+// fp32 -> fp16, saturating at the largest finite fp16 value; `bad` records a
+// value outside [-65504, 65504] (NaN included).
+__device__ __forceinline__ uint16_t f16_sat(float v, bool &bad) {
+    bad |= !(fabsf(v) <= 65504.0f);
     v = fminf(fmaxf(v, -65504.0f), 65504.0f);
     return __half_as_ushort(__float2half_rn(v));
 }
@@ -282,7 +309,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // of this warp's lane quadrant, written as the fp16 intermediate rows
 // a_row0 + column * I (columns >= nr are not stored).
 __device__ __forceinline__ void swiglu_store(uint32_t tl, int BM, int j_lo, int j_hi, int nr,
-                                             uint16_t *a_row0, int I) {
+                                             uint16_t *a_row0, int I, bool &bad) {
     for (int j0 = j_lo; j0 < j_hi; j0 += 16) {
         float gv[16], uv[16];
         tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
@@ -294,7 +321,7 @@ __device__ __forceinline__ void swiglu_store(uint32_t tl, int BM, int j_lo, int 
         uint16_t *dst = a_row0 + (size_t)j0 * I;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj, dst += I)
-            if (j0 + jj < nr) *dst = f16_sat(gv[jj]);
+            if (j0 + jj < nr) *dst = f16_sat(gv[jj], bad);
     }
 }
 
@@ -303,10 +330,22 @@ __device__ __forceinline__ void swiglu_store(uint32_t tl, int BM, int j_lo, int 
 // WIDE: the wide-block configuration (blocks of 144..192 tokens): A released
 // per sub-stage half (np = 2); down has one issuer and B slots of one
 // sub-stage.  Separate instantiations keep the common path's registers.
+// KIND 3 is the fused decode kernel: every role runs the gate/up GEMM's pieces,
+// then the down GEMM's, through the same rings (the down weights stream while
+// the gate/up epilogues finish); it also gathers the x rows and zeroes the
+// output accumulator, each CTA its share, and it waits on counters instead of
+// on a kernel boundary: the gate/up B loads wait until every CTA has finished
+// its gather share, and a block's down B loads until its gate/up tiles are all
+// written.  Every such wait is bounded.  Blocks of up to 128 rows only.
 // FMT: the weight format (0 INT4, 1 MXFP4); it changes only the dequant.
 template <int KIND, int WIDE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_b) {
+    moe_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmap_x,
+                    const __grid_constant__ CUtensorMap tmap_a) {
+    constexpr bool kFused = (KIND == 3);
+    static_assert(!(kFused && WIDE), "the fused kernel runs narrow blocks");
+    constexpr int kKind0 = kFused ? 1 : KIND;  // the GEMMs this kernel runs, in order
+    constexpr int kKind1 = kFused ? 2 : KIND;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -316,7 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int BM = p.block_m;
     const int n_w = p.n_w, n_b = p.n_b, n_a = p.n_a;
     const int ni = p.ni;    // MMA issuers (4: one per dequant group, 2: one per slab)
-    const int kss = p.KSS;  // sub-stages per tile
 
     // shared-memory map
     const uint32_t w_ring = base;
@@ -381,10 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // Everything above is set-up; from here on the kernel reads what the
-    // previous kernels of the forward wrote (routing buffers, gathered rows,
-    // zeroed counters and accumulators).
-    pdl_wait();
+    // Programmatic dependent launch.  In the separate GEMM kernels, the align
+    // kernel has completed before any CTA of this grid starts: the gather
+    // launches its dependents only after its own wait for the align, and the
+    // down GEMM's only predecessor is the gate/up GEMM.  So the routing buffers
+    // (align outputs) are read without waiting, through L2 (ld.global.cg: no
+    // stale L1 lines), and the weight stream, its dequant and the issue loop
+    // start while the previous kernel still runs.  Only the roles that read what
+    // the previous kernel wrote wait for it: the B loader (gathered x rows, or
+    // the intermediate) and the epilogue (split counters and partial slots, the
+    // accumulator that the gate/up GEMM zeroes).  The fused kernel follows the
+    // align kernel itself, so all of it waits.
+    if (kFused) pdl_wait();
     pdl_launch_dependents();
 
     // Tensor-memory column map: nbuf accumulator buffers of ni accumulators
@@ -395,37 +441,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_buf_cols = (uint32_t)(ni * BM);
     const uint32_t col_a = (uint32_t)nbuf * acc_buf_cols;
 
-    const Sched sched = make_sched(p);
-    PieceIter pi;
-    pi.init(sched);
     int tile, kb0, kb1;
 
     if (wid == 0 || wid == 3) {
         // --------------------------- weight (warp 0) / scale (warp 3) producer --
         if (lane == 0) {
             const bool scales = (wid == 3);
-            const uint8_t *src = scales ? p.wsc : p.wq;
             const uint32_t sub_bytes = scales ? kStageSBytes : kStageWBytes;
             const uint32_t dst_off = scales ? kStageW : 0u;
             const uint64_t pol = l2_policy_evict_first();
             uint32_t i = 0;
             Ring w(n_w);
             bool ok = true;
-            while (ok && pi.next(sched, tile, kb0, kb1)) {
-                const int b = tile / p.RT, r = tile % p.RT;
-                int e = p.expert_ids[b];
-                if (!bounds_ok(e >= 0 && e < p.E, p.err)) e = 0;
-                const size_t sub0 = ((size_t)e * p.RT + r) * kss;  // first sub-stage of the tile
-                for (int j = kb0; j < kb1; ++j, ++i, w.next()) {
-                    if (!mbar_wait(bar_w_empty + 8 * w.idx, w.ph ^ 1, abort_flag, p.err, 128)) {
-                        ok = false;
-                        break;
+            for (int kind = kKind0; kind <= kKind1 && ok; ++kind) {
+                const GemmPhase &G = p.g[kind - 1];
+                const Sched sched = make_sched(p, G);
+                PieceIter pi;
+                pi.init(sched);
+                const uint8_t *src = scales ? G.wsc : G.wq;
+                while (ok && pi.next(sched, tile, kb0, kb1)) {
+                    const int b = tile / G.RT, r = tile % G.RT;
+                    int e = __ldcg(p.expert_ids + b);
+                    if (!bounds_ok(e >= 0 && e < p.E, p.err)) e = 0;
+                    const size_t sub0 = ((size_t)e * G.RT + r) * G.KSS;  // first sub-stage of the tile
+                    for (int j = kb0; j < kb1; ++j, ++i, w.next()) {
+                        if (!mbar_wait(bar_w_empty + 8 * w.idx, w.ph ^ 1, abort_flag, p.err, 128)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bytes = stage_subs(j, G.KSS) * sub_bytes;
+                        if (!scales) w_tag[w.idx] = i;
+                        mbar_arrive_expect_tx(bar_w_full + 8 * w.idx, bytes);
+                        bulk_g2s(w_ring + w.idx * kStage + dst_off, src + (sub0 + 2 * j) * sub_bytes,
+                                 bytes, bar_w_full + 8 * w.idx, pol);
                     }
-                    const uint32_t bytes = stage_subs(j, kss) * sub_bytes;
-                    if (!scales) w_tag[w.idx] = i;
-                    mbar_arrive_expect_tx(bar_w_full + 8 * w.idx, bytes);
-                    bulk_g2s(w_ring + w.idx * kStage + dst_off, src + (sub0 + 2 * j) * sub_bytes,
-                             bytes, bar_w_full + 8 * w.idx, pol);
                 }
             }
             if (!ok) {  // let copies in flight land before the CTA exits
@@ -436,46 +485,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (wid == 1) {
-        // ------------------------------------------- output zeroing (gate/up) --
+        // ------------------------------------------------- output zeroing --
         // The tensor-memory owner has nothing to do until the end, so it clears
         // the down GEMM's fp32 accumulator, a grid-strided share per CTA, while
-        // the weights stream.  Streaming stores: the zero lines should not push
-        // the B rows that other row tiles re-read out of L2.  The down GEMM
-        // reads the accumulator only after this grid has completed.
+        // the weights stream (gate/up and fused kernels).  Streaming stores: the
+        // zero lines should not push the B rows that other row tiles re-read out
+        // of L2.  The separate down GEMM reads the accumulator only after this
+        // grid has completed; in the fused kernel the share is published below.
         if (p.zero_out) {
             const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
             const size_t stride = (size_t)gridDim.x * 32;
             for (size_t i = (size_t)blockIdx.x * 32 + lane; i < p.zero_n16; i += stride)
                 __stcs(p.zero_out + i, z4);
         }
+        if (kFused) {
+            // publish this CTA's share of the gather (epilogue warps) and of the
+            // zeroing: each thread's writes, then one release of the count
+            __threadfence();
+            fence_proxy_async_global();
+            named_bar_sync(kBarPrep, kPrepThreads);
+            if (lane == 0) red_release_gpu(p.prep_done, 1);
+        }
     } else if (wid == 2) {
         // ------------------------------------------------------ B loader --
         // B rows of the block (bucketed order) by 2-D TMA tensor copies: one
         // 64-column k block per copy, gate/up one per sub-stage, down two.
+        if (!kFused) pdl_wait();  // B rows are the previous kernel's output
         if (lane == 0) {
-            const int kb_per_sub = (KIND == 1) ? 1 : 2;
             uint32_t i = 0;
             bool ok = true;
             Ring bq(n_b);
-            while (ok && pi.next(sched, tile, kb0, kb1)) {
-                const int b = tile / p.RT;
-                for (int j = kb0; j < kb1 && ok; ++j) {
-                    // one slot per stage, or (wide blocks) one per sub-stage
-                    const int nsub = stage_subs(j, kss);
-                    const int nslots = b_sub ? nsub : 1;
-                    const int nblk = b_sub ? kb_per_sub : nsub * kb_per_sub;
-                    for (int sl = 0; sl < nslots; ++sl, ++i, bq.next()) {
-                        const uint32_t s = bq.idx;
-                        if (!mbar_wait(bar_b_empty + 8 * s, bq.ph ^ 1, abort_flag, p.err, 128)) {
-                            ok = false;
-                            break;
+            for (int kind = kKind0; kind <= kKind1 && ok; ++kind) {
+                const GemmPhase &G = p.g[kind - 1];
+                const CUtensorMap *tm = (kind == 1) ? &tmap_x : &tmap_a;
+                const int kb_per_sub = (kind == 1) ? 1 : 2;
+                const int kss = G.KSS;
+                const Sched sched = make_sched(p, G);
+                PieceIter pi;
+                pi.init(sched);
+                int ready_b = -1;  // fused: the block whose B rows are known written
+                if (kFused && kind == 1) {
+                    // every CTA's share of the gathered x rows is written
+                    ok = wait_counter(p.prep_done, (int)gridDim.x, abort_flag, p.err);
+                    fence_proxy_async_global();
+                }
+                while (ok && pi.next(sched, tile, kb0, kb1)) {
+                    const int b = tile / G.RT;
+                    if (kFused && kind == 2 && b != ready_b) {
+                        // every gate/up tile of block b (its whole intermediate rows)
+                        ok = wait_counter(p.blk_done + b, p.g[0].RT, abort_flag, p.err);
+                        fence_proxy_async_global();
+                        ready_b = b;
+                    }
+                    for (int j = kb0; j < kb1 && ok; ++j) {
+                        // one slot per stage, or (wide blocks) one per sub-stage
+                        const int nsub = stage_subs(j, kss);
+                        const int nslots = b_sub ? nsub : 1;
+                        const int nblk = b_sub ? kb_per_sub : nsub * kb_per_sub;
+                        for (int sl = 0; sl < nslots; ++sl, ++i, bq.next()) {
+                            const uint32_t s = bq.idx;
+                            if (!mbar_wait(bar_b_empty + 8 * s, bq.ph ^ 1, abort_flag, p.err, 128)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t dst = b_ring + s * p.b_stage_bytes;
+                            const int kb_first = 2 * kb_per_sub * j + sl * kb_per_sub;
+                            mbar_arrive_expect_tx(bar_b_full + 8 * s, (uint32_t)nblk * BM * 128u);
+                            for (int qb = 0; qb < nblk; ++qb)
+                                tma_load_2d(dst + qb * BM * 128, tm, (kb_first + qb) * 64, b * BM,
+                                            bar_b_full + 8 * s);
                         }
-                        const uint32_t dst = b_ring + s * p.b_stage_bytes;
-                        const int kb_first = 2 * kb_per_sub * j + sl * kb_per_sub;
-                        mbar_arrive_expect_tx(bar_b_full + 8 * s, (uint32_t)nblk * BM * 128u);
-                        for (int qb = 0; qb < nblk; ++qb)
-                            tma_load_2d(dst + qb * BM * 128, &tmap_b, (kb_first + qb) * 64,
-                                        b * BM, bar_b_full + 8 * s);
                     }
                 }
             }
@@ -512,58 +591,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         long long s0 = 0;           // CTA stage index of the current piece's first stage
         long long own = team;       // next stage of this team
         bool ok = true;
-        while (pi.next(sched, tile, kb0, kb1)) {
-            const long long s1 = s0 + (kb1 - kb0);
-            for (; own < s1; own += kTeams, w.advance(kTeams), a.advance(kTeams)) {
-                const int j = kb0 + (int)(own - s0);
-                if (ok)
-                    ok = wait_stage(bar_w_full + 8 * w.idx, w.ph, w_tag + w.idx, (uint32_t)own,
-                                    abort_flag, p.err);
-                const int nsub = ok ? stage_subs(j, kss) : 0;
-                const uint32_t sw = my_w + w.idx * kStage;
-                const uint32_t ss = my_s + w.idx * kStage;
-                const uint32_t st = my_t + a.idx * kACols;
-                for (int part = 0; part < np; ++part) {
-                    // Part `part` of the A slot is reused only once the MMAs of
-                    // the stage n_a earlier on it are done; the issuers signal
-                    // that on this team's own barrier for the part, whose phases
-                    // follow the team's stages in order, so a parity wait is never
-                    // more than one phase behind.  This wait happens even after an
-                    // error: it keeps this warp from arriving on the part's named
-                    // barrier again before the issuers have consumed the previous
-                    // arrival.
-                    if (own >= n_a) {
-                        const bool freed = warp_wait(bar_a_free + 8 * (team * np + part),
-                                                     (a_ph >> part) & 1u, &no_abort, p.err);
-                        a_ph ^= 1u << part;
-                        if (!freed) ok = false;
-                    }
-                    const int u_lo = (np == 2) ? part : 0, u_hi = (np == 2) ? part + 1 : 2;
-                    for (int uu = u_lo; uu < u_hi && uu < nsub && ok; ++uu) {
-#pragma unroll
-                        for (int g = 0; g < 2; ++g) {
-                            const uint32_t src = sw + uu * kStageWBytes + g * kSlabBytes;
-                            const uint4 lo = lds128(src);
-                            const uint4 hi = lds128(src + 2048);
-                            const uint32_t sc = lds32(ss + uu * kStageSBytes + g * 512);
-                            if (g == 1 && uu == nsub - 1) {  // every load of this stage is done
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
-                            }
-                            uint32_t v[32];
-                            if (FMT == 1)
-                                dequant_row_fp4(lo, hi, sc, v);
-                            else
-                                dequant_row(lo, hi, sc, dqc, v);
-                            tc_fence_after();
-                            tmem_st_32x32b_x32_wait(st + uu * 64 + g * 32, v);
+        for (int kind = kKind0; kind <= kKind1; ++kind) {
+            const GemmPhase &G = p.g[kind - 1];
+            const int kss = G.KSS;
+            const Sched sched = make_sched(p, G);
+            PieceIter pi;
+            pi.init(sched);
+            while (pi.next(sched, tile, kb0, kb1)) {
+                const long long s1 = s0 + (kb1 - kb0);
+                for (; own < s1; own += kTeams, w.advance(kTeams), a.advance(kTeams)) {
+                    const int j = kb0 + (int)(own - s0);
+                    if (ok)
+                        ok = wait_stage(bar_w_full + 8 * w.idx, w.ph, w_tag + w.idx,
+                                        (uint32_t)own, abort_flag, p.err);
+                    const int nsub = ok ? stage_subs(j, kss) : 0;
+                    const uint32_t sw = my_w + w.idx * kStage;
+                    const uint32_t ss = my_s + w.idx * kStage;
+                    const uint32_t st = my_t + a.idx * kACols;
+                    for (int part = 0; part < np; ++part) {
+                        // Part `part` of the A slot is reused only once the MMAs
+                        // of the stage n_a earlier on it are done; the issuers
+                        // signal that on this team's own barrier for the part,
+                        // whose phases follow the team's stages in order, so a
+                        // parity wait is never more than one phase behind.  This
+                        // wait happens even after an error: it keeps this warp
+                        // from arriving on the part's named barrier again before
+                        // the issuers have consumed the previous arrival.
+                        if (own >= n_a) {
+                            const bool freed = warp_wait(bar_a_free + 8 * (team * np + part),
+                                                         (a_ph >> part) & 1u, &no_abort, p.err);
+                            a_ph ^= 1u << part;
+                            if (!freed) ok = false;
                         }
+                        const int u_lo = (np == 2) ? part : 0, u_hi = (np == 2) ? part + 1 : 2;
+                        for (int uu = u_lo; uu < u_hi && uu < nsub && ok; ++uu) {
+#pragma unroll
+                            for (int g = 0; g < 2; ++g) {
+                                const uint32_t src = sw + uu * kStageWBytes + g * kSlabBytes;
+                                const uint4 lo = lds128(src);
+                                const uint4 hi = lds128(src + 2048);
+                                const uint32_t sc = lds32(ss + uu * kStageSBytes + g * 512);
+                                if (g == 1 && uu == nsub - 1) {  // every load of this stage is done
+                                    __syncwarp();
+                                    if (lane == 0) mbar_arrive(bar_w_empty + 8 * w.idx);
+                                }
+                                uint32_t v[32];
+                                if (FMT == 1)
+                                    dequant_row_fp4(lo, hi, sc, v);
+                                else
+                                    dequant_row(lo, hi, sc, dqc, v);
+                                tc_fence_after();
+                                tmem_st_32x32b_x32_wait(st + uu * 64 + g * 32, v);
+                            }
+                        }
+                        tc_fence_before();
+                        named_bar_arrive(kBarSlot0 + a.idx * np + part, slot_cnt);  // part written
                     }
-                    tc_fence_before();
-                    named_bar_arrive(kBarSlot0 + a.idx * np + part, slot_cnt);  // part written
                 }
+                s0 = s1;
             }
-            s0 = s1;
         }
     } else if (wid >= kFirstIssuerWarp && wid < kFirstEpilogueWarp) {
         // ------------------------------------------------------- MMA issue --
@@ -582,116 +668,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int iu_hi = (ni == 4) ? (qe >> 1) + 1 : 2;
         const uint32_t acc_off = (uint32_t)((ni == 4 ? 2 * ig + (qe >> 1) : ig) * BM);
         const uint32_t slot_cnt = (uint32_t)(kTeamWarps + part_issuers(ni, np)) * 32u;
-        const int kb_per_sub = (KIND == 1) ? 1 : 2;
         Ring a(n_a), bq(n_b);
         uint32_t next_team = (uint32_t)(n_a % kTeams);  // team of stage (CTA stage + n_a)
         uint32_t c = 0;
         bool ok = true;
-        // Wide blocks: the next piece's block entries are loaded while this
-        // piece is issued, so no piece starts with a dependent global load
-        // (measured faster for wide blocks only).
-        PieceIter pa = pi;
-        int tile_a, kb0_a, kb1_a;
-        RowsAhead ahead;
-        if (WIDE && pa.next(sched, tile_a, kb0_a, kb1_a))
-            rows_load(ahead, p.sorted_ids, (tile_a / p.RT) * BM, BM);
-        while (pi.next(sched, tile, kb0, kb1)) {
-            const int b = tile / p.RT;
-            const int pos0 = b * BM;
-            int nr;
-            if (WIDE) {
-                nr = rows_count(ahead, p.P);
-                if (pa.next(sched, tile_a, kb0_a, kb1_a))
-                    rows_load(ahead, p.sorted_ids, (tile_a / p.RT) * BM, BM);
-            } else {
-                // 16-row blocks issue 16-column MMAs whatever their row count, so
-                // they skip the dependent load of the block's entries (measured
-                // 2 % faster for the down GEMM at decode)
-                nr = (BM == 16) ? 16 : block_rows(p.sorted_ids, pos0, BM, p.P);
-            }
-            // ---- issue (every stage is visited, see the dequant role)
-            if (issuer) {
-                const uint32_t idesc = idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
-                const uint32_t buf = c % (uint32_t)nbuf;
-                const uint32_t acc_col = tmem + buf * acc_buf_cols + acc_off;
-                bool fresh = true;
-                if (ok)
-                    ok = warp_wait(bar_acc_empty + 8 * buf, ((c / nbuf) & 1) ^ 1, abort_flag,
-                                   p.err, 32);
-                for (int j = kb0; j < kb1; ++j, a.next(),
-                         next_team = (next_team + 1 == (uint32_t)kTeams) ? 0u : next_team + 1) {
-                    const int nsub = stage_subs(j, kss);
-                    const uint32_t a_st = tmem + col_a + a.idx * kACols;
-                    if (!b_sub && ok)
-                        ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
-                    for (int part = 0; part < np; ++part) {
-                        const int u_lo = (np == 2) ? (part > iu_lo ? part : iu_lo) : iu_lo;
-                        const int u_hi = (np == 2) ? (part + 1 < iu_hi ? part + 1 : iu_hi) : iu_hi;
-                        // this issuer takes part in the part's barrier if it has a
-                        // unit there (always with np = 1)
-                        if (u_lo >= u_hi) continue;
-                        named_bar_sync(kBarSlot0 + a.idx * np + part, slot_cnt);  // part in TMEM
-                        for (int uu = u_lo; uu < u_hi; ++uu) {
-                            // with one B slot per sub-stage, a missing tail sub-stage
-                            // has no B slot (the loader skips it too)
-                            const bool has_b = !b_sub || uu < nsub;
-                            if (b_sub && has_b && ok)
-                                ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
-                            const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
-                            // release the part after its last block (to the team that
-                            // uses the slot next) and the B slot after its last use
-                            const bool last_u = (uu == u_hi - 1);
-                            const uint32_t rel_a = last_u ? bar_a_free + 8 * (next_team * np + part) : 0u;
-                            const bool last_b = b_sub || (part == np - 1 && uu == u_hi - 1);
-                            for (int g = ig; g < g_hi; ++g) {
-                                const bool last_g = (g == g_hi - 1);
-                                const uint32_t sub = b_sub ? (uint32_t)g
-                                                   : (KIND == 1) ? (uint32_t)uu
-                                                                 : (uint32_t)(kb_per_sub * uu + g);
-                                const uint32_t r1 = last_g ? rel_a : 0u;
-                                const uint32_t r2 =
-                                    (last_g && last_b && has_b) ? bar_b_empty + 8 * bq.idx : 0u;
-                                if (ok && uu < nsub) {
-                                    const uint64_t bd = smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
-                                    tc_fence_after();
-                                    mma_ts_f16_k64_commit(acc_col, a_st + uu * 64 + g * 32, bd, idesc,
-                                                          fresh ? 0u : 1u, r1, r2);
-                                    fresh = false;
-                                } else {
-                                    tc_commit2_elect(r1, r2);
+        bool range_bad = false;  // a SwiGLU value saturated (helping issuers)
+        for (int kind = kKind0; kind <= kKind1; ++kind) {
+            const GemmPhase &G = p.g[kind - 1];
+            const int kss = G.KSS;
+            const int kb_per_sub = (kind == 1) ? 1 : 2;
+            const Sched sched = make_sched(p, G);
+            PieceIter pi;
+            pi.init(sched);
+            // Wide blocks: the next piece's block entries are loaded while this
+            // piece is issued, so no piece starts with a dependent global load
+            // (measured faster for wide blocks only).
+            PieceIter pa = pi;
+            int tile_a, kb0_a, kb1_a;
+            RowsAhead ahead;
+            if (WIDE && pa.next(sched, tile_a, kb0_a, kb1_a))
+                rows_load(ahead, p.sorted_ids, (tile_a / G.RT) * BM, BM);
+            while (pi.next(sched, tile, kb0, kb1)) {
+                const int b = tile / G.RT;
+                const int pos0 = b * BM;
+                int nr;
+                if (WIDE) {
+                    nr = rows_count(ahead, p.P);
+                    if (pa.next(sched, tile_a, kb0_a, kb1_a))
+                        rows_load(ahead, p.sorted_ids, (tile_a / G.RT) * BM, BM);
+                } else {
+                    // 16-row blocks issue 16-column MMAs whatever their row count,
+                    // so they skip the dependent load of the block's entries
+                    // (measured 2 % faster for the down GEMM at decode)
+                    nr = (BM == 16) ? 16 : block_rows(p.sorted_ids, pos0, BM, p.P);
+                }
+                // ---- issue (every stage is visited, see the dequant role)
+                if (issuer) {
+                    const uint32_t idesc =
+                        idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
+                    const uint32_t buf = c % (uint32_t)nbuf;
+                    const uint32_t acc_col = tmem + buf * acc_buf_cols + acc_off;
+                    bool fresh = true;
+                    if (ok)
+                        ok = warp_wait(bar_acc_empty + 8 * buf, ((c / nbuf) & 1) ^ 1, abort_flag,
+                                       p.err, 32);
+                    for (int j = kb0; j < kb1; ++j, a.next(),
+                             next_team = (next_team + 1 == (uint32_t)kTeams) ? 0u : next_team + 1) {
+                        const int nsub = stage_subs(j, kss);
+                        const uint32_t a_st = tmem + col_a + a.idx * kACols;
+                        if (!b_sub && ok)
+                            ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
+                        for (int part = 0; part < np; ++part) {
+                            const int u_lo = (np == 2) ? (part > iu_lo ? part : iu_lo) : iu_lo;
+                            const int u_hi =
+                                (np == 2) ? (part + 1 < iu_hi ? part + 1 : iu_hi) : iu_hi;
+                            // this issuer takes part in the part's barrier if it has
+                            // a unit there (always with np = 1)
+                            if (u_lo >= u_hi) continue;
+                            named_bar_sync(kBarSlot0 + a.idx * np + part, slot_cnt);  // part in TMEM
+                            for (int uu = u_lo; uu < u_hi; ++uu) {
+                                // with one B slot per sub-stage, a missing tail
+                                // sub-stage has no B slot (the loader skips it too)
+                                const bool has_b = !b_sub || uu < nsub;
+                                if (b_sub && has_b && ok)
+                                    ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag,
+                                                   p.err);
+                                const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
+                                // release the part after its last block (to the team
+                                // that uses the slot next) and the B slot after its
+                                // last use
+                                const bool last_u = (uu == u_hi - 1);
+                                const uint32_t rel_a =
+                                    last_u ? bar_a_free + 8 * (next_team * np + part) : 0u;
+                                const bool last_b = b_sub || (part == np - 1 && uu == u_hi - 1);
+                                for (int g = ig; g < g_hi; ++g) {
+                                    const bool last_g = (g == g_hi - 1);
+                                    const uint32_t sub = b_sub ? (uint32_t)g
+                                                       : (kind == 1) ? (uint32_t)uu
+                                                                     : (uint32_t)(kb_per_sub * uu + g);
+                                    const uint32_t r1 = last_g ? rel_a : 0u;
+                                    const uint32_t r2 =
+                                        (last_g && last_b && has_b) ? bar_b_empty + 8 * bq.idx : 0u;
+                                    if (ok && uu < nsub) {
+                                        const uint64_t bd =
+                                            smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128));
+                                        tc_fence_after();
+                                        mma_ts_f16_k64_commit(acc_col, a_st + uu * 64 + g * 32, bd,
+                                                              idesc, fresh ? 0u : 1u, r1, r2);
+                                        fresh = false;
+                                    } else {
+                                        tc_commit2_elect(r1, r2);
+                                    }
                                 }
+                                if (b_sub && has_b) bq.next();
                             }
-                            if (b_sub && has_b) bq.next();
                         }
+                        if (!b_sub) bq.next();
                     }
-                    if (!b_sub) bq.next();
+                    tc_commit_elect(bar_acc_full + 8 * buf);
                 }
-                tc_commit_elect(bar_acc_full + 8 * buf);
-            }
-            if (kHelp) {
-                // the upper half of a full piece's columns; every issuing warp
-                // arrives on acc_empty once per piece (full or not)
-                const uint32_t buf = c % (uint32_t)nbuf;
-                const bool got = warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag,
-                                           p.err, 32);
-                if (got) {
-                    tc_fence_after();
-                    if (kb0 == 0 && kb1 == p.KS) {
-                        const int hq = wid & 3;
-                        const int half = ((nr + 31) / 32) * 16;
-                        swiglu_store(tmem + ((uint32_t)(hq * 32) << 16) + buf * acc_buf_cols, BM,
-                                     half, nr, nr,
-                                     p.a_out + (size_t)pos0 * p.I + (tile % p.RT) * kSlabRows +
-                                         hq * 32 + lane,
-                                     p.I);
+                if (kHelp) {
+                    // the upper half of a full piece's columns; every issuing warp
+                    // arrives on acc_empty once per piece (full or not)
+                    const uint32_t buf = c % (uint32_t)nbuf;
+                    const bool got = warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag,
+                                               p.err, 32);
+                    if (got) {
+                        tc_fence_after();
+                        if (kb0 == 0 && kb1 == G.KS) {
+                            const int hq = wid & 3;
+                            const int half = ((nr + 31) / 32) * 16;
+                            swiglu_store(tmem + ((uint32_t)(hq * 32) << 16) + buf * acc_buf_cols,
+                                         BM, half, nr, nr,
+                                         p.a_out + (size_t)pos0 * p.I + (tile % G.RT) * kSlabRows +
+                                             hq * 32 + lane,
+                                         p.I, range_bad);
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
                 }
+                ++c;
             }
-            ++c;
         }
+        if (kHelp) report_range(range_bad, p.err);
         if (issuer) {  // every MMA of this CTA must finish before TMEM is released
             volatile int never = 0;
             tc_commit_elect(bar_drain);
@@ -704,201 +805,246 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = wid & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const long long T = sched.T;
         uint32_t c = 0;
         bool ok = true;
-        while (pi.next(sched, tile, kb0, kb1)) {
-            const int b = tile / p.RT, r = tile % p.RT;
-            const int pos0 = b * BM;
-            const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
-            const uint32_t buf = c % (uint32_t)nbuf;
-            if (KIND == 2) {
-                // The combine needs each column's token and routing weight: look
-                // them up once per block (these loads overlap the wait for the
-                // piece's MMAs) instead of as a dependent chain of global loads per
-                // column.  The barrier below orders these writes before the reads.
-                for (int col = row; col < nr; col += 128) {  // nr may exceed the 128 threads
-                    int pair = p.sorted_ids[pos0 + col];
-                    if (!bounds_ok(pair >= 0 && pair < p.P, p.err)) pair = 0;
-                    col_tab[col] = make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
-                }
+        bool range_bad = false;  // a SwiGLU value (or, fused, an x element) saturated
+        if (!kFused) pdl_wait();  // counters, partial slots and the accumulator (see above)
+        if (kFused) {
+            // this CTA's share of the gather: fp16 rows of x in bucketed order
+            // (the gate/up GEMM's B operand), one warp per row; published with
+            // the zeroing share by the tensor-memory owner warp
+            int npp = __ldcg(p.num_post_pad);
+            if (!bounds_ok(npp >= 0 && npp <= p.cap, p.err)) npp = 0;
+            for (int pos = blockIdx.x * 4 + q; pos < npp; pos += gridDim.x * 4) {
+                const int pair = __ldcg(p.sorted_ids + pos);
+                if (pair >= p.P) continue;  // a pad
+                if (!bounds_ok(pair >= 0, p.err)) continue;
+                gather_row<8>(p.x + (size_t)(pair / p.top_k) * p.H, p.x16 + (size_t)pos * p.H,
+                              p.H, range_bad);
             }
-            const bool u1 = !(kb1 - kb0 == 1 && stage_subs(kb0, p.KSS) == 1);
-            const bool got =
-                ok && warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag, p.err, 32);
-            // the four warps decide together (they share named barrier 1)
-            if (named_bar_or(kBarEpi, 128, !got)) ok = false;
-            if (ok) {
-                tc_fence_after();
-                const int feat = r * kSlabRows + row;
-                const uint32_t tl = tmem + lane_off + buf * acc_buf_cols;
-                if (KIND == 1) {
-                    const bool full = (kb0 == 0 && kb1 == p.KS);
-                    float *sl = nullptr;
-                    if (!full) {
-                        const long long piece_start = (long long)(tile - sched.rr) * p.KS + kb0;
-                        const int slot = (piece_start == sched.start) ? 0 : 1;
-                        sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
+            __threadfence();
+            fence_proxy_async_global();
+            named_bar_sync(kBarPrep, kPrepThreads);
+        }
+        bool zero_seen = !kFused;  // fused: every CTA's zeroing share is published
+        for (int kind = kKind0; kind <= kKind1; ++kind) {
+            const GemmPhase &G = p.g[kind - 1];
+            const Sched sched = make_sched(p, G);
+            PieceIter pi;
+            pi.init(sched);
+            const long long T = sched.T;
+            while (pi.next(sched, tile, kb0, kb1)) {
+                const int b = tile / G.RT, r = tile % G.RT;
+                const int pos0 = b * BM;
+                const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
+                const uint32_t buf = c % (uint32_t)nbuf;
+                if (kind == 2) {
+                    // The combine needs each column's token and routing weight: look
+                    // them up once per block (these loads overlap the wait for the
+                    // piece's MMAs) instead of as a dependent chain of global loads
+                    // per column.  The barrier below orders these writes before the
+                    // reads.
+                    for (int col = row; col < nr; col += 128) {  // nr may exceed the 128 threads
+                        int pair = __ldcg(p.sorted_ids + pos0 + col);
+                        if (!bounds_ok(pair >= 0 && pair < p.P, p.err)) pair = 0;
+                        col_tab[col] =
+                            make_int2(pair / p.top_k, __float_as_int(p.topk_weights[pair]));
                     }
-                    // wide: the issuing warps take columns [half, nr) of a full piece
-                    const int j_end = (kHelp && full) ? ((nr + 31) / 32) * 16 : nr;
-                    for (int j0 = 0; j0 < j_end; j0 += 16) {
-                        float gv[16], uv[16];
-                        if (ni == 4) {
-                            // accumulator of (slab g, sub-stage u) is column (2g + u) * BM
-                            tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, gv, uv);
-                            if (u1) {
-                                float g1[16], u1v[16];
-                                tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, g1,
-                                                         u1v);
+                }
+                const bool u1 = !(kb1 - kb0 == 1 && stage_subs(kb0, G.KSS) == 1);
+                bool got =
+                    ok && warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag, p.err, 32);
+                if (kind == 2 && !zero_seen && got) {
+                    // the combine adds into rows that every CTA zeroed its share of
+                    got = wait_counter(p.prep_done, (int)gridDim.x, abort_flag, p.err);
+                    zero_seen = got;
+                }
+                // the four warps decide together (they share named barrier 1)
+                if (named_bar_or(kBarEpi, 128, !got)) ok = false;
+                if (ok) {
+                    tc_fence_after();
+                    const int feat = r * kSlabRows + row;
+                    const uint32_t tl = tmem + lane_off + buf * acc_buf_cols;
+                    if (kind == 1) {
+                        const bool full = (kb0 == 0 && kb1 == G.KS);
+                        bool tile_done = full;  // this piece completes the tile's rows
+                        float *sl = nullptr;
+                        if (!full) {
+                            const long long piece_start = (long long)(tile - sched.rr) * G.KS + kb0;
+                            const int slot = (piece_start == sched.start) ? 0 : 1;
+                            sl = p.partial + ((size_t)(sched.cta * 2 + slot) * 2) * BM * 128;
+                        }
+                        // wide: the issuing warps take columns [half, nr) of a full piece
+                        const int j_end = (kHelp && full) ? ((nr + 31) / 32) * 16 : nr;
+                        for (int j0 = 0; j0 < j_end; j0 += 16) {
+                            float gv[16], uv[16];
+                            if (ni == 4) {
+                                // accumulator of (slab g, sub-stage u) is column (2g + u) * BM
+                                tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, gv, uv);
+                                if (u1) {
+                                    float g1[16], u1v[16];
+                                    tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, g1,
+                                                             u1v);
+#pragma unroll
+                                    for (int jj = 0; jj < 16; ++jj) {
+                                        gv[jj] += g1[jj];
+                                        uv[jj] += u1v[jj];
+                                    }
+                                }
+                            } else {
+                                tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
+                            }
+                            if (full) {
+                                // all 16 SwiGLU values first (independent exp and
+                                // reciprocal chains overlap; columns past nr hold
+                                // finite or garbage values that are never stored),
+                                // then the stores of the real columns
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj) gv[jj] = silu_mul(gv[jj], uv[jj]);
+                                uint16_t *dst = p.a_out + (size_t)(pos0 + j0) * p.I + feat;
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj, dst += p.I)
+                                    if (j0 + jj < nr) *dst = f16_sat(gv[jj], range_bad);
+                            } else {
 #pragma unroll
                                 for (int jj = 0; jj < 16; ++jj) {
-                                    gv[jj] += g1[jj];
-                                    uv[jj] += u1v[jj];
-                                }
-                            }
-                        } else {
-                            tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, gv, uv);
-                        }
-                        if (full) {
-                            // all 16 SwiGLU values first (independent exp and
-                            // reciprocal chains overlap; columns past nr hold
-                            // finite or garbage values that are never stored),
-                            // then the stores of the real columns
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) gv[jj] = silu_mul(gv[jj], uv[jj]);
-                            uint16_t *dst = p.a_out + (size_t)(pos0 + j0) * p.I + feat;
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj, dst += p.I)
-                                if (j0 + jj < nr) *dst = f16_sat(gv[jj]);
-                        } else {
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) {
-                                const int jr = j0 + jj;
-                                if (jr < nr) {
-                                    sl[(size_t)jr * 128 + row] = gv[jj];
-                                    sl[(size_t)(BM + jr) * 128 + row] = uv[jj];
+                                    const int jr = j0 + jj;
+                                    if (jr < nr) {
+                                        sl[(size_t)jr * 128 + row] = gv[jj];
+                                        sl[(size_t)(BM + jr) * 128 + row] = uv[jj];
+                                    }
                                 }
                             }
                         }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
-                    if (!full) {
-                        __threadfence();
-                        named_bar_sync(kBarEpi, 128);
-                        if (row == 0) {
-                            const int len = kb1 - kb0;
-                            const int old = atomicAdd(&p.tile_cnt[tile], len);
-                            *bcast = (old + len == p.KS) ? 1 : 0;
-                        }
-                        named_bar_sync(kBarEpi, 128);
-                        const bool last = *bcast != 0;
-                        named_bar_sync(kBarEpi, 128);
-                        if (last) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
+                        if (!full) {
                             __threadfence();
-                            const long long ts = (long long)(tile - sched.rr) * p.KS,
-                                            te = ts + p.KS;
-                            const int c_first = range_owner(T, sched.G, ts);
-                            const int c_last = range_owner(T, sched.G, te - 1);
-                            for (int jr = 0; jr < nr; ++jr) {
-                                float gs = 0.f, us = 0.f;
-                                for (int cc = c_first; cc <= c_last; ++cc) {
-                                    const long long cs = range_start(T, sched.G, cc);
-                                    if (range_start(T, sched.G, cc + 1) == cs) continue;  // empty
-                                    const int sslot = (cs >= ts) ? 0 : 1;
-                                    const float *ps =
-                                        p.partial + ((size_t)(cc * 2 + sslot) * 2) * BM * 128;
-                                    gs += __ldcg(ps + (size_t)jr * 128 + row);
-                                    us += __ldcg(ps + (size_t)(BM + jr) * 128 + row);
+                            named_bar_sync(kBarEpi, 128);
+                            if (row == 0) {
+                                const int len = kb1 - kb0;
+                                const int old = atomicAdd(&p.tile_cnt[tile], len);
+                                *bcast = (old + len == G.KS) ? 1 : 0;
+                            }
+                            named_bar_sync(kBarEpi, 128);
+                            const bool last = *bcast != 0;
+                            named_bar_sync(kBarEpi, 128);
+                            tile_done = last;
+                            if (last) {
+                                __threadfence();
+                                const long long ts = (long long)(tile - sched.rr) * G.KS,
+                                                te = ts + G.KS;
+                                const int c_first = range_owner(T, sched.G, ts);
+                                const int c_last = range_owner(T, sched.G, te - 1);
+                                for (int jr = 0; jr < nr; ++jr) {
+                                    float gs = 0.f, us = 0.f;
+                                    for (int cc = c_first; cc <= c_last; ++cc) {
+                                        const long long cs = range_start(T, sched.G, cc);
+                                        if (range_start(T, sched.G, cc + 1) == cs) continue;  // empty
+                                        const int sslot = (cs >= ts) ? 0 : 1;
+                                        const float *ps =
+                                            p.partial + ((size_t)(cc * 2 + sslot) * 2) * BM * 128;
+                                        gs += __ldcg(ps + (size_t)jr * 128 + row);
+                                        us += __ldcg(ps + (size_t)(BM + jr) * 128 + row);
+                                    }
+                                    p.a_out[(size_t)(pos0 + jr) * p.I + feat] =
+                                        f16_sat(silu_mul(gs, us), range_bad);
                                 }
-                                p.a_out[(size_t)(pos0 + jr) * p.I + feat] =
-                                    f16_sat(silu_mul(gs, us));
                             }
                         }
-                    }
-                } else {
-                    for (int j0 = 0; j0 < nr; j0 += 16) {
-                        float dv[16];
-                        if (ni == 1) {
-                            tmem_ld_32x32b_x16_wait(tl + j0, dv);
-                        } else if (ni == 4) {
-                            float d1[16];
-                            tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, dv, d1);
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
-                            if (u1) {
-                                float d2[16], d3[16];
-                                tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, d2,
-                                                         d3);
-#pragma unroll
-                                for (int jj = 0; jj < 16; ++jj) dv[jj] += d2[jj] + d3[jj];
-                            }
-                        } else {
-                            float d1[16];
-                            tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, dv, d1);
-#pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
+                        if (kFused && tile_done) {
+                            // the tile's intermediate rows are written: publish them to
+                            // the down B loads of block b (every thread's stores, then
+                            // one release of the block's count)
+                            __threadfence();
+                            fence_proxy_async_global();
+                            named_bar_sync(kBarEpi, 128);
+                            if (row == 0) red_release_gpu(p.blk_done + b, 1);
                         }
-                        if (b_sub || p.epi_f4) {
-                            // A lane's 16 values are one row (output feature) of 16
-                            // columns (tokens), and a scalar add per value is one
-                            // reduction request per column per warp.  Through shared
-                            // memory, each lane instead adds a float4: 4 consecutive
-                            // features of one token, a quarter of the requests.  8
-                            // columns at a time (1 KB per warp).
-                            float *stg = epi_stage + q * 256;
+                    } else {
+                        for (int j0 = 0; j0 < nr; j0 += 16) {
+                            float dv[16];
+                            if (ni == 1) {
+                                tmem_ld_32x32b_x16_wait(tl + j0, dv);
+                            } else if (ni == 4) {
+                                float d1[16];
+                                tmem_ld2_32x32b_x16_wait(tl + 0 * BM + j0, tl + 2 * BM + j0, dv, d1);
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj)
-                                dv[jj] *= __int_as_float(col_tab[j0 + jj].y);
+                                for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
+                                if (u1) {
+                                    float d2[16], d3[16];
+                                    tmem_ld2_32x32b_x16_wait(tl + 1 * BM + j0, tl + 3 * BM + j0, d2,
+                                                             d3);
 #pragma unroll
-                            for (int h = 0; h < 16; h += 8) {
-#pragma unroll
-                                for (int jj = 0; jj < 8; ++jj) stg[jj * 32 + lane] = dv[h + jj];
-                                __syncwarp();
-#pragma unroll
-                                for (int rr = 0; rr < 2; ++rr) {
-                                    const int idx = rr * 32 + lane;  // (column, 4-row group)
-                                    const int jt = idx >> 3, f4 = idx & 7;
-                                    const int jr = j0 + h + jt;
-                                    const float4 v4 =
-                                        *reinterpret_cast<const float4 *>(stg + jt * 32 + 4 * f4);
-                                    if (jr < nr)
-                                        atomicAdd(reinterpret_cast<float4 *>(
-                                                      p.out_acc + (size_t)col_tab[jr].x * p.H +
-                                                      r * kSlabRows + q * 32 + 4 * f4),
-                                                  v4);
+                                    for (int jj = 0; jj < 16; ++jj) dv[jj] += d2[jj] + d3[jj];
                                 }
-                                __syncwarp();
-                            }
-                        } else {
-                            // the 16 columns' (token, weight) entries and products
-                            // first, then the reductions of the real columns (the
-                            // table has 256 entries, so j0 + 15 is in bounds)
-                            int tok[16];
+                            } else {
+                                float d1[16];
+                                tmem_ld2_32x32b_x16_wait(tl + j0, tl + BM + j0, dv, d1);
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) {
-                                const int2 tw = col_tab[j0 + jj];
-                                tok[jj] = tw.x;
-                                dv[jj] *= __int_as_float(tw.y);
+                                for (int jj = 0; jj < 16; ++jj) dv[jj] += d1[jj];
                             }
+                            if (b_sub || p.epi_f4) {
+                                // A lane's 16 values are one row (output feature) of 16
+                                // columns (tokens), and a scalar add per value is one
+                                // reduction request per column per warp.  Through shared
+                                // memory, each lane instead adds a float4: 4 consecutive
+                                // features of one token, a quarter of the requests.  8
+                                // columns at a time (1 KB per warp).
+                                float *stg = epi_stage + q * 256;
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj)
-                                if (j0 + jj < nr)
-                                    atomicAdd(p.out_acc + (size_t)tok[jj] * p.H + feat, dv[jj]);
+                                for (int jj = 0; jj < 16; ++jj)
+                                    dv[jj] *= __int_as_float(col_tab[j0 + jj].y);
+#pragma unroll
+                                for (int h = 0; h < 16; h += 8) {
+#pragma unroll
+                                    for (int jj = 0; jj < 8; ++jj) stg[jj * 32 + lane] = dv[h + jj];
+                                    __syncwarp();
+#pragma unroll
+                                    for (int rr = 0; rr < 2; ++rr) {
+                                        const int idx = rr * 32 + lane;  // (column, 4-row group)
+                                        const int jt = idx >> 3, f4 = idx & 7;
+                                        const int jr = j0 + h + jt;
+                                        const float4 v4 =
+                                            *reinterpret_cast<const float4 *>(stg + jt * 32 + 4 * f4);
+                                        if (jr < nr)
+                                            atomicAdd(reinterpret_cast<float4 *>(
+                                                          p.out_acc + (size_t)col_tab[jr].x * p.H +
+                                                          r * kSlabRows + q * 32 + 4 * f4),
+                                                      v4);
+                                    }
+                                    __syncwarp();
+                                }
+                            } else {
+                                // the 16 columns' (token, weight) entries and products
+                                // first, then the reductions of the real columns (the
+                                // table has 256 entries, so j0 + 15 is in bounds)
+                                int tok[16];
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj) {
+                                    const int2 tw = col_tab[j0 + jj];
+                                    tok[jj] = tw.x;
+                                    dv[jj] *= __int_as_float(tw.y);
+                                }
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj)
+                                    if (j0 + jj < nr)
+                                        atomicAdd(p.out_acc + (size_t)tok[jj] * p.H + feat, dv[jj]);
+                            }
                         }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
+                        // every warp is done with the column table before any warp
+                        // writes the next block's
+                        named_bar_sync(kBarEpi, 128);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
-                    // every warp is done with the column table before any warp
-                    // writes the next block's
-                    named_bar_sync(kBarEpi, 128);
                 }
+                ++c;
             }
-            ++c;
         }
+        report_range(range_bad, p.err);
     }
 
     __syncthreads();
@@ -917,11 +1063,13 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
     p.dq.cm72 = 0xD480D480u;   // fp16 -72
     const int BM = p.block_m;
     if (BM < 16 || BM % 16 != 0 || BM > 192) return false;
+    if (kind == 3 && BM > 128) return false;  // the fused kernel runs narrow blocks
     p.np = 1;
     p.b_sub = 0;
     int n_b;
     if (BM <= 128) {
-        // k blocks per B stage: gate/up two 64-wide blocks, down four
+        // k blocks per B stage: gate/up two 64-wide blocks, down four (the fused
+        // kernel's slots are sized for down)
         p.b_stage_bytes = (uint32_t)((kind == 1 ? 2 : 4) * BM * 128);
         // MMA issuers (one accumulator each), accumulator buffers and the A
         // stages that tensor memory then leaves, in order of preference: more A
@@ -944,7 +1092,7 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
         if (p.n_a > kTeams) p.n_a = kTeams;  // a team's A-slot barrier stays within one phase
         if (p.n_a < 2) return false;
         n_b = (BM <= 32) ? 8 : (BM <= 64) ? 4 : 3;
-        if (kind == 2 && BM > 32) n_b = (BM <= 64) ? 3 : 2;  // down stages carry four k blocks
+        if (kind != 1 && BM > 32) n_b = (BM <= 64) ? 3 : 2;  // down stages carry four k blocks
     } else {
         // Wide blocks (up to 192 tokens: one pass over an expert's weights where
         // 128-token blocks would need two).  One A stage, released per sub-stage
@@ -980,7 +1128,7 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
         const int n = (int)((limit - b_bytes - misc_bytes) / kStage);
         return n > 10 ? 10 : n;
     };
-    p.epi_f4 = (kind == 2 && (p.b_sub || ring(misc0 + stage_bytes) == ring(misc0))) ? 1 : 0;
+    p.epi_f4 = (kind != 1 && (p.b_sub || ring(misc0 + stage_bytes) == ring(misc0))) ? 1 : 0;
     const uint32_t misc = misc0 + (p.epi_f4 ? stage_bytes : 0u);
     const int n_w = ring(misc);
     if (n_w < 3) return false;
@@ -992,30 +1140,41 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
     return p.smem_bytes <= 227u * 1024u;
 }
 
-cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_b, int grid,
-                        cudaStream_t s, int *launches) {
+cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_x,
+                        const CUtensorMap *tmap_a, int grid, cudaStream_t s, int *launches) {
     const int wide = (p.np == 2 || p.b_sub) ? 1 : 0;
     const int fmt = (p.fmt == 1) ? 1 : 0;  // MOE_W_MXFP4
-    const int v = (fmt * 2 + (kind - 1)) * 2 + wide;  // instantiation index
-    static bool attr_done[64][8] = {};
+    if (kind < 1 || kind > 3 || (kind == 3 && wide)) return cudaErrorInvalidValue;
+    const int v = (fmt * 3 + (kind - 1)) * 2 + wide;  // instantiation index
+    static std::mutex mu;
+    static bool attr_done[64][12] = {};
     int dev = 0;
-    cudaGetDevice(&dev);
-    typedef void (*KernelFn)(const GemmParams, const CUtensorMap);
-    const KernelFn fns[8] = {moe_gemm_kernel<1, 0, 0>, moe_gemm_kernel<1, 1, 0>,
-                             moe_gemm_kernel<2, 0, 0>, moe_gemm_kernel<2, 1, 0>,
-                             moe_gemm_kernel<1, 0, 1>, moe_gemm_kernel<1, 1, 1>,
-                             moe_gemm_kernel<2, 0, 1>, moe_gemm_kernel<2, 1, 1>};
-    if (dev >= 0 && dev < 64 && !attr_done[dev][v]) {
-        cudaError_t e = cudaFuncSetAttribute(fns[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_done[dev][v] = true;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    typedef void (*KernelFn)(const GemmParams, const CUtensorMap, const CUtensorMap);
+    const KernelFn fns[12] = {moe_gemm_kernel<1, 0, 0>, moe_gemm_kernel<1, 1, 0>,
+                              moe_gemm_kernel<2, 0, 0>, moe_gemm_kernel<2, 1, 0>,
+                              moe_gemm_kernel<3, 0, 0>, nullptr,
+                              moe_gemm_kernel<1, 0, 1>, moe_gemm_kernel<1, 1, 1>,
+                              moe_gemm_kernel<2, 0, 1>, moe_gemm_kernel<2, 1, 1>,
+                              moe_gemm_kernel<3, 0, 1>, nullptr};
+    {
+        // once per device and instantiation, under a lock (concurrent first
+        // calls); a failure is returned and not recorded as done
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_done[dev][v]) {
+            e = cudaFuncSetAttribute(fns[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     227 * 1024);
+            if (e != cudaSuccess) return e;
+            attr_done[dev][v] = true;
+        }
     }
     cudaLaunchConfig_t cfg = pdl_config((unsigned)grid, kThreads, p.smem_bytes, s);
     cudaLaunchAttribute attr;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl_attr(attr);
-    cudaLaunchKernelEx(&cfg, fns[v], p, *tmap_b);
+    cudaLaunchKernelEx(&cfg, fns[v], p, *tmap_x, *tmap_a);
     if (launches) *launches += 1;
     return cudaGetLastError();
 }

@@ -66,7 +66,8 @@ cudaError_t launch_gather_rows(const uint16_t *x, const int32_t *sorted, const i
 cudaError_t launch_finalize(const float *acc, uint16_t *out, size_t n, int sms, cudaStream_t s,
                             int *launches);
 cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
-                        int is_w13, void *packed, void *packed_scales, cudaStream_t s);
+                        int is_w13, void *packed, void *packed_scales, uint32_t *inexact,
+                        cudaStream_t s);
 cudaError_t launch_pack_mxfp4(const uint8_t *q, const uint8_t *scales, int E, int N, int K,
                               int is_w13, void *packed, void *packed_scales, uint32_t *bad,
                               cudaStream_t s);
@@ -89,9 +90,17 @@ struct DequantConsts {
     uint32_t c16th, cm72;       // fp16 pairs 1/16 and -72 (high nibble: x/16 - 72)
 };
 
-struct GemmParams {
+// One of the two grouped GEMMs: g[0] the gate/up GEMM, g[1] the down GEMM.
+struct GemmPhase {
     const uint8_t *wq;         // packed INT4 stages
     const uint8_t *wsc;        // packed scales
+    int RT;                    // row tiles per expert
+    int KSS, KS;               // k sub-stages per tile (one 8 KB packed stage each) and
+                               // pipeline stages per tile (two sub-stages, the last maybe one)
+};
+
+struct GemmParams {
+    GemmPhase g[2];            // the kernel runs g[kind - 1] (the fused kernel both, in turn)
     const int32_t *sorted_ids; // align output
     const int32_t *expert_ids;
     const int32_t *num_post_pad;
@@ -103,12 +112,14 @@ struct GemmParams {
     float4 *zero_out;          // gate/up: zeroes these zero_n16 16-byte units (the down
     size_t zero_n16;           // GEMM's accumulator) on the side; null: nothing
     uint32_t *err;             // [2]
+    // fused kernel only: the gather of x and the hand-offs between CTAs
+    const uint16_t *x;         // bf16 [M][H]
+    uint16_t *x16;             // fp16 rows of x in bucketed order [cap][H]
+    int32_t *blk_done;         // [blocks]: gate/up tiles finished, per expert block
+    int32_t *prep_done;        // [1]: CTAs done with their share of the gather and zeroing
     int M, top_k, H, I, P, E;
     int cap;                   // rows of sorted_ids, of the gathered x and of a_out
     int block_m;               // BM: routing block height (multiple of 16, <= 192)
-    int RT;                    // row tiles per expert
-    int KSS, KS;               // k sub-stages per tile (one 8 KB packed stage each) and
-                               // pipeline stages per tile (two sub-stages, the last maybe one)
     int n_w, n_b, n_a;         // ring depths: weight stages, B stages, A (TMEM) stages
     int ni;                    // MMA-issuing warps (= accumulators per buffer): 4 or 2
     int nbuf;                  // accumulator buffers (pieces alternate between them)
@@ -123,11 +134,13 @@ struct GemmParams {
     DequantConsts dq;
 };
 
-// kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine.  tmap_b
-// maps the B operand rows in bucketed order: fp16 x (gate/up) or the fp16
-// intermediate (down), 64-column x block_m-row boxes, 128-byte swizzle.
-cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_b, int grid,
-                        cudaStream_t s, int *launches);
+// kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine; kind 3:
+// both in one persistent launch (the fused decode kernel: gather, gate/up, then
+// down, blocks of at most 128 rows).  The tensor maps cover the B operand rows in
+// bucketed order, 64-column x block_m-row boxes, 128-byte swizzle: tmap_x the fp16
+// x rows (gate/up), tmap_a the fp16 intermediate (down); a kind uses its own.
+cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_x,
+                        const CUtensorMap *tmap_a, int grid, cudaStream_t s, int *launches);
 // Fills the ring depths and shared-memory layout of p for the given kind.
 bool plan_gemm_smem(int kind, GemmParams &p);
 

@@ -30,7 +30,10 @@ std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of g_align_chunk_tab on the current device, looked up once per
-// device (the first call on each device does this set-up).
+// device (the first call on each device that needs the table does this
+// set-up).  The cached address belongs to the device's primary context: after
+// cudaDeviceReset it is stale, so a process that resets a device does not call
+// moe_align_noalloc with a table-sized routing on it again.
 int noalloc_scratch(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -57,6 +60,9 @@ int moe_align_noalloc(const int32_t *topk_ids, int M, int top_k, int E, int bloc
     if ((long long)M * top_k > (1LL << 30)) return MOE_ERR_SHAPE;
     const size_t need = moe_align_scratch_bytes(M, top_k, E);
     if (need > kNoAllocScratchBytes) return MOE_ERR_NOALLOC_LIMIT;
+    if (need == 0)  // single-block align: no table, no device set-up
+        return moe_align(topk_ids, M, top_k, E, block_m, sorted_ids, expert_ids, num_post_pad,
+                         err_flags, nullptr, 0, stream);
     void *scratch = nullptr;
     const int rc = noalloc_scratch(&scratch);
     if (rc != MOE_OK) return rc;

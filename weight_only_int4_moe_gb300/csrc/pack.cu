@@ -53,9 +53,14 @@ __global__ void pack_weights_kernel(const uint8_t *__restrict__ q, uint32_t *__r
 }
 
 // bf16 scale -> fp16 (exact for magnitudes in [2^-14, 65504]; saturating above,
-// fp16 subnormals below).
-__device__ __forceinline__ uint16_t bf16_bits_to_f16_sat(uint16_t b) {
+// fp16 subnormals below).  A non-zero scale outside [2^-14, 8188] in magnitude
+// (or not finite) is counted in *inexact: there, a dequantised weight
+// (q - 8) * scale is not exact in fp16 (8 * 8188 < 65504 and, from 2^-14 up, a
+// bf16 scale's 8 significant bits times |q - 8| <= 8 fit in fp16's 11).
+__device__ __forceinline__ uint16_t bf16_bits_to_f16_sat(uint16_t b, uint32_t *inexact) {
     float v = __uint_as_float((uint32_t)b << 16);
+    const float m = fabsf(v);
+    if (inexact && v != 0.0f && !(m >= 0x1p-14f && m <= 8188.0f)) atomicAdd(inexact, 1u);
     v = fminf(fmaxf(v, -65504.0f), 65504.0f);
     return __half_as_ushort(__float2half_rn(v));
 }
@@ -76,7 +81,8 @@ __device__ __forceinline__ uint16_t e8m0_to_f16_factor(uint8_t e, uint32_t *bad)
 
 struct Bf16Scale {
     using T = uint16_t;
-    __device__ uint16_t operator()(uint16_t b) const { return bf16_bits_to_f16_sat(b); }
+    uint32_t *inexact;
+    __device__ uint16_t operator()(uint16_t b) const { return bf16_bits_to_f16_sat(b, inexact); }
 };
 struct E8m0Scale {
     using T = uint8_t;
@@ -133,8 +139,10 @@ cudaError_t launch_pack_impl(const uint8_t *q, const typename Conv::T *scales, C
 }
 
 cudaError_t launch_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
-                        int is_w13, void *packed, void *packed_scales, cudaStream_t s) {
-    return launch_pack_impl(q, scales, Bf16Scale{}, E, N, K, is_w13, packed, packed_scales, s);
+                        int is_w13, void *packed, void *packed_scales, uint32_t *inexact,
+                        cudaStream_t s) {
+    return launch_pack_impl(q, scales, Bf16Scale{inexact}, E, N, K, is_w13, packed,
+                            packed_scales, s);
 }
 
 cudaError_t launch_pack_mxfp4(const uint8_t *q, const uint8_t *scales, int E, int N, int K,

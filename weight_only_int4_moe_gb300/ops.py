@@ -23,13 +23,16 @@ MOE_OUT_F32 = 1
 MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_TIMEOUT = 0x2
 MOE_DEVERR_BOUNDS = 0x4  # debug-bounds builds only
+MOE_DEVERR_RANGE = 0x8
 MOE_W_INT4 = 0
 MOE_W_MXFP4 = 1
+MOE_FLAG_UNFUSED = 0x1
 
 EXPORTED = [
     "moe_int4_packed_bytes", "moe_int4_packed_scale_bytes", "moe_int4_pack", "moe_mxfp4_pack",
     "moe_align_capacity", "moe_align_scratch_bytes", "moe_align",
-    "moe_int4_workspace_bytes", "moe_int4_block_m", "moe_int4_workspace_layout",
+    "moe_int4_workspace_bytes", "moe_int4_block_m", "moe_int4_fused",
+    "moe_int4_workspace_layout",
     "moe_int4_forward",
     "moe_int4_forward_host", "moe_int4_get_errors", "moe_int4_clear_errors",
     "moe_int4_strerror", "moe_int4_profile_enable", "moe_int4_profile_read",
@@ -40,11 +43,12 @@ EXPORTED = [
 class Shape(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("inter", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("weight_format", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("weight_format", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
 
     @classmethod
-    def of(cls, E, top_k, hidden, inter, out_dtype=MOE_OUT_F32, weight_format=0):
-        return cls(E, top_k, hidden, inter, 32, out_dtype, weight_format)
+    def of(cls, E, top_k, hidden, inter, out_dtype=MOE_OUT_F32, weight_format=0, flags=0):
+        return cls(E, top_k, hidden, inter, 32, out_dtype, weight_format, flags)
 
     @property
     def torch_out_dtype(self):
@@ -80,12 +84,13 @@ def load_library(build_if_missing: bool = True):
         sig = {
             "moe_int4_packed_bytes": ([i, i, i], sz),
             "moe_int4_packed_scale_bytes": ([i, i, i], sz),
-            "moe_int4_pack": ([p, p, i, i, i, i, p, p, p], i),
+            "moe_int4_pack": ([p, p, i, i, i, i, p, p, p, p], i),
             "moe_mxfp4_pack": ([p, p, i, i, i, i, p, p, p, p], i),
             "moe_align_capacity": ([i, i, i, i], sz),
             "moe_align_scratch_bytes": ([i, i, i], sz),
             "moe_align": ([p, i, i, i, i, p, p, p, p, p, sz, p], i),
             "moe_int4_workspace_bytes": ([i, sp, i], sz),
+            "moe_int4_fused": ([i, sp], i),
             "moe_int4_block_m": ([i, sp], i),
             "moe_int4_workspace_layout": ([i, sp, p], i),
             "moe_int4_forward": ([p] * 8 + [i, sp, p, sz, p], i),
@@ -128,6 +133,16 @@ def _dptr(t: torch.Tensor) -> int:
     return t.data_ptr()
 
 
+def _on(*tensors):
+    """Context in which a library call runs: the device that holds the call's
+    device tensors, made current (the library launches on the current device
+    and the current stream belongs to it).  All of them must be on one device."""
+    devs = {t.device for t in tensors if isinstance(t, torch.Tensor) and t.is_cuda}
+    if len(devs) != 1:
+        raise ValueError(f"expected the tensors on one CUDA device, got {sorted(map(str, devs))}")
+    return torch.cuda.device(devs.pop())
+
+
 def _u16(t: torch.Tensor) -> torch.Tensor:
     """bf16 tensors are passed by bit pattern."""
     if t.dtype == torch.bfloat16:
@@ -146,17 +161,22 @@ def moe_int4_packed_scale_bytes(E: int, N: int, K: int) -> int:
     return load_library().moe_int4_packed_scale_bytes(E, N, K)
 
 
-def moe_int4_pack(q: torch.Tensor, scales: torch.Tensor, is_w13: bool, stream=None):
+def moe_int4_pack(q: torch.Tensor, scales: torch.Tensor, is_w13: bool, stream=None,
+                  inexact: torch.Tensor | None = None):
     """Canonical INT4 (uint8 [E, N, K/2]) + bf16 scales [E, N, K/32] -> packed
-    (uint8) and packed scales (uint8) device tensors."""
+    (uint8) and packed scales (uint8) device tensors.  ``inexact`` (optional
+    device int32 [1]) counts the scales whose dequantised weights are not exact
+    in fp16 (non-zero magnitudes outside [2^-14, 8188])."""
     lib = load_library()
     E, N, K2 = q.shape
     K = 2 * K2
     packed = torch.empty(lib.moe_int4_packed_bytes(E, N, K), dtype=torch.uint8, device=q.device)
     pscales = torch.empty(lib.moe_int4_packed_scale_bytes(E, N, K), dtype=torch.uint8,
                           device=q.device)
-    rc = lib.moe_int4_pack(_dptr(q), _dptr(_u16(scales)), E, N, K, int(bool(is_w13)),
-                           _dptr(packed), _dptr(pscales), _stream(stream))
+    with _on(q, scales, packed, pscales, inexact):
+        rc = lib.moe_int4_pack(_dptr(q), _dptr(_u16(scales)), E, N, K, int(bool(is_w13)),
+                               _dptr(packed), _dptr(pscales),
+                               None if inexact is None else _dptr(inexact), _stream(stream))
     _check(rc, "moe_int4_pack")
     return packed, pscales
 
@@ -172,8 +192,10 @@ def moe_mxfp4_pack(q: torch.Tensor, scales: torch.Tensor, is_w13: bool, stream=N
     pscales = torch.empty(lib.moe_int4_packed_scale_bytes(E, N, K), dtype=torch.uint8,
                           device=q.device)
     bad = torch.zeros(1, dtype=torch.int32, device=q.device)
-    rc = lib.moe_mxfp4_pack(_dptr(q), _dptr(scales.contiguous()), E, N, K, int(bool(is_w13)),
-                            _dptr(packed), _dptr(pscales), _dptr(bad), _stream(stream))
+    with _on(q, scales, packed, pscales, bad):
+        rc = lib.moe_mxfp4_pack(_dptr(q), _dptr(scales.contiguous()), E, N, K,
+                                int(bool(is_w13)), _dptr(packed), _dptr(pscales), _dptr(bad),
+                                _stream(stream))
     _check(rc, "moe_mxfp4_pack")
     return packed, pscales, bad
 
@@ -200,8 +222,10 @@ def moe_align(topk_ids: torch.Tensor, E: int, block_m: int, stream=None):
     err = torch.zeros(2, dtype=torch.int32, device=dev)
     scratch_bytes = lib.moe_align_scratch_bytes(M, k, E)
     scratch = torch.empty(max(scratch_bytes, 16), dtype=torch.uint8, device=dev)
-    rc = lib.moe_align(_dptr(topk_ids), M, k, E, block_m, _dptr(sorted_ids), _dptr(expert_ids),
-                       _dptr(npp), _dptr(err), _dptr(scratch), scratch_bytes, _stream(stream))
+    with _on(topk_ids, sorted_ids, expert_ids, npp, err, scratch):
+        rc = lib.moe_align(_dptr(topk_ids), M, k, E, block_m, _dptr(sorted_ids),
+                           _dptr(expert_ids), _dptr(npp), _dptr(err), _dptr(scratch),
+                           scratch_bytes, _stream(stream))
     _check(rc, "moe_align")
     return sorted_ids, expert_ids, npp, err
 
@@ -221,8 +245,10 @@ def moe_align_noalloc(topk_ids: torch.Tensor, E: int, block_m: int, out=None, st
                torch.zeros(1, dtype=torch.int32, device=dev),
                torch.zeros(2, dtype=torch.int32, device=dev))
     sorted_ids, expert_ids, npp, err = out
-    rc = lib.moe_align_noalloc(_dptr(topk_ids), M, k, E, block_m, _dptr(sorted_ids),
-                               _dptr(expert_ids), _dptr(npp), _dptr(err), _stream(stream))
+    # the library looks up its table on the current device: make it the ids'
+    with _on(topk_ids, sorted_ids, expert_ids, npp, err):
+        rc = lib.moe_align_noalloc(_dptr(topk_ids), M, k, E, block_m, _dptr(sorted_ids),
+                                   _dptr(expert_ids), _dptr(npp), _dptr(err), _stream(stream))
     _check(rc, "moe_align_noalloc")
     return sorted_ids, expert_ids, npp, err
 
@@ -230,6 +256,12 @@ def moe_align_noalloc(topk_ids: torch.Tensor, E: int, block_m: int, out=None, st
 # ----------------------------------------------------------------- forward --
 def moe_int4_workspace_bytes(M: int, shape: Shape, flags: int = 0) -> int:
     return load_library().moe_int4_workspace_bytes(M, ctypes.byref(shape), flags)
+
+
+def moe_int4_fused(M: int, shape: Shape) -> bool:
+    """Whether a forward of M tokens runs the fused decode kernel (the gather
+    and both GEMMs in one launch)."""
+    return load_library().moe_int4_fused(M, ctypes.byref(shape)) == 1
 
 
 def moe_int4_block_m(M: int, shape: Shape) -> int:
@@ -245,8 +277,12 @@ def moe_int4_workspace_layout(M: int, shape: Shape) -> dict:
 
 
 def alloc_workspace(M: int, shape: Shape, flags: int = 0, device="cuda") -> torch.Tensor:
+    """A workspace for forwards of up to M tokens, its error words cleared
+    (they accumulate over calls until moe_int4_clear_errors)."""
     n = moe_int4_workspace_bytes(M, shape, flags)
-    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
 
 
 def moe_int4_forward(x, w13_packed, w13_scales, w2_packed, w2_scales, topk_ids, topk_weights,
@@ -260,10 +296,12 @@ def moe_int4_forward(x, w13_packed, w13_scales, w2_packed, w2_scales, topk_ids, 
         raise TypeError(f"out must be {shape.torch_out_dtype}")
     if workspace is None:
         workspace = alloc_workspace(M, shape, device=x.device)
-    rc = lib.moe_int4_forward(
-        _dptr(_u16(x)), _dptr(w13_packed), _dptr(w13_scales), _dptr(w2_packed),
-        _dptr(w2_scales), _dptr(topk_ids), _dptr(topk_weights), _dptr(out), M,
-        ctypes.byref(shape), _dptr(workspace), workspace.numel(), _stream(stream))
+    with _on(x, w13_packed, w13_scales, w2_packed, w2_scales, topk_ids, topk_weights, out,
+             workspace):
+        rc = lib.moe_int4_forward(
+            _dptr(_u16(x)), _dptr(w13_packed), _dptr(w13_scales), _dptr(w2_packed),
+            _dptr(w2_scales), _dptr(topk_ids), _dptr(topk_weights), _dptr(out), M,
+            ctypes.byref(shape), _dptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "moe_int4_forward")
     return out
 
@@ -274,8 +312,9 @@ def moe_route(router_logits: torch.Tensor, top_k: int, stream=None):
     dev = router_logits.device
     ids = torch.empty((M, top_k), dtype=torch.int32, device=dev)
     w = torch.empty((M, top_k), dtype=torch.float32, device=dev)
-    _check(load_library().moe_route(_dptr(router_logits), M, E, top_k, _dptr(ids), _dptr(w),
-                                    _stream(stream)), "moe_route")
+    with _on(router_logits, ids, w):
+        _check(load_library().moe_route(_dptr(router_logits), M, E, top_k, _dptr(ids), _dptr(w),
+                                        _stream(stream)), "moe_route")
     return ids, w
 
 
@@ -294,10 +333,12 @@ def moe_int4_forward_routed(x, w13, w13_scales, w2, w2_scales, router_logits, sh
         topk_weights = torch.empty((M, shape.top_k), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = alloc_workspace(M, shape, device=dev)
-    rc = load_library().moe_int4_forward_routed(
-        _dptr(x), _dptr(w13), _dptr(w13_scales), _dptr(w2), _dptr(w2_scales),
-        _dptr(router_logits), _dptr(topk_ids), _dptr(topk_weights), _dptr(out), M,
-        ctypes.byref(shape), _dptr(workspace), workspace.numel(), _stream(stream))
+    with _on(x, w13, w13_scales, w2, w2_scales, router_logits, topk_ids, topk_weights, out,
+             workspace):
+        rc = load_library().moe_int4_forward_routed(
+            _dptr(x), _dptr(w13), _dptr(w13_scales), _dptr(w2), _dptr(w2_scales),
+            _dptr(router_logits), _dptr(topk_ids), _dptr(topk_weights), _dptr(out), M,
+            ctypes.byref(shape), _dptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "moe_int4_forward_routed")
     return out, topk_ids, topk_weights
 
@@ -311,11 +352,12 @@ def moe_int4_forward_host(x_host, w13_packed, w13_scales, w2_packed, w2_scales, 
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("host tensors must be contiguous CPU tensors")
     M = x_host.shape[0]
-    rc = lib.moe_int4_forward_host(
-        _u16(x_host).data_ptr(), _dptr(w13_packed), _dptr(w13_scales), _dptr(w2_packed),
-        _dptr(w2_scales), ids_host.data_ptr(), weights_host.data_ptr(),
-        out_host.data_ptr(), M, ctypes.byref(shape), _dptr(workspace), workspace.numel(),
-        _stream(stream))
+    with _on(w13_packed, w13_scales, w2_packed, w2_scales, workspace):
+        rc = lib.moe_int4_forward_host(
+            _u16(x_host).data_ptr(), _dptr(w13_packed), _dptr(w13_scales), _dptr(w2_packed),
+            _dptr(w2_scales), ids_host.data_ptr(), weights_host.data_ptr(),
+            out_host.data_ptr(), M, ctypes.byref(shape), _dptr(workspace), workspace.numel(),
+            _stream(stream))
     _check(rc, "moe_int4_forward_host")
     return out_host
 
@@ -324,15 +366,17 @@ def moe_int4_get_errors(workspace, stream=None):
     lib = load_library()
     flags = ctypes.c_uint32(0)
     count = ctypes.c_uint32(0)
-    rc = lib.moe_int4_get_errors(_dptr(workspace), ctypes.byref(flags), ctypes.byref(count),
-                                 _stream(stream))
+    with _on(workspace):
+        rc = lib.moe_int4_get_errors(_dptr(workspace), ctypes.byref(flags), ctypes.byref(count),
+                                     _stream(stream))
     _check(rc, "moe_int4_get_errors")
     return flags.value, count.value
 
 
 def moe_int4_clear_errors(workspace, stream=None):
-    _check(load_library().moe_int4_clear_errors(_dptr(workspace), _stream(stream)),
-           "moe_int4_clear_errors")
+    with _on(workspace):
+        _check(load_library().moe_int4_clear_errors(_dptr(workspace), _stream(stream)),
+               "moe_int4_clear_errors")
 
 
 def moe_int4_strerror(code: int) -> str:
@@ -376,13 +420,18 @@ class PackedWeights:
                 bad.append(nbad)
                 return packed, pscales
             sc = torch.from_numpy(np.ascontiguousarray(s_np).view(np.int16)).to(device)
-            return moe_int4_pack(q, sc, is_w13)
+            cnt = torch.zeros(1, dtype=torch.int32, device=device)
+            bad.append(cnt)
+            return moe_int4_pack(q, sc, is_w13, inexact=cnt)
 
         self.w13, self.w13_scales = pack(w["q13"], w["s13"], True)
         self.w2, self.w2_scales = pack(w["q2"], w["s2"], False)
         torch.cuda.synchronize()
         n_bad = sum(int(t.item()) for t in bad)
-        if n_bad:
+        # INT4: scales whose dequantised weights are not exact in fp16 (the
+        # forward still runs; see moe_int4_pack)
+        self.inexact_scales = 0 if mx else n_bad
+        if mx and n_bad:
             raise ValueError(f"{n_bad} E8M0 scales outside the supported range [89, 128]")
 
     def forward(self, x, topk_ids, topk_weights, out=None, workspace=None, stream=None):
