@@ -303,24 +303,27 @@ def run_reference(args, cfg, Ms, world, rank):
 
 # --------------------------------------------------------------- GPU arm --
 def roofline_of(recs, w13_b, w2_b, top_k, H, I, hbm_peak, tc_peak, peak_src, workload):
-    """Roofline position of the dominant kernel over profiled calls: the fused
-    decode kernel where the forward ran it (both GEMMs in one launch), else the
-    GEMM with the larger share of the per-kernel event time.  Algorithmic bytes
-    (touched experts x packed weights + scales) or FLOPs (2 x pairs x the
-    GEMM's weights) per launch over its CUDA-event duration, whichever bound is
-    the slower at the peaks."""
-    g1_ms = [r["stages"][1] for r in recs]
-    g2_ms = [r["stages"][2] for r in recs]
-    if all(r["fused"] for r in recs):
-        dominant, k_ms = "fused", g1_ms
-        k_bytes = [r["touched"] * (w13_b + w2_b) for r in recs]
-        k_flops = [2.0 * r["M"] * top_k * H * I * 3 for r in recs]
-    else:
-        dominant = "gate_up" if sum(g1_ms) >= sum(g2_ms) else "down"
-        k_ms = g1_ms if dominant == "gate_up" else g2_ms
-        k_bytes = [r["touched"] * (w13_b if dominant == "gate_up" else w2_b) for r in recs]
-        k_flops = [2.0 * r["M"] * top_k * H * I * (2 if dominant == "gate_up" else 1)
-                   for r in recs]
+    """Roofline position of the dominant kernel over profiled calls: of the fused
+    decode kernel (both GEMMs in one launch, where the forward ran it), the
+    gate/up GEMM and the down GEMM (where it ran them separately), the one with
+    the largest share of the per-kernel event time, over the calls that ran it.
+    Algorithmic bytes (touched experts x packed weights + scales) or FLOPs
+    (2 x pairs x the kernel's weights) per launch over its CUDA-event duration,
+    whichever bound is the slower at the peaks."""
+    mult = {"fused": 3, "gate_up": 2, "down": 1}
+    wbytes = {"fused": w13_b + w2_b, "gate_up": w13_b, "down": w2_b}
+
+    def launches(kernel):  # (ms, record) of every launch of the kernel
+        if kernel == "fused":
+            return [(r["stages"][1], r) for r in recs if r["fused"]]
+        col = 1 if kernel == "gate_up" else 2
+        return [(r["stages"][col], r) for r in recs if not r["fused"]]
+
+    dominant = max(mult, key=lambda k: sum(ms for ms, _ in launches(k)))
+    lr = launches(dominant)
+    k_ms = [ms for ms, _ in lr]
+    k_bytes = [r["touched"] * wbytes[dominant] for _, r in lr]
+    k_flops = [2.0 * r["M"] * top_k * H * I * mult[dominant] for _, r in lr]
     t_hbm = sum(k_bytes) / (hbm_peak * 1e9)
     t_tc = sum(k_flops) / (tc_peak * 1e12)
     bytes_mean = statistics.mean(k_bytes)

@@ -17,9 +17,10 @@
  * INT4, group size 32).  Activations are bf16 and the output bf16 or fp32.  The
  * tensor cores multiply fp16 operands with fp32 accumulation: each dequantised
  * weight (q - 8) * scale is formed in fp16 with one rounding (11 significant
- * bits, where bf16 would keep 8; it is exact for scales in [2^-14, 8188], since
- * a bf16 scale's 8 significant bits times |q - 8| <= 8 fit in 11, and
- * moe_int4_pack counts the scales outside that range), x is converted to fp16
+ * bits, where bf16 would keep 8; it is exact for scales in [2^-14, 2729], since
+ * a bf16 scale's 8 significant bits times |q - 8| <= 8 fit in 11 and the
+ * kernels' addend -24 * scale stays in range, and moe_int4_pack counts the
+ * scales outside that range), x is converted to fp16
  * (exact for |x| in [2^-14, 65504]; below, fp16 subnormals are within 2^-25 of
  * x), and the SwiGLU intermediate is stored as fp16.  An x element or an
  * intermediate beyond +-65504 (or not finite) is saturated to +-65504 and
@@ -145,7 +146,7 @@ size_t moe_int4_packed_scale_bytes(int E, int N, int K);
  *   magnitudes in [2^-14, 65504], saturating above, fp16 subnormal below).
  * inexact_scales  optional (NULL: not counted): device uint32, incremented
  *   (atomically, on the stream) once per non-zero scale whose magnitude lies
- *   outside [2^-14, 8188] or that is not finite.  When it stays 0, every
+ *   outside [2^-14, 2729] or that is not finite.  When it stays 0, every
  *   dequantised weight (q - 8) * scale the kernels form is exact in fp16.  The
  *   caller zeroes it first.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE (N or K not multiples as above),
@@ -164,13 +165,15 @@ int moe_int4_pack(const uint8_t *q, const uint16_t *scales, int E, int N, int K,
  *      scales  uint8 E8M0 [E][N][K/32] (2^(e - 127)); one per 32 consecutive k.
  *      is_w13  as for moe_int4_pack.
  * Out: packed (moe_int4_packed_bytes) and packed_scales
- *      (moe_int4_packed_scale_bytes), caller-allocated, 16-byte aligned, laid
- *      out as for moe_int4_pack.  Each scale is stored as the fp16 factor the
- *      kernels multiply by, 2^(e - 113) (the dequant's fp16 bit pattern of a
- *      code is its value times 2^-14), representable for e in [89, 128], i.e.
- *      scales 2^-38 .. 2; codes outside that range (and 255, NaN) are clamped to
- *      its ends and counted.  The dequantised fp16 weights are exact for e in
- *      [104, 128]; below, magnitudes under 2^-24 round in fp16.
+ *      (moe_int4_packed_scale_bytes), caller-allocated, 16-byte aligned.  Stages,
+ *      slabs, rows and words are laid out as for moe_int4_pack, but inside word v
+ *      of a row the bytes keep their canonical order: byte c holds the codes of
+ *      k = 8v + 2c (low nibble) and 8v + 2c + 1 (high nibble).  Each scale is
+ *      stored as the fp16 factor the kernels multiply by, the scale 2^(e - 127)
+ *      itself, supported for e in [103, 140] (scales 2^-24 .. 2^13: an fp16
+ *      power of two, and no weight beyond 65504); codes outside that range (and
+ *      255, NaN) are clamped to its ends and counted.  The dequantised fp16
+ *      weights are exact for e in [104, 140].
  *      bad_scales  optional (NULL: not counted): device uint32, incremented
  *              (atomically, on the stream) once per clamped scale; the caller
  *              zeroes it first.
@@ -291,12 +294,12 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
  *   them (moe_int4_clear_errors) once after allocating the workspace.
  * M == 0 returns MOE_OK without touching out.  Every pointer must be 16-byte
  * aligned.  The call launches only kernels (no host sync, no allocation).
- * Launch plan: the align kernel, then, for routings of at most 4096 pairs
- * whose block height is at most 128 (decode-sized batches), one persistent
- * kernel that gathers x, runs the gate/up GEMM and then the down GEMM (its
- * CTAs hand work to each other through counters in the workspace, with bounded
- * waits; it expects to get every SM within about two seconds); otherwise a
- * gather kernel and one kernel per GEMM.  bf16 output adds a conversion kernel.
+ * Launch plan: the align kernel, then, for routings of at most 512 pairs
+ * (decode batches), one persistent kernel that gathers x, runs the gate/up
+ * GEMM and then the down GEMM (its CTAs hand work to each other through
+ * counters in the workspace, with bounded waits; it expects to get every SM
+ * within about two seconds); otherwise a gather kernel and one kernel per
+ * GEMM.  bf16 output adds a conversion kernel.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,
  *   MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  */

@@ -87,18 +87,17 @@ def test_forward_matches_oracle(E, k, H, I, M, seed, plan):
 
 
 def test_fused_plan_covers_the_decode_shapes():
-    """Which forwards run the fused decode kernel: routings of up to 4096 pairs
-    in blocks of up to 128 rows."""
+    """Which forwards run the fused decode kernel: routings of up to 512 pairs
+    (the measured crossover) in blocks of up to 128 rows."""
     ops = _ops()
     k26 = ops.Shape.of(384, 8, 7168, 2048)
-    for M in (1, 9, 90, 256, 512):
-        assert ops.moe_int4_fused(M, k26), M
-    for M in (1024, 8192):  # multi-block align
-        assert not ops.moe_int4_fused(M, k26), M
+    assert [ops.moe_int4_fused(M, k26) for M in (1, 9, 64, 65, 90, 1024)] == [
+        True, True, True, False, False, False]
     mid = ops.Shape.of(64, 6, 4096, 1408)
-    assert [ops.moe_int4_fused(M, mid) for M in (1, 32, 128, 2048, 8192)] == [True, True, True,
+    assert [ops.moe_int4_fused(M, mid) for M in (1, 32, 128, 2048, 8192)] == [True, True, False,
                                                                               False, False]
-    assert not ops.moe_int4_fused(1000, ops.Shape.of(8, 2, 512, 256))  # block 192
+    assert ops.moe_int4_fused(64, ops.Shape.of(64, 8, 256, 128))  # 512 pairs, block 32
+    assert not ops.moe_int4_fused(512, ops.Shape.of(3, 1, 256, 128))  # 512 pairs, block 192
     assert not ops.moe_int4_fused(1, ops.Shape.of(384, 8, 7168, 2048,
                                                   flags=ops.MOE_FLAG_UNFUSED))
 

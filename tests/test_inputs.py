@@ -59,16 +59,21 @@ def test_router_logits_reproduce_the_routings():
 
 
 def test_dequantised_int4_weights_are_exact_in_fp16():
-    """The kernels form (q - 8) * scale in fp16.  For a bf16 scale s in
-    [2^-14, 8188] that product needs at most 8 + 3 significant bits and stays in
-    fp16's normal range, so it is exact: checked here over every positive bf16
-    value of that range and every q."""
-    bits = np.arange(0x3880, 0x4600, dtype=np.uint16)        # 2^-14 .. 8192 (exclusive)
+    """The kernels form (q - 8) * scale in fp16 as one FMA,
+    (16 + q) * s + fp16(-24 * s), rounded once.  For a bf16 scale s in
+    [2^-14, 2729] the addend -24 * s is exact in fp16 and so is the result
+    (8 + 3 significant bits): checked here over every positive bf16 value of
+    that range and every q, the FMA's exact sum rounded to fp16 once."""
+    bits = np.arange(0x3880, 0x4530, dtype=np.uint16)        # 2^-14 .. 2816 (exclusive)
     s = inputs.f32_from_bf16_bits(bits).astype(np.float64)
-    s = s[(s >= 2.0 ** -14) & (s <= 8188.0)]
-    assert s.min() == 2.0 ** -14 and s.max() > 8000.0
-    prod = np.arange(-8, 8, dtype=np.float64)[:, None] * s[None, :]
-    np.testing.assert_array_equal(prod.astype(np.float16).astype(np.float64), prod)
-    # the next bf16 value, 8192, overflows fp16 at q = 0: -8 * 8192 = -65536
+    s = s[(s >= 2.0 ** -14) & (s <= 2729.0)]
+    assert s.min() == 2.0 ** -14 and s.max() == 2720.0
+    addend = (-24.0 * s).astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(addend, -24.0 * s)           # exact
+    q = np.arange(16, dtype=np.float64)[:, None]
+    fma = ((16.0 + q) * s[None, :] + addend[None, :])          # exact in fp64
+    got = fma.astype(np.float16).astype(np.float64)            # one rounding
+    np.testing.assert_array_equal(got, (q - 8.0) * s[None, :])
+    # the next bf16 value, 2736, makes the addend overflow: -24 * 2736 = -65664
     with np.errstate(over="ignore"):
-        assert not np.isfinite(np.float16(-8.0 * 8192.0))
+        assert not np.isfinite(np.float16(-24.0 * 2736.0))

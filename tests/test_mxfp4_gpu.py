@@ -17,9 +17,9 @@ def _ops():
 
 
 def _factor_bits(e):
-    """fp16 bits of 2^(e - 113), the packed factor of an E8M0 code e, clamped to
-    the supported range -- from its definition, on the host."""
-    x = min(15, max(-24, int(e) - 113))
+    """fp16 bits of 2^(e - 127), the packed factor of an E8M0 code e, clamped to
+    the supported range [103, 140] -- from its definition, on the host."""
+    x = min(13, max(-24, int(e) - 127))
     return (x + 15) << 10 if x >= -14 else 1 << (x + 24)
 
 
@@ -29,10 +29,11 @@ def test_packed_scales_are_the_fp16_factors_and_out_of_range_codes_are_counted()
     E, N, K = 2, 256, 128
     rng = np.random.default_rng(4)
     q = torch.from_numpy(rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)).cuda()
-    s = rng.integers(89, 129, (E, N, K // 32), dtype=np.uint8)
+    s = rng.integers(103, 141, (E, N, K // 32), dtype=np.uint8)
+    s[0, 0, 0], s[0, 0, 1] = 103, 140  # the ends of the range
     s[0, 3, 1] = 255   # NaN code
-    s[1, 7, 0] = 200   # above the range
-    s[1, 9, 2] = 10    # below
+    s[1, 7, 0] = 141   # above the range
+    s[1, 9, 2] = 102   # below
     sd = torch.from_numpy(s).cuda()
     _, packed_s, bad = ops.moe_mxfp4_pack(q, sd, True)
     torch.cuda.synchronize()

@@ -96,15 +96,15 @@ def test_normal_inputs_raise_no_range_flag():
 
 
 def test_pack_counts_inexact_scales():
-    """Exactly the non-zero scales outside [2^-14, 8188] (and non-finite ones)
-    are counted; the largest bf16 inside is 8160, the next one 8192."""
+    """Exactly the non-zero scales outside [2^-14, 2729] (and non-finite ones)
+    are counted; the largest bf16 inside is 2720, the next one 2736."""
     import torch
     ops = _ops()
     rng = np.random.default_rng(45)
     q = inputs._random_nibble_bytes(rng, (1, 256, 32))
     s = rng.uniform(0.005, 0.02, size=(1, 256, 2)).astype(np.float32)
-    inside = [0.0, -0.0, 2.0 ** -14, -(2.0 ** -14), 8160.0, -8160.0]
-    outside = [2.0 ** -15, 1e-6, -1e-7, 8192.0, -9000.0, 1e5, np.inf, -np.inf, np.nan]
+    inside = [0.0, -0.0, 2.0 ** -14, -(2.0 ** -14), 2720.0, -2720.0]
+    outside = [2.0 ** -15, 1e-6, -1e-7, 2736.0, -9000.0, 1e5, np.inf, -np.inf, np.nan]
     vals = inside + outside
     s.flat[: len(vals)] = vals
     bits = inputs.bf16_bits_from_f32(s)

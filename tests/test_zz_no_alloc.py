@@ -6,10 +6,12 @@ is a fixed 1 MiB array inside the library.
 This file is collected last on purpose, so that a run stopping at the first
 failure has already run every other test.  The GPU tests call the entry point
 through the C ABI twice in a row and require the same bit-exact result as
-moe_align with caller-provided scratch (index work: no tolerance)."""
+moe_align with caller-provided scratch and as the oracle's align (index work:
+no tolerance)."""
 import numpy as np
 import pytest
 
+import oracle
 from weight_only_int4_moe_gb300 import ops
 
 LIMIT = 1 << 20
@@ -42,11 +44,17 @@ def _compare(ids, E, B, first, second):
     s_ref, e_ref, n_ref, err_ref = ops.moe_align(torch.from_numpy(ids).cuda(), E, B)
     torch.cuda.synchronize()
     n = int(n_ref.item())
+    rs, re_, rn, rd = oracle.align(ids, E, B)
+    assert n == rn
     for s, e, npp, err in (first, second):
         assert int(npp.item()) == n
         assert torch.equal(s[:n], s_ref[:n])
         assert torch.equal(e[: n // B], e_ref[: n // B])
         assert torch.equal(err, err_ref)
+        # and directly against the oracle's align
+        np.testing.assert_array_equal(s[:n].cpu().numpy(), rs)
+        np.testing.assert_array_equal(e[: n // B].cpu().numpy(), re_)
+        assert err.cpu().numpy().tolist() == [1 if rd else 0, rd]
 
 
 @pytest.mark.gpu

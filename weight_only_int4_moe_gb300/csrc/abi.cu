@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "moe_int4.h"
@@ -18,6 +19,12 @@ namespace {
 
 constexpr int kMaxGrid = 160;          // persistent GEMM grid cap (GB300: 152 SMs)
 constexpr int kSingleBlockAlignMax = 4096;
+// Largest routing (pairs) that runs the fused decode kernel.  Same-box A/B
+// against the separate kernels: faster at K2.6 M = 1 and 9 (8, 72 pairs) and
+// mid-size M = 1 and 32 (6, 192), slower by 0.6-1 % from about 700 pairs up
+// (K2.6 M = 90, verify M = 256 and 512, mid-size M = 128), where the separate
+// gather kernel copies the rows faster than the fused kernel's gather share.
+constexpr int kFusedMaxPairs = 512;
 constexpr int kAlignChunk = 1024;
 
 thread_local int g_last_launches = 0;
@@ -67,7 +74,7 @@ struct Plan {
     int M, E, k, H, I, P, BM, RT1, RT2, n_chunks, out_f32;
     bool fused;  // the fused decode kernel (gather + gate/up + down in one launch)
     size_t cap, blocks_cap, tiles1_cap;
-    size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_cnt, off_partial, off_a,
+    size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_pos, off_cnt, off_partial, off_a,
         off_x16, off_acc, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
 };
 
@@ -88,13 +95,14 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.cap = (size_t)p.P + touched * (size_t)(p.BM - 1);
     p.blocks_cap = p.cap / p.BM + 1;
     p.tiles1_cap = p.blocks_cap * p.RT1;
-    p.fused = !(sh->flags & MOE_FLAG_UNFUSED) && p.n_chunks == 0 && p.BM <= 128;
+    p.fused = !(sh->flags & MOE_FLAG_UNFUSED) && p.P <= kFusedMaxPairs && p.BM <= 128;
     size_t o = 0;
     p.off_err = o; o += 256;
     p.off_npp = o; o += 256;
     p.off_sorted = o; o = rup(o + p.cap * 4, 256);
     p.off_expert = o; o = rup(o + p.blocks_cap * 4, 256);
     p.off_chunk = o; o = rup(o + (size_t)p.n_chunks * p.E * 4, 256);
+    p.off_pos = o; o = rup(o + (p.fused ? (size_t)p.P * 4 : 0), 256);  // pair -> position
     // counters zeroed by the align launch: gate/up split counters, then (fused
     // kernel) per-block finished gate/up tiles and the CTAs done with their
     // gather and zeroing share
@@ -373,6 +381,7 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     al.err = err;
     al.chunk_tab = reinterpret_cast<int32_t *>(ws + pl.off_chunk);
     al.n_chunks = pl.n_chunks;
+    al.pos_of = pl.fused ? reinterpret_cast<int32_t *>(ws + pl.off_pos) : nullptr;
     // the align launch zeroes the counters; the gate/up GEMM (or the fused
     // kernel) zeroes the down accumulator (off the align's critical path)
     ZeroArgs z{};
@@ -417,6 +426,12 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
     g.block_m = pl.BM;
     g.round_robin = 1;
     g.fmt = shape->weight_format;
+    g.skip_stage = -1;
+#ifdef MOE_DEBUG_BOUNDS
+    // the debug build's timeout test: MOE_INT4_DEBUG_SKIP_STAGE=i makes CTA 0
+    // of the first GEMM kernel leave its weight stage i out (see GemmParams)
+    if (const char *v = getenv("MOE_INT4_DEBUG_SKIP_STAGE")) g.skip_stage = atoi(v);
+#endif
 
     int32_t *cnt = reinterpret_cast<int32_t *>(ws + pl.off_cnt);
     g.g[0].wq = reinterpret_cast<const uint8_t *>(w13_packed);
@@ -445,6 +460,7 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
         gf.zero_n16 = (size_t)pl.M * pl.H * 4 / 16;
         gf.x = x;
         gf.x16 = x16;
+        gf.pos_of = al.pos_of;
         gf.blk_done = cnt + pl.tiles1_cap;
         gf.prep_done = cnt + pl.tiles1_cap + pl.blocks_cap;
         if (!plan_gemm_smem(3, gf)) return MOE_ERR_SHAPE;
@@ -461,6 +477,7 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
             return MOE_ERR_CUDA;
         prof_record(2, s);
         GemmParams g2 = g;
+        g2.skip_stage = -1;
         if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
         if (launch_gemm(2, g2, &tmap_x, &tmap_a, grid, s, &launches) != cudaSuccess)
             return MOE_ERR_CUDA;

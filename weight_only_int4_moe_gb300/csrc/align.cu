@@ -103,6 +103,7 @@ __device__ void align_place_round(const AlignArgs &a, int i0, int *base, int *wt
     }
     __syncthreads();
     if (valid) a.sorted_ids[wtab[wid * a.E + e] + rank] = i;
+    if (a.pos_of && i < a.P) a.pos_of[i] = valid ? wtab[wid * a.E + e] + rank : -1;
     __syncthreads();
 }
 

@@ -95,8 +95,14 @@ constexpr bool kDebugBounds = false;
 
 // A pipeline wait that takes longer than this many SM cycles (about 2 s at the
 // GB300's 2.07 GHz maximum clock) is treated as a kernel bug: the waiting role
-// records kErrTimeout and the CTA winds down.
+// records kErrTimeout and the CTA winds down.  Debug-bounds builds give up
+// after about 50 ms, so that their timeout test (a stage whose copy is never
+// issued) ends quickly.
+#ifdef MOE_DEBUG_BOUNDS
+constexpr long long kWaitTimeoutCycles = 100000000ll;
+#else
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
+#endif
 
 MOE_DEV bool bounds_ok(bool in_range, uint32_t *err) {
     if (!kDebugBounds) return true;
@@ -160,7 +166,7 @@ MOE_DEV bool mbar_try_wait_nohint(uint32_t bar, uint32_t parity) {
 // Returns false (and records the timeout) if the wait gives up or another role
 // of the CTA already aborted.
 MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint32_t *err,
-                       uint32_t backoff_ns = 0) {
+                       uint32_t backoff_ns = 0, long long limit = kWaitTimeoutCycles) {
     if (mbar_try_wait_nohint(bar, parity)) return true;
 #pragma unroll 1
     for (int it = 0; it < 8; ++it)
@@ -174,7 +180,7 @@ MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, 
             if (backoff_ns) __nanosleep(backoff_ns);
         }
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitTimeoutCycles) break;
+        if (clock64() - t0 > limit) break;
     }
     *abort_flag = 1;
     if (err) atomicOr(err, kErrTimeout);

@@ -75,12 +75,18 @@ constexpr uint32_t kStageW = 2 * kStageWBytes;  // 16 KB of INT4 per stage
 constexpr uint32_t kStageS = 2 * kStageSBytes;  // 2 KB of scales per stage
 constexpr uint32_t kStage = kStageW + kStageS;  // 18 KB
 constexpr uint32_t kACols = 128;                // TMEM columns per A stage
-// hardware named barriers (0 is __syncthreads)
+// Hardware named barriers (0 is __syncthreads).  A hardware barrier cannot give
+// up, so each is used only where every participant is certain to arrive (see
+// the dequant role for the A-slot hand-off).
 constexpr uint32_t kBarEpi = 1;     // the four epilogue warps
 constexpr uint32_t kBarSlot0 = 2;   // A stage s written: all dequant warps arrive, issuers wait
                                     // (ids 2..4: one per A stage or stage half)
-constexpr uint32_t kBarPrep = 5;    // fused kernel: the gather and zeroing warps (1, 20..23)
-constexpr uint32_t kPrepThreads = 5 * 32;
+constexpr uint32_t kBarPrep = 5;    // fused kernel: the gather and zeroing warps (1, 4..23)
+constexpr uint32_t kGatherWarps = 20;  // fused kernel: warps 4..23 gather before their roles
+constexpr uint32_t kPrepThreads = (1 + kGatherWarps) * 32;
+// The dequant teams' wait for a free A slot gives up only after this many
+// cycles, far longer than any other wait (see the dequant role).
+constexpr long long kSlotWaitCycles = 16 * kWaitTimeoutCycles;
 
 // The schedule: tiles [0, rr) round-robin (whole tiles, CTA c takes c, c + G,
 // ...), then tiles [rr, tiles) split evenly by stages.  Stage indices of the
@@ -176,6 +182,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     bool ok = mbar_wait(bar, parity, abort, err, backoff_ns);
     return __all_sync(0xffffffffu, ok);
 }
+__device__ __forceinline__ bool warp_wait_limit(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                uint32_t *err, long long limit) {
+    bool ok = mbar_wait(bar, parity, abort, err, 0, limit);
+    return __all_sync(0xffffffffu, ok);
+}
 
 // Whole-warp wait for CTA stage `stage` in a weight-ring slot.  A team sees
 // only every fourth stage, so it does not follow every phase of a slot; a
@@ -220,6 +231,50 @@ __device__ bool wait_counter(const int32_t *ctr, int target, volatile int *abort
     }
 }
 
+// A GEMM kind as a type: the fused kernel runs each role's phase loop once per
+// kind through a generic lambda, so that `kind` is a compile-time constant in
+// both phases as it is in the separate kernels.
+template <int K>
+struct KindC {
+    static constexpr int value = K;
+};
+
+// The fused kernel's gather: fp16 rows of x in bucketed order (the gate/up
+// GEMM's B operand).  The work is cut into pieces of 256 elements of one pair's
+// row (one 16-byte load per lane), dealt out over the gathering warps of the
+// whole grid (`gw` of `nw`) in contiguous runs, so that even a handful of rows
+// (decode) is copied in about one memory round trip: a lane keeps up to 4 loads
+// in flight.  `pos_of` (from the align) gives each pair's row.
+__device__ __forceinline__ void fused_gather(const GemmParams &p, int gw, int nw, bool &bad) {
+    const int lane = threadIdx.x & 31;
+    const int pieces = (p.H + 255) / 256;  // H % 256 == 128: a half last piece
+    const long long total = (long long)p.P * pieces;
+    const long long lo = total * gw / nw, hi = total * (gw + 1) / nw;
+    for (long long i0 = lo; i0 < hi; i0 += 4) {
+        uint4 v[4];
+        int dst_row[4], col[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long long it = i0 + u;
+            dst_row[u] = -1;
+            if (it < hi) {
+                const int pair = (int)(it / pieces);
+                col[u] = (int)(it % pieces) * 256 + lane * 8;
+                if (col[u] < p.H) {
+                    v[u] = *reinterpret_cast<const uint4 *>(p.x + (size_t)(pair / p.top_k) * p.H +
+                                                            col[u]);
+                    dst_row[u] = __ldcg(p.pos_of + pair);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (dst_row[u] >= 0 && bounds_ok(dst_row[u] < p.cap, p.err))
+                *reinterpret_cast<uint4 *>(p.x16 + (size_t)dst_row[u] * p.H + col[u]) =
+                    bf16x8_to_f16x8_sat(v[u], bad);
+    }
+}
+
 // Sub-stages of stage j of a tile with `kss` sub-stages (the last may hold one).
 __device__ __forceinline__ int stage_subs(int j, int kss) {
     return (2 * j + 2 <= kss) ? 2 : 1;
@@ -235,37 +290,40 @@ __device__ __forceinline__ uint32_t as_u32(__half2 h) {
 // One slab row of a sub-stage: 64 weights (k = 0..63 of the slab's k block) as
 // 32 fp16 pairs (q - 8) * s, out[c] holding k = 2c (low half) and 2c + 1 (high).
 // Word v holds k = 8v..8v+7: bits 4s and 16+4s are k = 8v+2s and 8v+2s+1.
-// (w & mask) | magic is the fp16 pair (1024 + q) (or 1024 + 16 q for the odd
-// nibble position); subtracting 1032 (or the FMA x/16 - 72) is exact, and the
-// one rounding is the final product with the fp16 scale (two per word `sc`).
+// Shifted so that the pair's nibbles sit at bits 6..9 of each half, masked and
+// ORed with the exponent of 16, the word is the fp16 pair (16 + q): a mantissa
+// bit 6 of an fp16 in [16, 32) weighs 1.  One FMA then gives
+// (16 + q) * s - 24 * s = (q - 8) * s with a single rounding of the exact
+// result, so the weight is exact: 24 * s is exact in fp16 (24 has two
+// significant bits, s at most eight, from bf16) for |s| in [2^-14, 2729], and
+// (q - 8) * s needs at most 8 + 3 significant bits.  Four shifts, four
+// logic operations and four FMAs per eight weights; one FMA-pipe instruction
+// per two weights where a subtraction and a multiply took two (measured 3.5 %
+// faster at decode).
 __device__ __forceinline__ void dequant_row(const uint4 lo, const uint4 hi, uint32_t sc,
                                             const DequantConsts &k, uint32_t (&out)[32]) {
     const __half2 s0 = as_h2(__byte_perm(sc, 0, 0x1010));  // group 0 scale, both halves
     const __half2 s1 = as_h2(__byte_perm(sc, 0, 0x3232));  // group 1 scale
-    const __half2 c1032 = as_h2(k.c1032);
-    const __half2 c16th = as_h2(k.c16th);
-    const __half2 cm72 = as_h2(k.cm72);
+    const __half2 cm24 = as_h2(k.cm24);
+    const __half2 b0 = __hmul2(s0, cm24), b1 = __hmul2(s1, cm24);  // -24 * s, exact
     const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
     for (int v = 0; v < 8; ++v) {
         const __half2 s2 = (v < 4) ? s0 : s1;
-        const uint32_t w8 = w[v] >> 8;
-        out[4 * v + 0] = as_u32(__hmul2(__hsub2(as_h2((w[v] & k.mask_lo) | k.magic), c1032), s2));
-        out[4 * v + 1] =
-            as_u32(__hmul2(__hfma2(as_h2((w[v] & k.mask_hi) | k.magic), c16th, cm72), s2));
-        out[4 * v + 2] = as_u32(__hmul2(__hsub2(as_h2((w8 & k.mask_lo) | k.magic), c1032), s2));
-        out[4 * v + 3] =
-            as_u32(__hmul2(__hfma2(as_h2((w8 & k.mask_hi) | k.magic), c16th, cm72), s2));
+        const __half2 b2 = (v < 4) ? b0 : b1;
+        const uint32_t t[4] = {w[v] << 6, w[v] << 2, w[v] >> 2, w[v] >> 6};
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            out[4 * v + s] = as_u32(__hfma2(as_h2((t[s] & k.nib_mask) | k.magic16), s2, b2));
     }
 }
 
-// MXFP4: the same 32 pairs from FP4 E2M1 codes in the same nibble order,
-// e2m1(q) * 2^(e - 127).  With the code's magnitude bits (exponent, mantissa)
-// moved to fp16 bits 11..9 and its sign to bit 15, the fp16 value is exactly the
-// code's value times 2^-14 -- codes of exponent 0 (0 and 0.5) land on fp16 zero
-// and subnormals, the others on normals with the right exponent -- so the
-// packed scale carries 2^(e - 127 + 14) and one multiply finishes the weight.
-// Two shifts, two logic operations and a multiply per two weights.
+// MXFP4: the same 32 pairs from FP4 E2M1 codes, e2m1(q) * 2^(e - 127).  The
+// MXFP4 pack keeps each word's bytes in canonical order (byte c of word v holds
+// k = 8v + 2c in its low nibble and 8v + 2c + 1 in its high one), so one
+// cvt.rn.f16x2.e2m1x2 turns a byte into the exact fp16 pair (low nibble in the
+// low half) and one multiply by the packed scale 2^(e - 127) finishes it: two
+// instructions per two weights.
 __device__ __forceinline__ void dequant_row_fp4(const uint4 lo, const uint4 hi, uint32_t sc,
                                                 uint32_t out[32]) {
     const __half2 s0 = as_h2(__byte_perm(sc, 0, 0x1010));
@@ -274,12 +332,14 @@ __device__ __forceinline__ void dequant_row_fp4(const uint4 lo, const uint4 hi, 
 #pragma unroll
     for (int v = 0; v < 8; ++v) {
         const __half2 s2 = (v < 4) ? s0 : s1;
+        uint32_t c[4];
+        asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+            "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+            : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3])
+            : "r"(w[v]));
 #pragma unroll
-        for (int b = 0; b < 16; b += 4) {  // nibbles at bits b.. and 16 + b..
-            const uint32_t mag = ((b <= 9) ? (w[v] << (9 - b)) : (w[v] >> (b - 9))) & 0x0E000E00u;
-            const uint32_t sgn = (w[v] << (12 - b)) & 0x80008000u;
-            out[4 * v + b / 4] = as_u32(__hmul2(as_h2(mag | sgn), s2));
-        }
+        for (int b = 0; b < 4; ++b) out[4 * v + b] = as_u32(__hmul2(as_h2(c[b]), s2));
     }
 }
 
@@ -443,6 +503,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int tile, kb0, kb1;
 
+    if (kFused && wid >= kFirstDequantWarp) {
+        // The fused kernel's warps 4..23 gather x first (each CTA its share), an
+        // idle time for them anyway: the weight stream waits for the gather.  The
+        // tensor-memory owner warp then publishes the share with its zeroing.
+        bool bad = false;
+        fused_gather(p, blockIdx.x * kGatherWarps + (wid - kFirstDequantWarp),
+                     gridDim.x * kGatherWarps, bad);
+        report_range(bad, p.err);
+        __threadfence();
+        fence_proxy_async_global();
+        named_bar_sync(kBarPrep, kPrepThreads);
+    }
+
     if (wid == 0 || wid == 3) {
         // --------------------------- weight (warp 0) / scale (warp 3) producer --
         if (lane == 0) {
@@ -453,7 +526,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t i = 0;
             Ring w(n_w);
             bool ok = true;
-            for (int kind = kKind0; kind <= kKind1 && ok; ++kind) {
+            // Fused kernel: the weight stream starts once every CTA has published
+            // its gather share.  Started earlier, its burst of requests (about
+            // 150 KB per SM) queues ahead of the gather's few row loads in the
+            // memory system and delays them several times over (measured at
+            // decode sizes: the gather then took 10 us instead of about 2).
+            if (kFused) ok = wait_counter(p.prep_done, (int)gridDim.x, abort_flag, p.err);
+            auto phase = [&](auto kc) {
+                constexpr int kind = decltype(kc)::value;
                 const GemmPhase &G = p.g[kind - 1];
                 const Sched sched = make_sched(p, G);
                 PieceIter pi;
@@ -470,13 +550,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         const uint32_t bytes = stage_subs(j, G.KSS) * sub_bytes;
+                        if (kDebugBounds && !scales && (int)i == p.skip_stage && blockIdx.x == 0)
+                            continue;  // the timeout test: this stage never lands
                         if (!scales) w_tag[w.idx] = i;
                         mbar_arrive_expect_tx(bar_w_full + 8 * w.idx, bytes);
                         bulk_g2s(w_ring + w.idx * kStage + dst_off, src + (sub0 + 2 * j) * sub_bytes,
                                  bytes, bar_w_full + 8 * w.idx, pol);
                     }
                 }
-            }
+            };
+            if (kKind0 == 1) phase(KindC<1>{});
+            if (kKind1 == 2 && ok) phase(KindC<2>{});
             if (!ok) {  // let copies in flight land before the CTA exits
                 volatile int never = 0;
                 const uint32_t first = (i > (uint32_t)n_w) ? i - n_w : 0;
@@ -499,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __stcs(p.zero_out + i, z4);
         }
         if (kFused) {
-            // publish this CTA's share of the gather (epilogue warps) and of the
+            // publish this CTA's share of the gather (warps 4..23) and of the
             // zeroing: each thread's writes, then one release of the count
             __threadfence();
             fence_proxy_async_global();
@@ -515,7 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t i = 0;
             bool ok = true;
             Ring bq(n_b);
-            for (int kind = kKind0; kind <= kKind1 && ok; ++kind) {
+            auto phase = [&](auto kc) {
+                constexpr int kind = decltype(kc)::value;
                 const GemmPhase &G = p.g[kind - 1];
                 const CUtensorMap *tm = (kind == 1) ? &tmap_x : &tmap_a;
                 const int kb_per_sub = (kind == 1) ? 1 : 2;
@@ -557,7 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-            }
+            };
+            if (kKind0 == 1) phase(KindC<1>{});
+            if (kKind1 == 2 && ok) phase(KindC<2>{});
             if (!ok) {
                 volatile int never = 0;
                 const uint32_t first = (i > (uint32_t)n_b) ? i - n_b : 0;
@@ -591,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         long long s0 = 0;           // CTA stage index of the current piece's first stage
         long long own = team;       // next stage of this team
         bool ok = true;
-        for (int kind = kKind0; kind <= kKind1; ++kind) {
+        auto phase = [&](auto kc) {
+            constexpr int kind = decltype(kc)::value;
             const GemmPhase &G = p.g[kind - 1];
             const int kss = G.KSS;
             const Sched sched = make_sched(p, G);
@@ -613,13 +701,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // of the stage n_a earlier on it are done; the issuers
                         // signal that on this team's own barrier for the part,
                         // whose phases follow the team's stages in order, so a
-                        // parity wait is never more than one phase behind.  This
-                        // wait happens even after an error: it keeps this warp
-                        // from arriving on the part's named barrier again before
-                        // the issuers have consumed the previous arrival.
+                        // parity wait is never more than one phase behind.
+                        //
+                        // The hand-off to the issuers is a hardware named barrier
+                        // (a bar.arrive here, a bar.sync there; measured 5 %
+                        // faster than an mbarrier at decode), which cannot give up.
+                        // So this team must never arrive on the part's barrier
+                        // again before the issuers have consumed its previous
+                        // arrival, even after an error: this wait ignores the abort
+                        // flag and its limit is 16 times every other wait's.  The
+                        // issuers release the slot as soon as they have passed
+                        // the (at most three) stages before it, and each of those
+                        // stalls them only for other waits, every one bounded by
+                        // the normal limit and ended early by the abort flag, so
+                        // this wait runs out only if the tensor cores stop
+                        // completing MMAs.
                         if (own >= n_a) {
-                            const bool freed = warp_wait(bar_a_free + 8 * (team * np + part),
-                                                         (a_ph >> part) & 1u, &no_abort, p.err);
+                            const bool freed =
+                                warp_wait_limit(bar_a_free + 8 * (team * np + part),
+                                                (a_ph >> part) & 1u, &no_abort, p.err,
+                                                kSlotWaitCycles);
                             a_ph ^= 1u << part;
                             if (!freed) ok = false;
                         }
@@ -650,7 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 s0 = s1;
             }
-        }
+        };
+        if (kKind0 == 1) phase(KindC<1>{});
+        if (kKind1 == 2) phase(KindC<2>{});
     } else if (wid >= kFirstIssuerWarp && wid < kFirstEpilogueWarp) {
         // ------------------------------------------------------- MMA issue --
         // Warp 16 + qe issues the MMAs of sub-tile qe (slab qe & 1,
@@ -673,7 +776,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t c = 0;
         bool ok = true;
         bool range_bad = false;  // a SwiGLU value saturated (helping issuers)
-        for (int kind = kKind0; kind <= kKind1; ++kind) {
+        auto phase = [&](auto kc) {
+            constexpr int kind = decltype(kc)::value;
             const GemmPhase &G = p.g[kind - 1];
             const int kss = G.KSS;
             const int kb_per_sub = (kind == 1) ? 1 : 2;
@@ -791,7 +895,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++c;
             }
-        }
+        };
+        if (kKind0 == 1) phase(KindC<1>{});
+        if (kKind1 == 2) phase(KindC<2>{});
         if (kHelp) report_range(range_bad, p.err);
         if (issuer) {  // every MMA of this CTA must finish before TMEM is released
             volatile int never = 0;
@@ -807,27 +913,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         uint32_t c = 0;
         bool ok = true;
-        bool range_bad = false;  // a SwiGLU value (or, fused, an x element) saturated
+        bool range_bad = false;  // a SwiGLU value saturated
         if (!kFused) pdl_wait();  // counters, partial slots and the accumulator (see above)
-        if (kFused) {
-            // this CTA's share of the gather: fp16 rows of x in bucketed order
-            // (the gate/up GEMM's B operand), one warp per row; published with
-            // the zeroing share by the tensor-memory owner warp
-            int npp = __ldcg(p.num_post_pad);
-            if (!bounds_ok(npp >= 0 && npp <= p.cap, p.err)) npp = 0;
-            for (int pos = blockIdx.x * 4 + q; pos < npp; pos += gridDim.x * 4) {
-                const int pair = __ldcg(p.sorted_ids + pos);
-                if (pair >= p.P) continue;  // a pad
-                if (!bounds_ok(pair >= 0, p.err)) continue;
-                gather_row<8>(p.x + (size_t)(pair / p.top_k) * p.H, p.x16 + (size_t)pos * p.H,
-                              p.H, range_bad);
-            }
-            __threadfence();
-            fence_proxy_async_global();
-            named_bar_sync(kBarPrep, kPrepThreads);
-        }
         bool zero_seen = !kFused;  // fused: every CTA's zeroing share is published
-        for (int kind = kKind0; kind <= kKind1; ++kind) {
+        auto phase = [&](auto kc) {
+            constexpr int kind = decltype(kc)::value;
             const GemmPhase &G = p.g[kind - 1];
             const Sched sched = make_sched(p, G);
             PieceIter pi;
@@ -998,6 +1088,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     dv[jj] *= __int_as_float(col_tab[j0 + jj].y);
 #pragma unroll
                                 for (int h = 0; h < 16; h += 8) {
+                                    if (j0 + h >= nr) break;  // no real column left (decode)
 #pragma unroll
                                     for (int jj = 0; jj < 8; ++jj) stg[jj * 32 + lane] = dv[h + jj];
                                     __syncwarp();
@@ -1043,7 +1134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++c;
             }
-        }
+        };
+        if (kKind0 == 1) phase(KindC<1>{});
+        if (kKind1 == 2) phase(KindC<2>{});
         report_range(range_bad, p.err);
     }
 
@@ -1055,12 +1148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 bool plan_gemm_smem(int kind, GemmParams &p) {
-    p.dq.mask_lo = 0x000F000Fu;
-    p.dq.mask_hi = 0x00F000F0u;
-    p.dq.magic = 0x64006400u;  // fp16 1024 in both halves
-    p.dq.c1032 = 0x64086408u;  // fp16 1032
-    p.dq.c16th = 0x2C002C00u;  // fp16 1/16
-    p.dq.cm72 = 0xD480D480u;   // fp16 -72
+    p.dq.nib_mask = 0x03C003C0u;  // bits 6..9 of each half
+    p.dq.magic16 = 0x4C004C00u;   // fp16 16 in both halves
+    p.dq.cm24 = 0xCE00CE00u;      // fp16 -24 in both halves
     const int BM = p.block_m;
     if (BM < 16 || BM % 16 != 0 || BM > 192) return false;
     if (kind == 3 && BM > 128) return false;  // the fused kernel runs narrow blocks

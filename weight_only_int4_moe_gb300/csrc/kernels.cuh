@@ -35,6 +35,7 @@ struct AlignArgs {
     uint32_t *err;         // [2] or null
     int32_t *chunk_tab;    // [n_chunks][E] (multi-block path)
     int n_chunks;          // 0: single-block path
+    int32_t *pos_of;       // [P] or null: each pair's position in sorted_ids (-1: dropped)
 };
 
 // Router: per token, the top_k experts by logit (ties: lower index first) and
@@ -84,10 +85,9 @@ constexpr int kStageBytes = kStageWBytes + kStageSBytes;  // 9216
 // parameters so that they stay constant-bank operands instead of immediates
 // the compiler re-materialises in registers for every use.
 struct DequantConsts {
-    uint32_t mask_lo, mask_hi;  // nibble masks 0x000F000F, 0x00F000F0
-    uint32_t magic;             // fp16 pair (1024, 1024): 0x6400 exponent bits
-    uint32_t c1032;             // fp16 pair 1032 = 1024 + 8
-    uint32_t c16th, cm72;       // fp16 pairs 1/16 and -72 (high nibble: x/16 - 72)
+    uint32_t nib_mask;  // 0x03C003C0: a nibble at bits 6..9 of each half
+    uint32_t magic16;   // fp16 pair (16, 16): with the nibble, the pair (16 + q)
+    uint32_t cm24;      // fp16 pair (-24, -24): times the scale, the FMA's addend
 };
 
 // One of the two grouped GEMMs: g[0] the gate/up GEMM, g[1] the down GEMM.
@@ -115,6 +115,7 @@ struct GemmParams {
     // fused kernel only: the gather of x and the hand-offs between CTAs
     const uint16_t *x;         // bf16 [M][H]
     uint16_t *x16;             // fp16 rows of x in bucketed order [cap][H]
+    const int32_t *pos_of;     // [P]: each pair's row in x16 (-1: dropped), from the align
     int32_t *blk_done;         // [blocks]: gate/up tiles finished, per expert block
     int32_t *prep_done;        // [1]: CTAs done with their share of the gather and zeroing
     int M, top_k, H, I, P, E;
@@ -129,6 +130,9 @@ struct GemmParams {
     int fmt;                   // weight format: MOE_W_INT4 or MOE_W_MXFP4 (picks the kernel)
     int round_robin;           // 1: whole waves of tiles round-robin, the rest split by stages
                                // (0: all split by stages)
+    int skip_stage;            // debug-bounds builds: CTA 0 never issues the weight copy of
+                               // its stage with this index (-1: none), so the wait for it
+                               // runs out (the timeout test); ignored by other builds
     uint32_t b_stage_bytes;
     uint32_t smem_b_off, smem_misc_off, smem_bytes;
     DequantConsts dq;

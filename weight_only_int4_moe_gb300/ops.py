@@ -432,7 +432,7 @@ class PackedWeights:
         # forward still runs; see moe_int4_pack)
         self.inexact_scales = 0 if mx else n_bad
         if mx and n_bad:
-            raise ValueError(f"{n_bad} E8M0 scales outside the supported range [89, 128]")
+            raise ValueError(f"{n_bad} E8M0 scales outside the supported range [103, 140]")
 
     def forward(self, x, topk_ids, topk_weights, out=None, workspace=None, stream=None):
         return moe_int4_forward(x, self.w13, self.w13_scales, self.w2, self.w2_scales, topk_ids,
