@@ -17,10 +17,10 @@
 //    scales), so the weight stream reaches HBM speed with few, large requests.
 //  * Three teams of four dequant warps take stages in turn; each warp covers
 //    its 32-row lane quadrant of both slabs and both sub-stages, turning the
-//    packed words into fp16 weights (q-8)*s -- a mask/OR into an fp16 with
-//    exponent 2^10, an exact subtraction (or 1/16-scaled FMA for the high
-//    nibble), one multiply by the scale; two weights per instruction -- and
-//    storing them into tensor memory, which tcgen05.mma reads as its A operand.
+//    packed words into fp16 weights (q-8)*s -- a shift and a mask/OR that put
+//    the nibble into the mantissa of fp16 16, then one FMA (v*s - 24s, exact),
+//    two weights per instruction -- and storing them into tensor memory, which
+//    tcgen05.mma reads as its A operand.
 //  * The B operand (fp16 activations) sits in shared memory in the 128-byte-
 //    swizzled K-major layout, fetched by 2-D TMA tensor copies of rows in
 //    bucketed order: x gathered once per call into that order (gate/up), the
@@ -46,11 +46,14 @@
 //    a counter); no CTA ever waits for another.
 //
 // Warp roles (768 threads): 0 weight producer, 1 TMEM owner (in gate/up it
-// also zeroes the down GEMM's fp32 accumulator), 2 B loader, 3 scale producer,
-// 4-15 dequant (three teams), 16-19 MMA issue, 20-23 epilogue.  Each (slab,
-// sub-stage) has its own issuing warp and accumulator (the epilogue sums them):
-// one thread issuing tcgen05.mma waits tens of cycles per instruction while
-// MMAs from several warps overlap.  Every mbarrier wait is bounded
+// also zeroes the down GEMM's fp32 accumulator; with blocks of up to 128 rows
+// it then waits for each stage's B slot on the issuers' behalf), 2 B loader,
+// 3 scale producer, 4-15 dequant (three teams), 16-19 MMA issue, 20-23
+// epilogue.  Each (slab, sub-stage) has its own issuing warp and accumulator
+// (the epilogue sums them): one thread issuing tcgen05.mma waits tens of
+// cycles per instruction while MMAs from several warps overlap.  At decode
+// sizes the issuers' per-stage path (barrier, MMAs, commits) sets the stage
+// rate, so it is kept short.  Every mbarrier wait is bounded
 // (MOE_DEVERR_TIMEOUT).
 #include <cuda_fp16.h>
 
@@ -414,6 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BM = p.block_m;
     const int n_w = p.n_w, n_b = p.n_b, n_a = p.n_a;
+    // Narrow blocks (one part, one B slot per stage, two or four issuers):
+    // warp 1 waits for each stage's B slot and then joins the stage's A-slot
+    // barrier, so no MMA issuer waits for B (the issuers' per-stage path
+    // bounds the stage rate at decode sizes).
+    const bool b_waiter = !WIDE && p.ni != 1;
     const int ni = p.ni;    // MMA issuers (4: one per dequant group, 2: one per slab)
 
     // shared-memory map
@@ -590,6 +598,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(kBarPrep, kPrepThreads);
             if (lane == 0) red_release_gpu(p.prep_done, 1);
         }
+        if (b_waiter) {
+            // ------------------------------------------------ B waiter --
+            // Every stage in order, as the issuers take them: B slot landed,
+            // then the stage's A-slot barrier (a bar.sync like the issuers',
+            // so this warp never arrives twice on one barrier instance).
+            // After an error it still visits every barrier, without waiting.
+            const uint32_t slot_cnt = (uint32_t)(kTeamWarps + part_issuers(ni, np) + 1) * 32u;
+            Ring a(n_a), bq(n_b);
+            bool ok = true;
+            auto phase = [&](auto kc) {
+                constexpr int kind = decltype(kc)::value;
+                const GemmPhase &G = p.g[kind - 1];
+                const Sched sched = make_sched(p, G);
+                PieceIter pi;
+                pi.init(sched);
+                while (pi.next(sched, tile, kb0, kb1)) {
+#pragma unroll 1
+                    for (int j = kb0; j < kb1; ++j, a.next(), bq.next()) {
+                        if (ok) ok = warp_wait(bar_b_full + 8 * bq.idx, bq.ph, abort_flag, p.err);
+                        named_bar_sync(kBarSlot0 + a.idx, slot_cnt);
+                    }
+                }
+            };
+            if (kKind0 == 1) phase(KindC<1>{});
+            if (kKind1 == 2) phase(KindC<2>{});
+        }
     } else if (wid == 2) {
         // ------------------------------------------------------ B loader --
         // B rows of the block (bucketed order) by 2-D TMA tensor copies: one
@@ -668,7 +702,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t my_w = w_ring + (uint32_t)row * 16u;  // shared addresses
         const uint32_t my_s = w_ring + kStageW + (uint32_t)row * 4u;
         const uint32_t my_t = tmem + lane_off + col_a;
-        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + part_issuers(ni, np)) * 32u;
+        const uint32_t slot_cnt =
+            (uint32_t)(kTeamWarps + part_issuers(ni, np) + (b_waiter ? 1 : 0)) * 32u;
         const DequantConsts dqc = p.dq;
         volatile int no_abort = 0;
         Ring w(n_w), a(n_a);  // a: the A slot only (its phase is not used)
@@ -770,10 +805,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int iu_lo = (ni == 4) ? (qe >> 1) : 0;
         const int iu_hi = (ni == 4) ? (qe >> 1) + 1 : 2;
         const uint32_t acc_off = (uint32_t)((ni == 4 ? 2 * ig + (qe >> 1) : ig) * BM);
-        const uint32_t slot_cnt = (uint32_t)(kTeamWarps + part_issuers(ni, np)) * 32u;
+        const uint32_t slot_cnt =
+            (uint32_t)(kTeamWarps + part_issuers(ni, np) + (b_waiter ? 1 : 0)) * 32u;
         Ring a(n_a), bq(n_b);
+        Ring acc((uint32_t)nbuf);  // accumulator buffer and its lap parity, per piece
         uint32_t next_team = (uint32_t)(n_a % kTeams);  // team of stage (CTA stage + n_a)
-        uint32_t c = 0;
         bool ok = true;
         bool range_bad = false;  // a SwiGLU value saturated (helping issuers)
         auto phase = [&](auto kc) {
@@ -810,12 +846,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (issuer) {
                     const uint32_t idesc =
                         idesc_f16_m128(nr <= 16 ? 16u : (uint32_t)((nr + 15) & ~15));
-                    const uint32_t buf = c % (uint32_t)nbuf;
+                    const uint32_t buf = acc.idx;
                     const uint32_t acc_col = tmem + buf * acc_buf_cols + acc_off;
                     bool fresh = true;
                     if (ok)
-                        ok = warp_wait(bar_acc_empty + 8 * buf, ((c / nbuf) & 1) ^ 1, abort_flag,
-                                       p.err, 32);
+                        ok = warp_wait(bar_acc_empty + 8 * buf, acc.ph ^ 1, abort_flag, p.err, 32);
+                    if (b_waiter) {
+                        // Narrow blocks: one part and this issuer's unit(s) of slab
+                        // ig, in straight-line code; warp 1 has seen the B slot
+                        // land when the barrier completes.
+#pragma unroll 1
+                        for (int j = kb0; j < kb1; ++j, a.next(), bq.next(),
+                                 next_team = (next_team + 1 == (uint32_t)kTeams) ? 0u
+                                                                                : next_team + 1) {
+                            const int nsub = stage_subs(j, kss);
+                            const uint32_t a_st = tmem + col_a + a.idx * kACols + ig * 32;
+                            const uint32_t bsm = b_ring + bq.idx * p.b_stage_bytes;
+                            const uint32_t rel_a = bar_a_free + 8 * next_team;  // np = 1
+                            const uint32_t rel_b = bar_b_empty + 8 * bq.idx;
+                            named_bar_sync(kBarSlot0 + a.idx, slot_cnt);  // A written, B landed
+                            tc_fence_after();
+                            for (int uu = iu_lo; uu < iu_hi; ++uu) {
+                                const bool last_u = (uu == iu_hi - 1);
+                                const uint32_t sub = (kind == 1) ? (uint32_t)uu
+                                                                 : (uint32_t)(kb_per_sub * uu + ig);
+                                const uint32_t r1 = last_u ? rel_a : 0u, r2 = last_u ? rel_b : 0u;
+                                if (ok && uu < nsub) {
+                                    mma_ts_f16_k64_commit(
+                                        acc_col, a_st + uu * 64,
+                                        smem_desc_sw128(bsm + sub * (uint32_t)(BM * 128)), idesc,
+                                        fresh ? 0u : 1u, r1, r2);
+                                    fresh = false;
+                                } else {
+                                    tc_commit2_elect(r1, r2);
+                                }
+                            }
+                        }
+                    } else
                     for (int j = kb0; j < kb1; ++j, a.next(),
                              next_team = (next_team + 1 == (uint32_t)kTeams) ? 0u : next_team + 1) {
                         const int nsub = stage_subs(j, kss);
@@ -874,9 +941,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kHelp) {
                     // the upper half of a full piece's columns; every issuing warp
                     // arrives on acc_empty once per piece (full or not)
-                    const uint32_t buf = c % (uint32_t)nbuf;
-                    const bool got = warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag,
-                                               p.err, 32);
+                    const uint32_t buf = acc.idx;
+                    const bool got = warp_wait(bar_acc_full + 8 * buf, acc.ph, abort_flag, p.err, 32);
                     if (got) {
                         tc_fence_after();
                         if (kb0 == 0 && kb1 == G.KS) {
@@ -893,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) mbar_arrive(bar_acc_empty + 8 * buf);
                     }
                 }
-                ++c;
+                acc.next();
             }
         };
         if (kKind0 == 1) phase(KindC<1>{});
@@ -911,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = wid & 3;
         const int row = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        uint32_t c = 0;
+        Ring acc((uint32_t)nbuf);  // accumulator buffer and its lap parity, per piece
         bool ok = true;
         bool range_bad = false;  // a SwiGLU value saturated
         if (!kFused) pdl_wait();  // counters, partial slots and the accumulator (see above)
@@ -927,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = tile / G.RT, r = tile % G.RT;
                 const int pos0 = b * BM;
                 const int nr = block_rows(p.sorted_ids, pos0, BM, p.P);
-                const uint32_t buf = c % (uint32_t)nbuf;
+                const uint32_t buf = acc.idx;
                 if (kind == 2) {
                     // The combine needs each column's token and routing weight: look
                     // them up once per block (these loads overlap the wait for the
@@ -943,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool u1 = !(kb1 - kb0 == 1 && stage_subs(kb0, G.KSS) == 1);
                 bool got =
-                    ok && warp_wait(bar_acc_full + 8 * buf, (c / nbuf) & 1, abort_flag, p.err, 32);
+                    ok && warp_wait(bar_acc_full + 8 * buf, acc.ph, abort_flag, p.err, 32);
                 if (kind == 2 && !zero_seen && got) {
                     // the combine adds into rows that every CTA zeroed its share of
                     got = wait_counter(p.prep_done, (int)gridDim.x, abort_flag, p.err);
@@ -1132,7 +1198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         named_bar_sync(kBarEpi, 128);
                     }
                 }
-                ++c;
+                acc.next();
             }
         };
         if (kKind0 == 1) phase(KindC<1>{});
@@ -1166,11 +1232,19 @@ bool plan_gemm_smem(int kind, GemmParams &p) {
         // stages first, then more issuers, then more buffers -- four issuers
         // with three A stages (two buffers, else one: measured faster at 32-row
         // blocks than two buffers with two A stages), then two A stages (four
-        // issuers with one buffer measured faster at 64-row blocks than two with
-        // two), then two issuers.  With one buffer the issuers wait for the
-        // epilogue at every piece end.
+        // issuers with one buffer measured faster at 64-row gate/up blocks than
+        // two with two), then two issuers.  With one buffer the issuers wait for
+        // the epilogue at every piece end, which the down GEMM's short pieces
+        // (eight stages, an epilogue of atomics) feel most: there two issuers
+        // with two buffers come first (2 % faster at 64-row blocks).
         p.ni = 0;
-        const int opts[6][3] = {{4, 2, 3}, {4, 1, 3}, {4, 2, 2}, {4, 1, 2}, {2, 2, 2}, {2, 1, 2}};
+        int opts[6][3] = {{4, 2, 3}, {4, 1, 3}, {4, 2, 2}, {4, 1, 2}, {2, 2, 2}, {2, 1, 2}};
+        if (kind == 2) {
+            opts[3][0] = 2;  // {2, 2, 2} before {4, 1, 2}
+            opts[3][1] = 2;
+            opts[4][0] = 4;
+            opts[4][1] = 1;
+        }
         for (int o = 0; o < 6 && !p.ni; ++o)
             if (opts[o][0] * opts[o][1] * BM + opts[o][2] * (int)kACols <= kTmemCols) {
                 p.ni = opts[o][0];
