@@ -82,8 +82,9 @@ constexpr uint32_t kACols = 128;                // TMEM columns per A stage
 // up, so each is used only where every participant is certain to arrive (see
 // the dequant role for the A-slot hand-off).
 constexpr uint32_t kBarEpi = 1;     // the four epilogue warps
-constexpr uint32_t kBarSlot0 = 2;   // A stage s written: all dequant warps arrive, issuers wait
-                                    // (ids 2..4: one per A stage or stage half)
+constexpr uint32_t kBarSlot0 = 2;   // A stage s written: its team arrives; the issuers and
+                                    // (narrow blocks) warp 1 wait (ids 2..4: one per A
+                                    // stage or stage half)
 constexpr uint32_t kBarPrep = 5;    // fused kernel: the gather and zeroing warps (1, 4..23)
 constexpr uint32_t kGatherWarps = 20;  // fused kernel: warps 4..23 gather before their roles
 constexpr uint32_t kPrepThreads = (1 + kGatherWarps) * 32;
