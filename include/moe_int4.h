@@ -388,6 +388,30 @@ int moe_int4_profile_read(float *ms);
 /* Number of kernel launches the last moe_int4_forward made on this thread. */
 int moe_int4_last_launch_count(void);
 
+/*
+ * Expert-parallel row movement ("From PCIe to NVLink", section "Part I: Laying
+ * the Foundation": the experts sharded over the GPUs).  Around the all-to-all
+ * exchanges of an expert-parallel layer, a rank gathers the x rows of the pairs
+ * it sends, and adds the expert outputs that come back into its tokens' rows.
+ * Both are stream-ordered, allocate nothing and do not synchronise.
+ *
+ * moe_ep_gather: dst[i][:] = src[rows[i]][:] for i < n, rows of H 2-byte
+ *   elements (bf16 bits; H a multiple of 8).  src is [src_rows][H]; a row index
+ *   outside [0, src_rows) zeroes dst[i] and sets bit 0 of *bad (device uint32;
+ *   may be NULL).  src and dst 16-byte aligned.
+ * moe_ep_combine: out[rows[i]][:] += src[i][:] for i < n, fp32 rows of H
+ *   elements (H a multiple of 4); out is [out_rows][H], rows may repeat (the adds
+ *   are atomic, so their order, and the last bits of a sum, may vary).  A row
+ *   index outside [0, out_rows) is dropped and sets bit 0 of *bad.  src and out
+ *   16-byte aligned.
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_CUDA.  n = 0 is a
+ * no-op.
+ */
+int moe_ep_gather(const uint16_t *src, int src_rows, const int32_t *rows, int n, int H,
+                  uint16_t *dst, uint32_t *bad, moe_stream_t stream);
+int moe_ep_combine(const float *src, const int32_t *rows, int n, int H, float *out,
+                   int out_rows, uint32_t *bad, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

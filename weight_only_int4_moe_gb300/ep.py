@@ -17,8 +17,12 @@ tokens.  One call:
 
 The collectives are torch.distributed's all_to_all_single (NCCL between GPUs,
 gloo on the host).  `local_forward` computes step 3: on the GPU, the library's
-forward on the rank's own packed experts (`gpu_local_forward`).  Ids outside
-[0, E) are dropped, as in the single-GPU layer.
+forward on the rank's own packed experts (`gpu_local_forward`).  On CUDA tensors
+the row movement of steps 2 and 4 runs in the library's kernels
+(`moe_ep_gather`: the x row of every sent pair; `moe_ep_combine`: the returned
+rows added into their tokens' output rows); torch indexes only the per-pair
+routing weights.  Host tensors (the gloo path) use torch's indexing for the
+same two steps.  Ids outside [0, E) are dropped, as in the single-GPU layer.
 """
 from __future__ import annotations
 
@@ -76,7 +80,11 @@ def dispatch(plan: DispatchPlan, x: torch.Tensor, topk_weights: torch.Tensor, gr
     recv_counts = exchange_counts(plan.send_counts, dev, group)
     R = int(recv_counts.sum())
     tok = torch.as_tensor(plan.send_tokens, device=dev)
-    send_x = x.index_select(0, tok)
+    if x.is_cuda and x.element_size() == 2:
+        from . import ops
+        send_x = ops.moe_ep_gather(x, tok)
+    else:
+        send_x = x.index_select(0, tok)
     send_ids = torch.as_tensor(plan.local_ids, device=dev)
     send_w = topk_weights.reshape(-1).index_select(0, torch.as_tensor(plan.send_pairs, device=dev))
     # 2-byte rows (bf16 x) travel as int32 pairs: not every backend moves 16-bit
@@ -96,7 +104,12 @@ def combine(plan: DispatchPlan, rows_out: torch.Tensor, recv_counts, group) -> t
     token's pairs: out [M, H]."""
     back = _a2a(len(plan.send_pairs), rows_out, recv_counts, plan.send_counts, group)
     out = torch.zeros((plan.M, rows_out.shape[1]), dtype=rows_out.dtype, device=rows_out.device)
-    out.index_add_(0, torch.as_tensor(plan.send_tokens, device=rows_out.device), back)
+    tok = torch.as_tensor(plan.send_tokens, device=rows_out.device)
+    if back.is_cuda and back.dtype == torch.float32:
+        from . import ops
+        ops.moe_ep_combine(back, tok, out)
+    else:
+        out.index_add_(0, tok, back)
     return out
 
 

@@ -37,6 +37,7 @@ EXPORTED = [
     "moe_int4_forward_host", "moe_int4_get_errors", "moe_int4_clear_errors",
     "moe_int4_strerror", "moe_int4_profile_enable", "moe_int4_profile_read",
     "moe_int4_last_launch_count", "moe_align_noalloc", "moe_route", "moe_int4_forward_routed",
+    "moe_ep_gather", "moe_ep_combine",
 ]
 
 
@@ -104,6 +105,8 @@ def load_library(build_if_missing: bool = True):
             "moe_align_noalloc": ([p, i, i, i, i, p, p, p, p, p], i),
             "moe_route": ([p, i, i, i, p, p, p], i),
             "moe_int4_forward_routed": ([p] * 9 + [i, sp, p, sz, p], i),
+            "moe_ep_gather": ([p, i, p, i, i, p, p, p], i),
+            "moe_ep_combine": ([p, p, i, i, p, i, p, p], i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -316,6 +319,48 @@ def moe_route(router_logits: torch.Tensor, top_k: int, stream=None):
         _check(load_library().moe_route(_dptr(router_logits), M, E, top_k, _dptr(ids), _dptr(w),
                                         _stream(stream)), "moe_route")
     return ids, w
+
+
+def moe_ep_gather(src: torch.Tensor, rows: torch.Tensor, out=None, bad=None, stream=None):
+    """out[i] = src[rows[i]] for a 2-byte [R, H] tensor and int32 row indices
+    (expert-parallel dispatch).  bad: optional device uint32 word, bit 0 set for
+    an index outside [0, R) (that row of out is zeroed)."""
+    if src.element_size() != 2 or src.dim() != 2:
+        raise ValueError("moe_ep_gather: expected a 2-D tensor of 2-byte elements")
+    src = src.contiguous()
+    rows = rows.to(torch.int32).contiguous()
+    n, H = rows.numel(), src.shape[1]
+    if out is None:
+        out = torch.empty((n, H), dtype=src.dtype, device=src.device)
+    with _on(src, rows, out):
+        _check(load_library().moe_ep_gather(_dptr(src), src.shape[0], _dptr(rows) if n else None,
+                                            n, H, _dptr(out) if n else None,
+                                            _dptr(bad) if bad is not None else None,
+                                            _stream(stream)), "moe_ep_gather")
+    return out
+
+
+def moe_ep_combine(src: torch.Tensor, rows: torch.Tensor, out: torch.Tensor, bad=None,
+                   stream=None):
+    """out[rows[i]] += src[i] for fp32 [n, H] rows (expert-parallel combine);
+    rows may repeat.  bad: optional device uint32 word, bit 0 set for an index
+    outside [0, out rows) (that row is dropped)."""
+    if src.dtype != torch.float32 or out.dtype != torch.float32:
+        raise ValueError("moe_ep_combine: expected fp32 rows")
+    src = src.contiguous()
+    rows = rows.to(torch.int32).contiguous()
+    n, H = rows.numel(), out.shape[1]
+    if n and tuple(src.shape) != (n, H):
+        raise ValueError("moe_ep_combine: src must be [len(rows), H]")
+    if not out.is_contiguous():
+        raise ValueError("moe_ep_combine: out must be contiguous")
+    with _on(src, rows, out):
+        _check(load_library().moe_ep_combine(_dptr(src) if n else None,
+                                             _dptr(rows) if n else None, n, H, _dptr(out),
+                                             out.shape[0],
+                                             _dptr(bad) if bad is not None else None,
+                                             _stream(stream)), "moe_ep_combine")
+    return out
 
 
 def moe_int4_forward_routed(x, w13, w13_scales, w2, w2_scales, router_logits, shape: Shape,
