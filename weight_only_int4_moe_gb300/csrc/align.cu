@@ -80,13 +80,19 @@ __device__ void align_layout(const AlignArgs &a, const int *cnt, int *off, int *
 }
 
 // Place the pairs of items [i0, i0 + 1024) using per-expert running bases
-// base[e] (shared, advanced on return).  wtab: shared [32][E] ints.
-__device__ void align_place_round(const AlignArgs &a, int i0, int *base, int *wtab) {
+// base[e] (shared, advanced on return).  wtab: shared [32][E] ints.  e_pre >= -1:
+// this thread's item's id, already read (-2: read it here).  Only the warps
+// that hold items take part in the per-expert running sums (one warp at a
+// handful of pairs, where walking all 32 was most of the round).
+__device__ void align_place_round(const AlignArgs &a, int i0, int *base, int *wtab,
+                                  int e_pre = -2) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int idx = threadIdx.x; idx < kAlignWarps * a.E; idx += kAlignThreads) wtab[idx] = 0;
+    const int items = (a.P - i0 < kAlignThreads) ? a.P - i0 : kAlignThreads;
+    const int nw = (items + 31) / 32;  // warps with items
+    for (int idx = threadIdx.x; idx < nw * a.E; idx += kAlignThreads) wtab[idx] = 0;
     __syncthreads();
     const int i = i0 + threadIdx.x;
-    const int e = (i < a.P) ? a.ids[i] : -1;
+    const int e = (e_pre >= -1) ? e_pre : (i < a.P) ? a.ids[i] : -1;
     const bool valid = (e >= 0) && (e < a.E);
     const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
     const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -94,7 +100,7 @@ __device__ void align_place_round(const AlignArgs &a, int i0, int *base, int *wt
     __syncthreads();
     for (int ee = threadIdx.x; ee < a.E; ee += kAlignThreads) {
         int acc = base[ee];
-        for (int w = 0; w < kAlignWarps; ++w) {
+        for (int w = 0; w < nw; ++w) {
             const int t = wtab[w * a.E + ee];
             wtab[w * a.E + ee] = acc;
             acc += t;
@@ -176,14 +182,17 @@ __device__ void align_one_block(const AlignArgs &a, int *sm) {
     int *wtab = scan_tmp + 64;        // [32][E]
     for (int e = threadIdx.x; e < a.E; e += kAlignThreads) cnt[e] = 0;
     __syncthreads();
+    int e_first = -1;  // this thread's id in the first round, kept for the placement
     for (int i = threadIdx.x; i < a.P; i += kAlignThreads) {
         const int e = a.ids[i];
+        if (i == (int)threadIdx.x) e_first = e;
         if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
     align_layout(a, cnt, base, scan_tmp);
     __syncthreads();
-    for (int i0 = 0; i0 < a.P; i0 += kAlignThreads) align_place_round(a, i0, base, wtab);
+    for (int i0 = 0; i0 < a.P; i0 += kAlignThreads)
+        align_place_round(a, i0, base, wtab, i0 == 0 ? e_first : -2);
 }
 
 // Whole align in one block (P small); blocks 1.. zero the accumulators.
