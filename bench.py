@@ -118,6 +118,8 @@ def kernel_traffic(kernel, workload, bytes_per_launch):
         d = json.load(f)
     if kernel_source_hash() != d.get("kernel_source_sha256"):
         return None, "kernel changed since the ncu capture"
+    if d.get("traffic_per_algorithmic_byte") is None:  # no single ratio applies
+        return None, d.get("reason", "no single traffic ratio for this workload")
     ratio = float(d["traffic_per_algorithmic_byte"])
     return ratio * bytes_per_launch, (f"ncu dram bytes of {d['captured_case']}: "
                                       f"{ratio:.4f} x algorithmic bytes, scaled")
