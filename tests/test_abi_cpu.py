@@ -181,3 +181,21 @@ def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
     assert int(out[4]) == 0          # M == 0: a no-op
     assert int(out[5]) == 0          # a rejected shape needs no workspace
     assert out[6] == ops.moe_int4_strerror(-2)
+
+
+def test_ep_row_kernels_check_arguments_on_the_host():
+    """moe_ep_gather / moe_ep_combine reject bad arguments before any launch
+    (no GPU needed) and treat n = 0 as a no-op."""
+    lib = ops.load_library()
+    s = None
+    err_null, err_shape, err_align = -1, -2, -3  # MOE_ERR_NULL, _SHAPE, _ALIGN
+    assert lib.moe_ep_gather(None, 4, None, 0, 64, None, None, s) == ops.MOE_OK
+    assert lib.moe_ep_combine(None, None, 0, 64, None, 4, None, s) == ops.MOE_OK
+    fake = ctypes.c_void_p(16)  # never dereferenced: the checks fail first
+    assert lib.moe_ep_gather(None, 4, fake, 3, 64, fake, None, s) == err_null
+    assert lib.moe_ep_gather(fake, 4, fake, 3, 60, fake, None, s) == err_shape
+    assert lib.moe_ep_gather(fake, 4, fake, -1, 64, fake, None, s) == err_shape
+    assert lib.moe_ep_gather(ctypes.c_void_p(24), 4, fake, 3, 64, fake, None, s) == err_align
+    assert lib.moe_ep_combine(fake, None, 3, 64, fake, 4, None, s) == err_null
+    assert lib.moe_ep_combine(fake, fake, 3, 66, fake, 4, None, s) == err_shape
+    assert lib.moe_ep_combine(fake, fake, 3, 64, ctypes.c_void_p(40), 4, None, s) == err_align
