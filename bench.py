@@ -88,7 +88,7 @@ def make_weights(cfg, fmt):
     return inputs.make_weights(cfg.E, cfg.H, cfg.I, cfg.weight_seed)
 
 
-GEMM_SOURCES = ("gemm.cu", "kernels.cuh", "common.cuh")
+GEMM_SOURCES = ("gemm.cu", "dequant.cuh", "kernels.cuh", "common.cuh")
 
 
 def kernel_source_hash():
@@ -402,7 +402,8 @@ class Workload:
             ev1.synchronize()
             rec.append({"M": M, "ms": ev0.elapsed_time(ev1), "stages": stages,
                         "touched": n_touched, "launches": launches,
-                        "fused": ops.moe_int4_fused(M, shape)})
+                        "fused": ops.moe_int4_fused(M, shape),
+                        "gemv": ops.moe_int4_gemv(M, shape)})
 
     def profiled(self, steps, first, stream):
         """The same calls again with CUDA events between the kernels, on the
@@ -433,6 +434,7 @@ class Workload:
             t_tc = flops / (tc_peak * 1e12) * 1e6
             st = np.mean([r["stages"] for r in prec if r["M"] == M], axis=0)
             fused = all(r["fused"] for r in rs)
+            gemv = all(r["gemv"] for r in rs)
             out[str(M)] = {
                 "us_per_call": t_med, "us_mean": statistics.mean(us), "calls": len(us),
                 "tokens_per_s": M / (t_med / 1e6),
@@ -445,8 +447,10 @@ class Workload:
                 "ideal_us": {"hbm": t_hbm, "tensor": t_tc},
                 "bound": "hbm" if t_hbm >= t_tc else "tensor",
                 "roofline_frac": max(t_hbm, t_tc) / t_med,
-                "kernels": "fused" if fused else "separate",
-                "stage_us": ({"align": st[0] * 1e3, "fused": st[1] * 1e3, "finalize": st[3] * 1e3}
+                "kernels": "gemv" if gemv else ("fused" if fused else "separate"),
+                "stage_us": ({"route": st[0] * 1e3, "gate_up": st[1] * 1e3, "down": st[2] * 1e3,
+                              "finalize": st[3] * 1e3} if gemv else
+                             {"align": st[0] * 1e3, "fused": st[1] * 1e3, "finalize": st[3] * 1e3}
                              if fused else
                              {"align+gather": st[0] * 1e3, "gate_up": st[1] * 1e3,
                               "down": st[2] * 1e3, "finalize": st[3] * 1e3}),

@@ -90,8 +90,11 @@ enum {
 #define MOE_W_MXFP4 1
 
 /* Forward flags (moe_int4_shape.flags). */
-#define MOE_FLAG_UNFUSED 0x1 /* run the gather, gate/up and down steps as separate kernels
-                                even where the fused decode kernel applies (same results) */
+#define MOE_FLAG_UNFUSED 0x1 /* run the gather, gate/up and down steps as separate
+                                tensor-core kernels even where the fused decode kernel or
+                                the small-batch path applies (same results) */
+#define MOE_FLAG_NO_GEMV 0x2 /* keep to the tensor-core kernels (fused where it applies)
+                                where the small-batch matrix-vector path would run */
 
 /* Layer shape.  Supported: 1 <= E <= 1024, 1 <= top_k <= min(E, 32),
  * hidden % 128 == 0, inter % 128 == 0, group == 32, weight_format one of
@@ -265,6 +268,10 @@ int moe_int4_block_m(int M, const moe_int4_shape *shape);
  * kernels (or M or the shape is invalid). */
 int moe_int4_fused(int M, const moe_int4_shape *shape);
 
+/* 1 if a forward of M tokens runs the small-batch path (the expert MLP as
+ * matrix-vector products on the CUDA cores; see moe_int4_forward), 0 otherwise. */
+int moe_int4_gemv(int M, const moe_int4_shape *shape);
+
 /*
  * moe_int4_workspace_layout: byte offsets inside the workspace of a forward of
  * M tokens, for inspecting a finished call: offsets[0] error words (uint32 flags,
@@ -294,12 +301,18 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
  *   them (moe_int4_clear_errors) once after allocating the workspace.
  * M == 0 returns MOE_OK without touching out.  Every pointer must be 16-byte
  * aligned.  The call launches only kernels (no host sync, no allocation).
- * Launch plan: the align kernel, then, for routings of at most 512 pairs
- * (decode batches), one persistent kernel that gathers x, runs the gate/up
- * GEMM and then the down GEMM (its CTAs hand work to each other through
- * counters in the workspace, with bounded waits; it expects to get every SM
- * within about two seconds); otherwise a gather kernel and one kernel per
- * GEMM.  bf16 output adds a conversion kernel.
+ * Launch plan: for routings of at most 64 pairs that read at most 128 Mi weights
+ * (pairs x 3 x hidden x inter: a few tokens on small experts), two
+ * matrix-vector kernels on the CUDA cores, gate/up + SwiGLU and then down +
+ * combine, each routed pair reading its token's row and its expert's packed
+ * weights directly (no align).  Otherwise the align kernel, then, for routings
+ * of at most 512 pairs (decode batches), one persistent tensor-core kernel that
+ * gathers x, runs the gate/up GEMM and then the down GEMM (its CTAs hand work to
+ * each other through counters in the workspace, with bounded waits; it expects
+ * to get every SM within about two seconds); otherwise a gather kernel and one
+ * kernel per GEMM.  All plans form the same fp16 weights and intermediates and
+ * accumulate in fp32; they differ only in summation order.  bf16 output adds a
+ * conversion kernel.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,
  *   MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
  */

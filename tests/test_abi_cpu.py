@@ -34,7 +34,7 @@ def test_header_constants_match_the_binding():
                            flags=re.M))
     for name in ("MOE_DEVERR_BAD_EXPERT_ID", "MOE_DEVERR_TIMEOUT", "MOE_DEVERR_BOUNDS",
                  "MOE_DEVERR_RANGE", "MOE_OUT_BF16", "MOE_OUT_F32", "MOE_W_INT4", "MOE_W_MXFP4",
-                 "MOE_WS_HOST_IO", "MOE_FLAG_UNFUSED"):
+                 "MOE_WS_HOST_IO", "MOE_FLAG_UNFUSED", "MOE_FLAG_NO_GEMV"):
         assert int(defs[name], 0) == getattr(ops, name), name
     flags = [int(v, 0) for k, v in defs.items() if k.startswith("MOE_DEVERR_")]
     assert all(f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)

@@ -70,32 +70,77 @@ def with_flags(pw, flags):
     return b
 
 
-@pytest.mark.parametrize("plan", ["default", "unfused"])
+@pytest.mark.parametrize("plan", ["default", "tensor", "unfused"])
 @pytest.mark.parametrize("E,k,H,I,M,seed", SMALL)
 def test_forward_matches_oracle(E, k, H, I, M, seed, plan):
-    """Every shape through the default launch plan (the fused decode kernel
-    where it applies) and through the separate kernels."""
+    """Every shape through the default launch plan (the small-batch kernels or
+    the fused decode kernel where they apply), the tensor-core kernels only
+    (MOE_FLAG_NO_GEMV) and the separate kernels."""
     ops = _ops()
     w, pw, t = setup(E, k, H, I, M, seed)
+    if plan == "tensor":
+        pw = with_flags(pw, ops.MOE_FLAG_NO_GEMV)
+        assert not ops.moe_int4_gemv(M, pw.shape)
     if plan == "unfused":
         pw = with_flags(pw, ops.MOE_FLAG_UNFUSED)
-        assert not ops.moe_int4_fused(M, pw.shape)
+        assert not ops.moe_int4_fused(M, pw.shape) and not ops.moe_int4_gemv(M, pw.shape)
     got = gpu_forward(pw, t)
     ref = oracle_out(w, t)
     m = assert_parity(got, ref, f"E{E} k{k} H{H} I{I} M{M} {plan}")
-    print(plan, ops.moe_int4_fused(M, pw.shape), m)
+    print(plan, ops.moe_int4_gemv(M, pw.shape), ops.moe_int4_fused(M, pw.shape), m)
+
+
+# the small-batch kernels: ragged row-tile groups (I / 128 and H / 128 not
+# multiples of 4), one to many k splits, top-1 to top-8, up to the 64-pair limit
+GEMV = [
+    (16, 4, 384, 256, 3, 40),     # 2 gate/up row tiles, 3 down row tiles
+    (32, 8, 1280, 384, 1, 41),    # 3 gate/up tiles, 10 down tiles (ragged groups)
+    (64, 8, 512, 256, 8, 42),     # 64 pairs: the limit
+    (8, 1, 2048, 512, 7, 43),     # top-1
+    (48, 8, 2048, 1024, 2, 44),   # 16 pairs, about 100 M weights: near the size limit
+]
+
+
+@pytest.mark.parametrize("E,k,H,I,M,seed", GEMV)
+def test_small_batch_kernels_match_oracle(E, k, H, I, M, seed):
+    ops = _ops()
+    w, pw, t = setup(E, k, H, I, M, seed)
+    assert ops.moe_int4_gemv(M, pw.shape)
+    got = gpu_forward(pw, t)
+    ref = oracle_out(w, t)
+    print(assert_parity(got, ref, f"gemv E{E} k{k} H{H} I{I} M{M}"))
+
+
+def test_small_batch_kernels_match_the_tensor_path_closely():
+    """Both paths form the same fp16 weights and intermediates and sum exact
+    products in fp32, so they differ only by summation order: far below the
+    oracle bound."""
+    ops = _ops()
+    w, pw, t = setup(32, 8, 1024, 384, 4, 45)
+    a = gpu_forward(pw, t)
+    b = gpu_forward(with_flags(pw, ops.MOE_FLAG_NO_GEMV), t)
+    rms = float(np.sqrt(np.mean(b.astype(np.float64) ** 2)))
+    assert np.abs(a.astype(np.float64) - b).max() <= 1e-3 * rms
 
 
 def test_fused_plan_covers_the_decode_shapes():
-    """Which forwards run the fused decode kernel: routings of up to 512 pairs
-    (the measured crossover) in blocks of up to 128 rows."""
+    """Which forwards run which plan (the measured crossovers): the small-batch
+    kernels up to 64 pairs and 128 Mi weights read, the fused decode kernel up
+    to 512 pairs in blocks of up to 128 rows, the separate kernels beyond."""
     ops = _ops()
     k26 = ops.Shape.of(384, 8, 7168, 2048)
-    assert [ops.moe_int4_fused(M, k26) for M in (1, 9, 64, 65, 90, 1024)] == [
-        True, True, True, False, False, False]
+    Ms = (1, 8, 9, 64, 65, 90, 1024)
+    assert not any(ops.moe_int4_gemv(M, k26) for M in Ms)  # 352 M weights per token
+    assert [ops.moe_int4_fused(M, k26) for M in Ms] == [True, True, True, True, False, False,
+                                                        False]
     mid = ops.Shape.of(64, 6, 4096, 1408)
-    assert [ops.moe_int4_fused(M, mid) for M in (1, 32, 128, 2048, 8192)] == [True, True, False,
+    assert [ops.moe_int4_gemv(M, mid) for M in (1, 2, 32)] == [True, False, False]
+    assert [ops.moe_int4_fused(M, mid) for M in (1, 32, 128, 2048, 8192)] == [False, True, False,
                                                                               False, False]
+    no_gemv = ops.Shape.of(64, 6, 4096, 1408, flags=ops.MOE_FLAG_NO_GEMV)
+    assert ops.moe_int4_fused(1, no_gemv) and not ops.moe_int4_gemv(1, no_gemv)
+    tiny = ops.Shape.of(8, 2, 256, 128)
+    assert ops.moe_int4_gemv(16, tiny) and not ops.moe_int4_gemv(33, tiny)  # 66 pairs
     assert ops.moe_int4_fused(64, ops.Shape.of(64, 8, 256, 128))  # 512 pairs, block 32
     assert not ops.moe_int4_fused(512, ops.Shape.of(3, 1, 256, 128))  # 512 pairs, block 192
     assert not ops.moe_int4_fused(1, ops.Shape.of(384, 8, 7168, 2048,

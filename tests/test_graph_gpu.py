@@ -47,6 +47,7 @@ def _capture(fn):
 
 
 @pytest.mark.parametrize("E,k,H,I,M,routing", [
+    (16, 4, 384, 256, 5, "uniform"),      # 20 pairs: the small-batch kernels
     (16, 4, 384, 256, 37, "uniform"),     # ragged M, single-block align
     (64, 6, 512, 256, 700, "skewed"),     # multi-block align, skewed routing
     (8, 2, 512, 256, 1000, "uniform"),    # wide blocks of 192 rows

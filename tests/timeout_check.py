@@ -59,7 +59,7 @@ def main():
     assert ops.debug_bounds(), "run with MOE_INT4_DEBUG_BOUNDS=1"
     ops.load_library()
     assert ops.library_path() == build.DEBUG_LIB
-    run(0, "fused decode kernel")
+    run(ops.MOE_FLAG_NO_GEMV, "fused decode kernel")
     run(ops.MOE_FLAG_UNFUSED, "separate kernels")
     print("timeouts: all cases reported and recovered", flush=True)
 

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <mutex>
+#include <utility>
 
 #include "moe_int4.h"
 #include "kernels.cuh"
@@ -25,6 +26,17 @@ constexpr int kSingleBlockAlignMax = 4096;
 // (K2.6 M = 90, verify M = 256 and 512, mid-size M = 128), where the separate
 // gather kernel copies the rows faster than the fused kernel's gather share.
 constexpr int kFusedMaxPairs = 512;
+// The small-batch matrix-vector kernels run where a call's weight reads are
+// small enough that the tensor-core kernels' fixed per-call latency dominates:
+// at most 64 pairs and at most this many weights (pairs x 3 x hidden x inter).
+// They spend about four instructions per weight on the CUDA cores, so their
+// time grows with the weights they read.  Same-box A/B: mid-size M = 1 (104 M
+// weights) 43.7 -> 33.4 us; K2.6 M = 1 (352 M) 69.3 -> 78.5 us, slower.
+constexpr int kGemvMaxPairs = 64;
+constexpr long long kGemvMaxWeights = 128ll << 20;
+// Their k splits: enough CTAs (16 warps each) for about two per SM of a GB300,
+// within a 48 KB shared-memory stage of the split's activations.
+constexpr int kGemvTargetCtas = 304;
 constexpr int kAlignChunk = 1024;
 
 thread_local int g_last_launches = 0;
@@ -41,7 +53,7 @@ int check_shape(const moe_int4_shape *sh) {
     if (sh->group != 32) return MOE_ERR_SHAPE;
     if (sh->out_dtype != MOE_OUT_BF16 && sh->out_dtype != MOE_OUT_F32) return MOE_ERR_SHAPE;
     if (sh->weight_format != MOE_W_INT4 && sh->weight_format != MOE_W_MXFP4) return MOE_ERR_SHAPE;
-    if (sh->flags & ~MOE_FLAG_UNFUSED) return MOE_ERR_SHAPE;
+    if (sh->flags & ~(MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) return MOE_ERR_SHAPE;
     return MOE_OK;
 }
 
@@ -73,9 +85,11 @@ int choose_block_m(long long P, int E) {
 struct Plan {
     int M, E, k, H, I, P, BM, RT1, RT2, n_chunks, out_f32;
     bool fused;  // the fused decode kernel (gather + gate/up + down in one launch)
+    bool gemv;   // the small-batch matrix-vector kernels
+    int SA, KBs, SB, KS2s;  // their k splits (gate/up over H, down over I)
     size_t cap, blocks_cap, tiles1_cap;
     size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_pos, off_cnt, off_partial, off_a,
-        off_x16, off_acc, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
+        off_x16, off_acc, off_gu, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
 };
 
 Plan make_plan(int M, const moe_int4_shape *sh) {
@@ -95,7 +109,24 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.cap = (size_t)p.P + touched * (size_t)(p.BM - 1);
     p.blocks_cap = p.cap / p.BM + 1;
     p.tiles1_cap = p.blocks_cap * p.RT1;
-    p.fused = !(sh->flags & MOE_FLAG_UNFUSED) && p.P <= kFusedMaxPairs && p.BM <= 128;
+    p.gemv = !(sh->flags & (MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) && p.P <= kGemvMaxPairs &&
+             (long long)p.P * 3 * p.H * p.I <= kGemvMaxWeights;
+    p.fused = !p.gemv && !(sh->flags & MOE_FLAG_UNFUSED) && p.P <= kFusedMaxPairs && p.BM <= 128;
+    if (p.gemv) {
+        auto splits = [&](int per_split_ctas, int n, int max_per) {  // (splits, per split)
+            int sp = (kGemvTargetCtas + per_split_ctas - 1) / per_split_ctas;
+            if (sp < (n + max_per - 1) / max_per) sp = (n + max_per - 1) / max_per;
+            if (sp > n) sp = n;
+            const int per = (n + sp - 1) / sp;
+            return std::make_pair((n + per - 1) / per, per);
+        };
+        const auto a = splits(p.P * ((p.RT1 + 3) / 4), p.H / 64, 192);   // 64-k blocks
+        const auto b = splits(p.P * ((p.RT2 + 3) / 4), p.I / 128, 96);   // 128-k stages
+        p.SA = a.first;
+        p.KBs = a.second;
+        p.SB = b.first;
+        p.KS2s = b.second;
+    }
     size_t o = 0;
     p.off_err = o; o += 256;
     p.off_npp = o; o += 256;
@@ -111,6 +142,7 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.off_a = o; o = rup(o + p.cap * (size_t)p.I * 2, 256);
     p.off_x16 = o; o = rup(o + p.cap * (size_t)p.H * 2, 256);  // x rows, bucketed, fp16
     p.off_acc = o; o = rup(o + (p.out_f32 ? 0 : (size_t)p.M * p.H * 4), 256);
+    p.off_gu = o; o = rup(o + (p.gemv ? (size_t)p.SA * p.P * 2 * p.I * 4 : 0), 256);
     p.total = o;
     p.off_io_x = o; o = rup(o + (size_t)p.M * p.H * 2, 256);
     p.off_io_ids = o; o = rup(o + (size_t)p.P * 4, 256);
@@ -292,6 +324,11 @@ int moe_int4_fused(int M, const moe_int4_shape *shape) {
     return make_plan(M, shape).fused ? 1 : 0;
 }
 
+int moe_int4_gemv(int M, const moe_int4_shape *shape) {
+    if (check_shape(shape) != MOE_OK || M < 1 || M > (1 << 20)) return 0;
+    return make_plan(M, shape).gemv ? 1 : 0;
+}
+
 int moe_int4_block_m(int M, const moe_int4_shape *shape) {
     if (check_shape(shape) != MOE_OK || M < 0) return 0;
     return choose_block_m((long long)M * shape->top_k, shape->E);
@@ -369,6 +406,59 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
         }
     }
     prof_record(0, s);
+
+    if (pl.gemv) {
+        // a few tokens: matrix-vector kernels on the CUDA cores, no align
+        if (router_logits) {
+            RouteArgs ra{};
+            ra.logits = router_logits;
+            ra.M = pl.M;
+            ra.E = pl.E;
+            ra.top_k = pl.k;
+            ra.ids = const_cast<int32_t *>(topk_ids);
+            ra.weights = const_cast<float *>(topk_weights);
+            if (launch_route(ra, sms, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        prof_record(1, s);
+        GemvArgs ga{};
+        ga.x = x;
+        ga.ids = topk_ids;
+        ga.topk_weights = topk_weights;
+        ga.w13 = reinterpret_cast<const uint8_t *>(w13_packed);
+        ga.s13 = reinterpret_cast<const uint8_t *>(w13_scales);
+        ga.w2 = reinterpret_cast<const uint8_t *>(w2_packed);
+        ga.s2 = reinterpret_cast<const uint8_t *>(w2_scales);
+        ga.gu = reinterpret_cast<float *>(ws + pl.off_gu);
+        ga.out = acc;
+        ga.out_n16 = (size_t)pl.M * pl.H / 4;
+        ga.err = err;
+        ga.M = pl.M;
+        ga.top_k = pl.k;
+        ga.P = pl.P;
+        ga.E = pl.E;
+        ga.H = pl.H;
+        ga.I = pl.I;
+        ga.RT1 = pl.RT1;
+        ga.KB = pl.H / 64;
+        ga.SA = pl.SA;
+        ga.KBs = pl.KBs;
+        ga.RT2 = pl.RT2;
+        ga.KS2 = pl.I / 128;
+        ga.SB = pl.SB;
+        ga.KS2s = pl.KS2s;
+        ga.fmt = shape->weight_format;
+        ga.dq = int4_dequant_consts();
+        if (launch_gemv(ga, 1, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+        prof_record(2, s);
+        if (launch_gemv(ga, 2, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+        prof_record(3, s);
+        if (!pl.out_f32 && launch_finalize(acc, reinterpret_cast<uint16_t *>(out),
+                                           (size_t)pl.M * pl.H, sms, s, &launches) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        prof_record(4, s);
+        g_last_launches = launches;
+        return MOE_OK;
+    }
 
     AlignArgs al{};
     al.ids = topk_ids;

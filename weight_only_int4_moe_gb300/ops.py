@@ -27,11 +27,12 @@ MOE_DEVERR_RANGE = 0x8
 MOE_W_INT4 = 0
 MOE_W_MXFP4 = 1
 MOE_FLAG_UNFUSED = 0x1
+MOE_FLAG_NO_GEMV = 0x2
 
 EXPORTED = [
     "moe_int4_packed_bytes", "moe_int4_packed_scale_bytes", "moe_int4_pack", "moe_mxfp4_pack",
     "moe_align_capacity", "moe_align_scratch_bytes", "moe_align",
-    "moe_int4_workspace_bytes", "moe_int4_block_m", "moe_int4_fused",
+    "moe_int4_workspace_bytes", "moe_int4_block_m", "moe_int4_fused", "moe_int4_gemv",
     "moe_int4_workspace_layout",
     "moe_int4_forward",
     "moe_int4_forward_host", "moe_int4_get_errors", "moe_int4_clear_errors",
@@ -92,6 +93,7 @@ def load_library(build_if_missing: bool = True):
             "moe_align": ([p, i, i, i, i, p, p, p, p, p, sz, p], i),
             "moe_int4_workspace_bytes": ([i, sp, i], sz),
             "moe_int4_fused": ([i, sp], i),
+            "moe_int4_gemv": ([i, sp], i),
             "moe_int4_block_m": ([i, sp], i),
             "moe_int4_workspace_layout": ([i, sp, p], i),
             "moe_int4_forward": ([p] * 8 + [i, sp, p, sz, p], i),
@@ -265,6 +267,12 @@ def moe_int4_fused(M: int, shape: Shape) -> bool:
     """Whether a forward of M tokens runs the fused decode kernel (the gather
     and both GEMMs in one launch)."""
     return load_library().moe_int4_fused(M, ctypes.byref(shape)) == 1
+
+
+def moe_int4_gemv(M: int, shape: Shape) -> bool:
+    """Whether a forward of M tokens runs the small-batch matrix-vector kernels
+    (a few tokens: the expert MLP on the CUDA cores, no align)."""
+    return load_library().moe_int4_gemv(M, ctypes.byref(shape)) == 1
 
 
 def moe_int4_block_m(M: int, shape: Shape) -> int:
