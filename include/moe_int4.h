@@ -269,7 +269,7 @@ int moe_int4_block_m(int M, const moe_int4_shape *shape);
 int moe_int4_fused(int M, const moe_int4_shape *shape);
 
 /* 1 if a forward of M tokens runs the small-batch path (the expert MLP as
- * matrix-vector products on the CUDA cores; see moe_int4_forward), 0 otherwise. */
+ * per-pair matrix-vector products; see moe_int4_forward), 0 otherwise. */
 int moe_int4_gemv(int M, const moe_int4_shape *shape);
 
 /*
@@ -301,16 +301,17 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
  *   them (moe_int4_clear_errors) once after allocating the workspace.
  * M == 0 returns MOE_OK without touching out.  Every pointer must be 16-byte
  * aligned.  The call launches only kernels (no host sync, no allocation).
- * Launch plan: for routings of at most 64 pairs that read at most 128 Mi weights
- * (pairs x 3 x hidden x inter: a few tokens on small experts), two
- * matrix-vector kernels on the CUDA cores, gate/up + SwiGLU and then down +
- * combine, each routed pair reading its token's row and its expert's packed
- * weights directly (no align).  Otherwise the align kernel, then, for routings
- * of at most 512 pairs (decode batches), one persistent tensor-core kernel that
- * gathers x, runs the gate/up GEMM and then the down GEMM (its CTAs hand work to
- * each other through counters in the workspace, with bounded waits; it expects
- * to get every SM within about two seconds); otherwise a gather kernel and one
- * kernel per GEMM.  All plans form the same fp16 weights and intermediates and
+ * Launch plan: where the pairs seldom share an expert (at most 64 pairs and at
+ * most 1.2 pairs per expert that a uniform routing of M tokens is expected to
+ * touch), or where all experts together fit in 64 MiB (at most 256 pairs), two
+ * matrix-vector kernels, gate/up + SwiGLU and then down + combine, each routed
+ * pair reading its token's row and its expert's packed weights directly (no
+ * align; a shared expert is read once per pair).  Otherwise the align kernel,
+ * then, for routings of at most 512 pairs (decode batches), one persistent
+ * tensor-core kernel that gathers x, runs the gate/up GEMM and then the down
+ * GEMM (its CTAs hand work to each other through counters in the workspace,
+ * with bounded waits; it expects to get every SM within about two seconds);
+ * otherwise a gather kernel and one kernel per GEMM.  All plans form the same fp16 weights and intermediates and
  * accumulate in fp32; they differ only in summation order.  bf16 output adds a
  * conversion kernel.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,

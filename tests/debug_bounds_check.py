@@ -31,10 +31,11 @@ CASES = [
 ]
 
 
-def run_case(E, k, H, I, M, routing, seed):
+def run_case(E, k, H, I, M, routing, seed, flags=0):
     import torch
     w = inputs.make_weights(E, H, I, 900 + seed)
     pw = ops.PackedWeights(w, E, H, I, k)
+    pw.shape = ops.Shape.of(E, k, H, I, flags=flags)
     t = inputs.make_tokens(inputs.MoEConfig("dbg", E, k, H, I, (M,), routing, 0, 950 + seed), M)
     x = torch.from_numpy(t["x"].view(np.int16)).cuda().view(torch.bfloat16)
     ids = torch.from_numpy(t["topk_ids"]).cuda()
@@ -47,18 +48,21 @@ def run_case(E, k, H, I, M, routing, seed):
     ref, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
                                 t["topk_weights"])
     m = assert_parity(out.cpu().numpy(), ref, f"E{E} M{M}")
-    print(f"E={E} k={k} H={H} I={I} M={M} block_m={ops.moe_int4_block_m(M, pw.shape)} "
+    plan = "small-batch" if ops.moe_int4_gemv(M, pw.shape) else (
+        f"block_m={ops.moe_int4_block_m(M, pw.shape)}")
+    print(f"E={E} k={k} H={H} I={I} M={M} {plan} "
           f"max/rms={m['max_over_rms']:.2e} rel_l1={m['rel_l1']:.2e}", flush=True)
     return w, pw
 
 
-def run_invalid_ids():
+def run_invalid_ids(flags):
     """Out-of-range ids are dropped and reported (MOE_DEVERR_BAD_EXPERT_ID);
     the bounds checks stay quiet."""
     import torch
     E, k, H, I, M = 16, 4, 384, 256, 37
     w = inputs.make_weights(E, H, I, 990)
     pw = ops.PackedWeights(w, E, H, I, k)
+    pw.shape = ops.Shape.of(E, k, H, I, flags=flags)
     t = inputs.make_tokens(inputs.MoEConfig("dbg", E, k, H, I, (M,), "uniform", 0, 991), M)
     bad = t["topk_ids"].copy()
     bad[::5, 1] = E + 2
@@ -74,14 +78,16 @@ def run_invalid_ids():
     ref, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], bad,
                                 t["topk_weights"])
     assert_parity(out.cpu().numpy(), ref, "invalid ids")
-    print(f"invalid ids: flags={flags:#x} dropped={dropped}", flush=True)
+    print(f"invalid ids (plan flags {pw.shape.flags:#x}): flags={flags:#x} dropped={dropped}",
+          flush=True)
 
 
-def run_routed():
+def run_routed(flags):
     import torch
     E, k, H, I, M = 32, 4, 384, 256, 29
     w = inputs.make_weights(E, H, I, 995)
     pw = ops.PackedWeights(w, E, H, I, k)
+    pw.shape = ops.Shape.of(E, k, H, I, flags=flags)
     rng = np.random.default_rng([9, 5])
     xb = inputs.bf16_bits_from_f32(rng.standard_normal((M, H), dtype=np.float32))
     lg = rng.standard_normal((M, E), dtype=np.float32)
@@ -125,10 +131,16 @@ def main():
     assert ops.debug_bounds(), "run with MOE_INT4_DEBUG_BOUNDS=1"
     ops.load_library()
     assert ops.library_path() == build.DEBUG_LIB
+    # every case through the tensor-core kernels, and through the small-batch
+    # kernels where the default plan picks them
     for i, case in enumerate(CASES):
-        run_case(*case, seed=i)
-    run_invalid_ids()
-    run_routed()
+        run_case(*case, seed=i, flags=ops.MOE_FLAG_NO_GEMV)
+        E, k, H, I, M, _ = case
+        if ops.moe_int4_gemv(M, ops.Shape.of(E, k, H, I)):
+            run_case(*case, seed=i)
+    for flags in (ops.MOE_FLAG_NO_GEMV, 0):
+        run_invalid_ids(flags)
+        run_routed(flags)
     run_mxfp4()
     print("debug-bounds: all cases clean", flush=True)
 

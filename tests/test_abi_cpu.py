@@ -199,3 +199,31 @@ def test_ep_row_kernels_check_arguments_on_the_host():
     assert lib.moe_ep_combine(fake, None, 3, 64, fake, 4, None, s) == err_null
     assert lib.moe_ep_combine(fake, fake, 3, 66, fake, 4, None, s) == err_shape
     assert lib.moe_ep_combine(fake, fake, 3, 64, ctypes.c_void_p(40), 4, None, s) == err_align
+
+
+def test_launch_plans():
+    """Which forwards run which plan (host logic; the measured crossovers): the
+    small-batch kernels up to 64 pairs and 1.2 pairs per expected touched
+    expert, or up to 256 pairs when all experts fit in half the L2; the fused
+    decode kernel up to 512 pairs in blocks of up to 128 rows; the separate
+    kernels beyond."""
+    k26 = ops.Shape.of(384, 8, 7168, 2048)
+    Ms = (1, 8, 9, 64, 65, 90, 1024)
+    # 8 of 384 experts per token: 64 pairs touch about 59.4 experts (1.08 per)
+    assert [ops.moe_int4_gemv(M, k26) for M in Ms] == [True, True] + [False] * 5
+    assert [ops.moe_int4_fused(M, k26) for M in Ms] == [False, False, True, True, False, False,
+                                                        False]
+    mid = ops.Shape.of(64, 6, 4096, 1408)
+    # M = 4: 24 pairs on about 20.8 experts (1.15); M = 5: 30 on 24.9 (1.20+)
+    assert [ops.moe_int4_gemv(M, mid) for M in (1, 4, 5, 32)] == [True, True, False, False]
+    assert [ops.moe_int4_fused(M, mid) for M in (1, 32, 128, 2048, 8192)] == [False, True, False,
+                                                                              False, False]
+    no_gemv = ops.Shape.of(64, 6, 4096, 1408, flags=ops.MOE_FLAG_NO_GEMV)
+    assert ops.moe_int4_fused(1, no_gemv) and not ops.moe_int4_gemv(1, no_gemv)
+    tiny = ops.Shape.of(8, 2, 256, 128)  # 8 experts of 55 KB: L2-resident
+    assert ops.moe_int4_gemv(128, tiny) and not ops.moe_int4_gemv(129, tiny)  # 256 pairs
+    assert ops.moe_int4_fused(129, tiny)
+    assert ops.moe_int4_fused(64, ops.Shape.of(64, 8, 256, 128))  # 512 pairs, block 32
+    assert not ops.moe_int4_fused(512, ops.Shape.of(3, 1, 256, 128))  # 512 pairs, block 192
+    unfused = ops.Shape.of(384, 8, 7168, 2048, flags=ops.MOE_FLAG_UNFUSED)
+    assert not ops.moe_int4_fused(1, unfused) and not ops.moe_int4_gemv(1, unfused)

@@ -46,17 +46,20 @@ def _capture(fn):
     return g
 
 
-@pytest.mark.parametrize("E,k,H,I,M,routing", [
-    (16, 4, 384, 256, 5, "uniform"),      # 20 pairs: the small-batch kernels
-    (16, 4, 384, 256, 37, "uniform"),     # ragged M, single-block align
-    (64, 6, 512, 256, 700, "skewed"),     # multi-block align, skewed routing
-    (8, 2, 512, 256, 1000, "uniform"),    # wide blocks of 192 rows
+@pytest.mark.parametrize("E,k,H,I,M,routing,plan", [
+    (16, 4, 384, 256, 5, "uniform", "default"),      # 20 pairs: the small-batch kernels
+    (16, 4, 384, 256, 37, "uniform", "default"),     # 148 pairs, L2-resident experts: the same
+    (16, 4, 384, 256, 37, "uniform", "tensor"),      # ragged M, single-block align
+    (64, 6, 512, 256, 700, "skewed", "default"),     # multi-block align, skewed routing
+    (8, 2, 512, 256, 1000, "uniform", "default"),    # wide blocks of 192 rows
 ])
-def test_forward_graph_replays_new_inputs(E, k, H, I, M, routing):
+def test_forward_graph_replays_new_inputs(E, k, H, I, M, routing, plan):
     import torch
     ops = _ops()
     w = inputs.make_weights(E, H, I, 300 + E)
     pw = ops.PackedWeights(w, E, H, I, k)
+    if plan == "tensor":
+        pw.shape = ops.Shape.of(E, k, H, I, flags=ops.MOE_FLAG_NO_GEMV)
     ws = ops.alloc_workspace(M, pw.shape)
     x = torch.empty((M, H), dtype=torch.int16, device="cuda")
     ids = torch.empty((M, k), dtype=torch.int32, device="cuda")

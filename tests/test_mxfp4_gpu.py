@@ -68,17 +68,23 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("plan", ["default", "tensor"])
 @pytest.mark.parametrize("E,k,H,I,M,seed", SHAPES)
-def test_mxfp4_forward_matches_oracle(E, k, H, I, M, seed):
+def test_mxfp4_forward_matches_oracle(E, k, H, I, M, seed, plan):
+    """Each shape through the default plan (the small-batch kernels where they
+    apply) and through the tensor-core kernels."""
     ops = _ops()
     w = inputs.make_weights_mxfp4(E, H, I, 40 + seed)
     pw = ops.PackedWeights(w, E, H, I, k, fmt="mxfp4")
     assert pw.shape.weight_format == ops.MOE_W_MXFP4
+    if plan == "tensor":
+        pw.shape = ops.Shape.of(E, k, H, I, weight_format=ops.MOE_W_MXFP4,
+                                flags=ops.MOE_FLAG_NO_GEMV)
     t = inputs.make_tokens(inputs.MoEConfig("mx", E, k, H, I, (M,), "uniform", 0, 60 + seed), M)
     got = gpu_forward(pw, t)
     ref, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
                                 t["topk_weights"], fmt="mxfp4")
-    print(assert_parity(got, ref, f"mxfp4 E{E} M{M}"))
+    print(assert_parity(got, ref, f"mxfp4 E{E} M{M} {plan}"))
 
 
 def test_the_two_formats_agree_on_weights_both_hold():

@@ -16,6 +16,9 @@ from helpers import assert_parity, gpu_forward
 pytestmark = pytest.mark.gpu
 
 E, K, H, I, M = 8, 2, 256, 128, 24
+# the default plan at this size is the small-batch kernels; "tensor" forces the
+# tensor-core kernels, which have their own conversions and range checks
+PLANS = ["default", "tensor"]
 
 
 def _ops():
@@ -31,16 +34,20 @@ def _tokens(seed, x_scale=1.0):
     return t
 
 
-def _forward(w, t):
+def _forward(w, t, plan="default"):
     ops = _ops()
     pw = ops.PackedWeights(w, E, H, I, K)
+    if plan == "tensor":
+        pw.shape = ops.Shape.of(E, K, H, I, flags=ops.MOE_FLAG_NO_GEMV)
+    assert ops.moe_int4_gemv(M, pw.shape) == (plan == "default")
     ws = ops.alloc_workspace(M, pw.shape)
     got = gpu_forward(pw, t, workspace=ws)
     flags, _ = ops.moe_int4_get_errors(ws)
     return pw, got, flags
 
 
-def test_edge_of_exact_range_meets_the_bound():
+@pytest.mark.parametrize("plan", PLANS)
+def test_edge_of_exact_range_meets_the_bound(plan):
     """Scales down at 2^-14 (the smallest normal fp16) and x up to +-3e4: the
     operands are exact, the intermediate stays in range, and the result meets
     the bound with no flag raised."""
@@ -57,7 +64,7 @@ def test_edge_of_exact_range_meets_the_bound():
     t["x"] = inputs.bf16_bits_from_f32(x)
     a = oracle.moe_intermediate(t["x"], w["q13"], w["s13"], t["topk_ids"], np.arange(M * K))
     assert np.abs(a).max() < 65504  # the case stays inside the range
-    pw, got, flags = _forward(w, t)
+    pw, got, flags = _forward(w, t, plan)
     assert pw.inexact_scales == 0
     assert flags == 0, hex(flags)
     ref, _ = oracle.moe_forward(t["x"], w["q13"], w["s13"], w["q2"], w["s2"], t["topk_ids"],
@@ -65,18 +72,20 @@ def test_edge_of_exact_range_meets_the_bound():
     assert_parity(got, ref, "edge of the exact range")
 
 
-def test_x_beyond_fp16_range_raises_the_flag():
+@pytest.mark.parametrize("plan", PLANS)
+def test_x_beyond_fp16_range_raises_the_flag(plan):
     ops = _ops()
     w = inputs.make_weights(E, H, I, 42)
     t = _tokens(2)
     x = inputs.f32_from_bf16_bits(t["x"])
     x[5, 17] = 1.0e5  # finite in bf16, beyond fp16
     t["x"] = inputs.bf16_bits_from_f32(x)
-    _, _, flags = _forward(w, t)
+    _, _, flags = _forward(w, t, plan)
     assert flags & ops.MOE_DEVERR_RANGE
 
 
-def test_intermediate_beyond_fp16_range_raises_the_flag():
+@pytest.mark.parametrize("plan", PLANS)
+def test_intermediate_beyond_fp16_range_raises_the_flag(plan):
     """x in range (|x| < 1e4) but SiLU(g) * u beyond 65504."""
     ops = _ops()
     w = inputs.make_weights(E, H, I, 43)
@@ -85,13 +94,14 @@ def test_intermediate_beyond_fp16_range_raises_the_flag():
     ref_a = oracle.moe_intermediate(t["x"], w["q13"], w["s13"], t["topk_ids"],
                                     np.arange(M * K))
     assert np.abs(ref_a).max() > 65504  # the case really leaves the range
-    _, _, flags = _forward(w, t)
+    _, _, flags = _forward(w, t, plan)
     assert flags & ops.MOE_DEVERR_RANGE
 
 
-def test_normal_inputs_raise_no_range_flag():
+@pytest.mark.parametrize("plan", PLANS)
+def test_normal_inputs_raise_no_range_flag(plan):
     w = inputs.make_weights(E, H, I, 44)
-    _, _, flags = _forward(w, _tokens(4))
+    _, _, flags = _forward(w, _tokens(4), plan)
     assert flags == 0
 
 

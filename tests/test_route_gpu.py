@@ -61,12 +61,18 @@ ROUTED = [
     (64, 6, 512, 256, 700, 3), (384, 8, 256, 128, 9, 4)]
 
 
+@pytest.mark.parametrize("plan", ["default", "tensor"])
 @pytest.mark.parametrize("E,k,H,I,M,seed", ROUTED)
-def test_forward_routed_matches_oracle(E, k, H, I, M, seed):
+def test_forward_routed_matches_oracle(E, k, H, I, M, seed, plan):
+    """The router in front of the default plan (the small-batch kernels at
+    these sizes where they apply) and of the tensor-core kernels (the fused
+    route + align, or the router kernel and the align)."""
     import torch
     ops = _ops()
     w = inputs.make_weights(E, H, I, 600 + seed)
     pw = ops.PackedWeights(w, E, H, I, k)
+    if plan == "tensor":
+        pw.shape = ops.Shape.of(E, k, H, I, flags=ops.MOE_FLAG_NO_GEMV)
     rng = np.random.default_rng([12, seed])
     x = inputs.bf16_bits_from_f32(rng.standard_normal((M, H), dtype=np.float32))
     lg = _logits(M, E, seed)
@@ -78,7 +84,7 @@ def test_forward_routed_matches_oracle(E, k, H, I, M, seed):
     np.testing.assert_array_equal(ids.cpu().numpy(), rid)
     np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
     ref, _ = oracle.moe_forward(x, w["q13"], w["s13"], w["q2"], w["s2"], rid, rw)
-    assert_parity(out.float().cpu().numpy(), ref, f"routed E{E} k{k} M{M}")
+    assert_parity(out.float().cpu().numpy(), ref, f"routed E{E} k{k} M{M} {plan}")
 
 
 def test_forward_routed_equals_forward_on_its_routing():

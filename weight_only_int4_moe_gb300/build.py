@@ -24,7 +24,7 @@ LIB = os.path.join(BUILD, "libmoe_int4.so")
 DEBUG_BUILD = os.path.join(BUILD, "debug_bounds")
 DEBUG_LIB = os.path.join(DEBUG_BUILD, "libmoe_int4.so")
 SOURCES = ["abi.cu", "align.cu", "pack.cu", "gemm.cu", "noalloc.cu", "ep.cu", "gemv.cu"]
-HEADERS = ["common.cuh", "kernels.cuh", "dequant.cuh"]
+HEADERS = ["common.cuh", "kernels.cuh", "dequant.cuh", "gemv.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

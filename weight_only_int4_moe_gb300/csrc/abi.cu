@@ -13,6 +13,7 @@
 
 #include "moe_int4.h"
 #include "kernels.cuh"
+#include "gemv.cuh"
 
 using namespace moe;
 
@@ -26,17 +27,23 @@ constexpr int kSingleBlockAlignMax = 4096;
 // (K2.6 M = 90, verify M = 256 and 512, mid-size M = 128), where the separate
 // gather kernel copies the rows faster than the fused kernel's gather share.
 constexpr int kFusedMaxPairs = 512;
-// The small-batch matrix-vector kernels run where a call's weight reads are
-// small enough that the tensor-core kernels' fixed per-call latency dominates:
-// at most 64 pairs and at most this many weights (pairs x 3 x hidden x inter).
-// They spend about four instructions per weight on the CUDA cores, so their
-// time grows with the weights they read.  Same-box A/B: mid-size M = 1 (104 M
-// weights) 43.7 -> 33.4 us; K2.6 M = 1 (352 M) 69.3 -> 78.5 us, slower.
+// The small-batch matrix-vector kernels stream each routed pair's expert on its
+// own, so they run where that re-reads little: at most 64 pairs and at most
+// 1.2 pairs per expert the routing is expected to touch (uniform routing), or
+// at most 256 pairs when all experts together fit in half the L2, where a
+// re-read is an L2 hit.  Same-box A/B against the tensor-core plans (us):
+// K2.6 M = 1 47.8 / 69.3, M = 8 285 / 313; mid-size M = 1 24.2 / 34.4, M = 4
+// 54.9 / 74.4, but M = 16 (1.8 pairs per touched expert) 174 / 133; the tiny
+// shape M = 128 12.9 / 106.
 constexpr int kGemvMaxPairs = 64;
-constexpr long long kGemvMaxWeights = 128ll << 20;
-// Their k splits: enough CTAs (16 warps each) for about two per SM of a GB300,
-// within a 48 KB shared-memory stage of the split's activations.
-constexpr int kGemvTargetCtas = 304;
+constexpr double kGemvMaxRereads = 1.2;
+constexpr int kGemvMaxPairsL2 = 256;
+constexpr double kGemvL2Bytes = 64.0 * (1 << 20);
+// Their k splits: slots for one wave of 4-warp CTAs over a GB300's 152 SMs at
+// six resident CTAs per SM, and a CTA's fixed cost (staging, first loads) in
+// units of one 64-k block of its loop.
+constexpr int kGemvSlots = 152 * 6;
+constexpr int kGemvCtaCost = 2;
 constexpr int kAlignChunk = 1024;
 
 thread_local int g_last_launches = 0;
@@ -86,7 +93,7 @@ struct Plan {
     int M, E, k, H, I, P, BM, RT1, RT2, n_chunks, out_f32;
     bool fused;  // the fused decode kernel (gather + gate/up + down in one launch)
     bool gemv;   // the small-batch matrix-vector kernels
-    int SA, KBs, SB, KS2s;  // their k splits (gate/up over H, down over I)
+    int SA, KBs, SB, KB2s;  // their k splits in 64-k blocks (gate/up over H, down over I)
     size_t cap, blocks_cap, tiles1_cap;
     size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_pos, off_cnt, off_partial, off_a,
         off_x16, off_acc, off_gu, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
@@ -109,23 +116,40 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.cap = (size_t)p.P + touched * (size_t)(p.BM - 1);
     p.blocks_cap = p.cap / p.BM + 1;
     p.tiles1_cap = p.blocks_cap * p.RT1;
-    p.gemv = !(sh->flags & (MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) && p.P <= kGemvMaxPairs &&
-             (long long)p.P * 3 * p.H * p.I <= kGemvMaxWeights;
+    {
+        // expected touched experts: each token picks top_k distinct of E
+        const double miss = std::pow(1.0 - (double)p.k / p.E, (double)p.M);
+        const double touched = p.E * (1.0 - miss);
+        const double expert_bytes = 3.0 * p.H * p.I * (0.5 + 2.0 / 32);  // weights + scales
+        const bool in_l2 = p.E * expert_bytes <= kGemvL2Bytes;
+        p.gemv = !(sh->flags & (MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) &&
+                 (in_l2 ? p.P <= kGemvMaxPairsL2
+                        : p.P <= kGemvMaxPairs && p.P <= kGemvMaxRereads * touched);
+    }
     p.fused = !p.gemv && !(sh->flags & MOE_FLAG_UNFUSED) && p.P <= kFusedMaxPairs && p.BM <= 128;
     if (p.gemv) {
-        auto splits = [&](int per_split_ctas, int n, int max_per) {  // (splits, per split)
-            int sp = (kGemvTargetCtas + per_split_ctas - 1) / per_split_ctas;
-            if (sp < (n + max_per - 1) / max_per) sp = (n + max_per - 1) / max_per;
-            if (sp > n) sp = n;
-            const int per = (n + sp - 1) / sp;
-            return std::make_pair((n + per - 1) / per, per);
+        // (splits, 64-k blocks per split) of n blocks over `base` CTAs per split:
+        // the fewest waves x (blocks per CTA + fixed cost), fewer splits on ties
+        auto splits = [&](int base, int n, int max_per) {
+            int best_sp = 1, best_per = n;
+            long long best = -1;
+            for (int sp = 1; sp <= n && sp <= 64; ++sp) {
+                const int per = (n + sp - 1) / sp;
+                if (per > max_per) continue;
+                const int used = (n + per - 1) / per;
+                const long long waves = ((long long)base * used + kGemvSlots - 1) / kGemvSlots;
+                const long long cost = waves * (per + kGemvCtaCost);
+                if (best < 0 || cost < best) best = cost, best_sp = used, best_per = per;
+            }
+            return std::make_pair(best_sp, best_per);
         };
-        const auto a = splits(p.P * ((p.RT1 + 3) / 4), p.H / 64, 192);   // 64-k blocks
-        const auto b = splits(p.P * ((p.RT2 + 3) / 4), p.I / 128, 96);   // 128-k stages
+        // at most 256 blocks per split (32 KB of fp16 activations)
+        const auto a = splits(p.P * p.RT1, p.H / 64, 256);
+        const auto b = splits(p.P * ((p.RT2 + 1) / 2), p.I / 64, 256);
         p.SA = a.first;
         p.KBs = a.second;
         p.SB = b.first;
-        p.KS2s = b.second;
+        p.KB2s = b.second;
     }
     size_t o = 0;
     p.off_err = o; o += 256;
@@ -443,9 +467,9 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
         ga.SA = pl.SA;
         ga.KBs = pl.KBs;
         ga.RT2 = pl.RT2;
-        ga.KS2 = pl.I / 128;
+        ga.KB2 = pl.I / 64;
         ga.SB = pl.SB;
-        ga.KS2s = pl.KS2s;
+        ga.KB2s = pl.KB2s;
         ga.fmt = shape->weight_format;
         ga.dq = int4_dequant_consts();
         if (launch_gemv(ga, 1, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;

@@ -1,40 +1,64 @@
-// Small-batch decode on the CUDA cores: the expert MLP as matrix-vector
-// products, one routed pair at a time.
+// Small-batch decode: the expert MLP as matrix-vector products, one routed pair
+// at a time.
 //
 // "The Throughput Lever" (section "The Result: Two Regimes"): below a few hundred
 // tokens per call the layer streams the touched experts' weights from memory.
-// At a handful of pairs the tensor-core GEMMs run one 16-column MMA per 128
-// weight rows, and their time is the per-stage latency of the dequant -> MMA ->
-// release loop, not memory.  Here every lane owns one weight row and streams it:
-// 32 lanes read 32 consecutive rows' 16-byte pieces of the packed layout, one
-// coalesced 512-byte read per warp, dequantise them in registers with the same
-// fp16 arithmetic as the GEMM kernels (so the weights are bit-identical), and
-// accumulate fp16 weight x fp16 activation products in fp32 (exact products, as
-// on the tensor cores).  No align and no gather: a pair's token row is read
-// directly.
+// At a handful of pairs the tcgen05 GEMMs run one 16-column MMA per 128 weight
+// rows, and their time is the per-stage latency of the dequant -> MMA -> release
+// hand-off between warps, not memory.  Here every warp is on its own: it
+// streams weight rows, dequantises them in registers with the GEMM kernels' fp16
+// arithmetic (so the weights are bit-identical) and reduces them against the
+// activation with register-operand MMAs (mma.sync m16n8k16, fp16 operands,
+// fp32 accumulators: exact products, as on the tcgen05 path).  No align, no
+// gather and no shared-memory weight tiles.
 //
-//  * Gate/up kernel: CTA (pair, k split, group of 4 row tiles), 16 warps = 4
-//    tiles x 4 lane quadrants of 32 rows.  A lane computes the gate and the up
-//    dot products of one intermediate feature over the split's k range and
-//    writes them to a per-split partial buffer (no atomics: every (split, pair,
-//    feature) has one writer).  It also zeroes the fp32 output accumulator.
-//  * Down kernel (programmatic dependent launch): CTA (pair, k split, group of
-//    4 output row tiles).  It sums the gate/up partials of its k range, forms
-//    the fp16 intermediate SiLU(g) * u (saturating, as the GEMM epilogue does),
-//    then a lane computes one output feature's dot product over the range and
-//    adds routing weight x result into the token's fp32 output row.
-// The k splits give every SM tens of warps with loads in flight; their count
-// is chosen per call (moe_int4_forward) so the grid covers the SMs.
+// A lane owns two weight rows (gate/up: the gate and the up row of one
+// intermediate feature; down: two output rows 64 apart) and, per MMA, four
+// consecutive k of each.  Its rows fill the A operand's rows g and g + 8 of the
+// MMA (g = lane / 4); the B operand is block-diagonal: B[k'][n] holds the
+// activation only where n = (k' mod 8) / 2, so column n of the result gathers
+// the lanes 4g + n alone, and D[g][n], D[g + 8][n] are lane 4g + n's two dot
+// products.  Only lanes with g == lane % 4 supply the activation; the others
+// point at zeros.  One MMA covers 8 weights per lane, against 4 fp32 FMAs and
+// 4 conversions per 4 weights on the plain CUDA-core dot product: about 1.7
+// instructions per weight with the dequantisation, where that took 3.75.
+//
+//  * Gate/up kernel: CTA (k split, 128-feature tile, pair), pair fastest so the
+//    pairs of one expert read the same weights close together in time; 4 warps
+//    of 32 features.  Per-split partial sums go to a workspace buffer (one
+//    writer each, no atomics).  It also zeroes the fp32 output accumulator.
+//  * Down kernel (programmatic dependent launch): CTA (k split, 256 output
+//    rows, pair); 4 warps of 64 rows.  It sums the gate/up partials of its k
+//    range, forms the fp16 intermediate SiLU(g) * u (saturating, as the GEMM
+//    epilogue does), and adds routing weight x result into the token's fp32
+//    output row with float2 atomics.
+// The k splits are chosen per call (moe_int4_forward) so the grid is about one
+// wave of small CTAs over the SMs.
 #include <cuda_fp16.h>
 
 #include "dequant.cuh"
 #include "kernels.cuh"
+#include "gemv.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kGvThreads = 512;  // 16 warps: 4 row tiles x 4 lane quadrants
+constexpr int kGvWarps = 4;
+constexpr int kGvThreads = 32 * kGvWarps;
+#ifndef GV_AHEAD
+#define GV_AHEAD 1
+#endif
+#ifndef GV_MIN_CTAS
+#define GV_MIN_CTAS 6
+#endif
+constexpr int kGvAhead = GV_AHEAD;      // slabs of weight loads in flight per warp
+constexpr int kGvMinCtas = GV_MIN_CTAS;  // resident CTAs per SM the register budget allows
+// Shared memory of both kernels: 128 bytes of zeros (the B operand of the
+// off-diagonal lanes), 64 bytes of padding so that the zeros and the
+// activation rows sit in different banks, then the split's activation in fp16.
+constexpr int kGvZeroBytes = 128;
+constexpr int kGvActOffset = 192;
 
 // 16 bytes of a weight stream, read once: no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
@@ -45,21 +69,22 @@ __device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
     return v;
 }
 
-// One lane's row of one packed stage: two 64-k slab rows (32 bytes each, in two
-// 16-byte halves 2048 bytes apart) and their two scale words.
-struct RowLoad {
-    uint4 a_lo, a_hi, b_lo, b_hi;
-    uint32_t sa, sb;
+// A lane's two rows of one 64-k slab: 32 bytes each (two 16-byte halves 2048
+// bytes apart) and each row's scale word (two fp16 group scales).
+struct RowPair {
+    uint4 lo0, hi0, lo1, hi1;
+    uint32_t s0, s1;
 };
 
-__device__ __forceinline__ RowLoad load_row(const uint8_t *w, const uint8_t *sc) {
-    RowLoad r;
-    r.a_lo = ld_stream(w);
-    r.a_hi = ld_stream(w + 2048);
-    r.b_lo = ld_stream(w + kSlabBytes);
-    r.b_hi = ld_stream(w + kSlabBytes + 2048);
-    r.sa = __ldg(reinterpret_cast<const uint32_t *>(sc));
-    r.sb = __ldg(reinterpret_cast<const uint32_t *>(sc + kStageSBytes / 2));
+__device__ __forceinline__ RowPair load_pair(const uint8_t *w0, const uint8_t *w1,
+                                             const uint8_t *sc0, const uint8_t *sc1) {
+    RowPair r;
+    r.lo0 = ld_stream(w0);
+    r.hi0 = ld_stream(w0 + kSlabBytes / 2);
+    r.lo1 = ld_stream(w1);
+    r.hi1 = ld_stream(w1 + kSlabBytes / 2);
+    r.s0 = __ldg(reinterpret_cast<const uint32_t *>(sc0));
+    r.s1 = __ldg(reinterpret_cast<const uint32_t *>(sc1));
     return r;
 }
 
@@ -72,26 +97,88 @@ __device__ __forceinline__ void dequant(const uint4 lo, const uint4 hi, uint32_t
         dequant_row(lo, hi, sc, k, v);
 }
 
-// acc += sum over 64 k of w[k] * x[k]: v holds the 64 fp16 weights as pairs
-// (k = 2c low, 2c + 1 high), xs the 64 activations.
-__device__ __forceinline__ float dot64(const uint32_t (&v)[32], const float *xs, float acc) {
-    const float4 *x4 = reinterpret_cast<const float4 *>(xs);
+// d += A * B for one m16n8k16 tile: fp16 A (four registers), fp16 B (two), fp32 d.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One 64-k slab of the lane's two rows against 64 activations.  v0 / v1 hold
+// the rows' fp16 pairs (v[c]: k = 2c, 2c + 1); xk points at the 64 fp16
+// activations (diagonal lanes) or at 128 bytes of zeros (the others).  Each
+// 16-byte activation load feeds two MMAs of four k each.
+__device__ __forceinline__ void slab_mma(float (&d)[4], const uint32_t (&v0)[32],
+                                         const uint32_t (&v1)[32], const uint8_t *xk) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const float4 xv = x4[c];
-        const float2 w0 = __half22float2(as_h2(v[2 * c]));
-        const float2 w1 = __half22float2(as_h2(v[2 * c + 1]));
-        acc = fmaf(w0.x, xv.x, acc);
-        acc = fmaf(w0.y, xv.y, acc);
-        acc = fmaf(w1.x, xv.z, acc);
-        acc = fmaf(w1.y, xv.w, acc);
+    for (int w = 0; w < 8; ++w) {
+        const uint4 xb = *reinterpret_cast<const uint4 *>(xk + 16 * w);
+        mma_f16_16816(d, v0[4 * w], v1[4 * w], v0[4 * w + 1], v1[4 * w + 1], xb.x, xb.y);
+        mma_f16_16816(d, v0[4 * w + 2], v1[4 * w + 2], v0[4 * w + 3], v1[4 * w + 3], xb.z, xb.w);
     }
-    return acc;
+}
+
+// Where a lane's two rows live: slab(kb) is the byte offset of 64-k slab kb
+// from the rows' first slab, scale(kb) the same for the scale words.
+template <class SlabOff, class ScaleOff>
+struct RowPairSrc {
+    const uint8_t *w0, *w1, *sc0, *sc1;
+    SlabOff slab;
+    ScaleOff scale;
+    __device__ __forceinline__ RowPair load(int kb) const {
+        return load_pair(w0 + slab(kb), w1 + slab(kb), sc0 + scale(kb), sc1 + scale(kb));
+    }
+};
+template <class SlabOff, class ScaleOff>
+__device__ __forceinline__ RowPairSrc<SlabOff, ScaleOff> row_pair_src(
+    const uint8_t *w0, const uint8_t *w1, const uint8_t *sc0, const uint8_t *sc1, SlabOff slab,
+    ScaleOff scale) {
+    return {w0, w1, sc0, sc1, slab, scale};
+}
+
+// The first kGvAhead slabs' loads, issued before the activation is staged
+// (the weights are call inputs, independent of it).
+template <class Src>
+__device__ __forceinline__ void prefetch_slabs(RowPair (&ring)[kGvAhead + 1], const Src &src,
+                                               int kb0, int kb1) {
+#pragma unroll
+    for (int i = 0; i < kGvAhead; ++i)
+        if (kb0 + i < kb1) ring[i] = src.load(kb0 + i);
+}
+
+// The k loop of one warp: slabs kb0 .. kb1 - 1 of the lane's two rows, with
+// kGvAhead slabs of loads in flight ahead of the one being reduced (the first
+// ones issued by prefetch_slabs).  act is the split's activation (kb0 first)
+// or the zeros.
+template <int FMT, class Src>
+__device__ __forceinline__ void reduce_slabs(float (&d)[4], RowPair (&ring)[kGvAhead + 1],
+                                             const Src &src, int kb0, int kb1,
+                                             const uint8_t *act, bool diag,
+                                             const DequantConsts &dq) {
+#pragma unroll 1
+    for (int kb = kb0; kb < kb1; ++kb) {
+        if (kb + kGvAhead < kb1) ring[kGvAhead] = src.load(kb + kGvAhead);
+        uint32_t v0[32], v1[32];
+        dequant<FMT>(ring[0].lo0, ring[0].hi0, ring[0].s0, dq, v0);
+        dequant<FMT>(ring[0].lo1, ring[0].hi1, ring[0].s1, dq, v1);
+        slab_mma(d, v0, v1, diag ? act + (size_t)(kb - kb0) * 128 : act);
+#pragma unroll
+        for (int i = 0; i < kGvAhead; ++i) ring[i] = ring[i + 1];
+    }
+}
+
+// Zeroes the 128 bytes at smem (threads 0..7).
+__device__ __forceinline__ void zero_b_operand(uint8_t *smem) {
+    if (threadIdx.x < kGvZeroBytes / 16)
+        reinterpret_cast<uint4 *>(smem)[threadIdx.x] = make_uint4(0, 0, 0, 0);
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kGvThreads) gemv_gate_up_kernel(const GemvArgs a) {
-    extern __shared__ float xs[];  // the split's k range of x: fp32 of the fp16 operand
+__global__ void __launch_bounds__(kGvThreads, kGvMinCtas) gemv_gate_up_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
     // the fp32 output accumulator, zeroed before the down kernel adds into it
     {
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -100,143 +187,136 @@ __global__ void __launch_bounds__(kGvThreads) gemv_gate_up_kernel(const GemvArgs
             reinterpret_cast<float4 *>(a.out)[i] = z;
     }
     pdl_launch_dependents();  // the down kernel may set up; it waits for this grid
-    const int tgroups = (a.RT1 + 3) / 4;
-    const int per_pair = a.SA * tgroups;
-    const int p = blockIdx.x / per_pair;
-    const int s = (blockIdx.x % per_pair) / tgroups, tg = blockIdx.x % tgroups;
+    const int p = blockIdx.x % a.P;
+    const int r = (blockIdx.x / a.P) % a.RT1;
+    const int s = blockIdx.x / (a.P * a.RT1);
     const int kb0 = s * a.KBs;
     const int kb1 = (kb0 + a.KBs < a.KB) ? kb0 + a.KBs : a.KB;
-    if (p >= a.P || kb0 >= kb1) return;
+    if (s >= a.SA || kb0 >= kb1) return;
     const int e = a.ids[p];
     if (e < 0 || e >= a.E) {  // dropped pair: counted once, as the align counts it
-        if (s == 0 && tg == 0 && threadIdx.x == 0 && a.err) {
+        if (s == 0 && r == 0 && threadIdx.x == 0 && a.err) {
             atomicOr(&a.err[0], kErrBadExpert);
             atomicAdd(&a.err[1], 1u);
         }
         return;
     }
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = wid * 32 + lane;  // the feature's row in its 128-row slabs
+    const size_t st0 = ((size_t)e * a.RT1 + r) * a.KB;
+    const uint8_t *wg = a.w13 + st0 * kStageWBytes + row * 16;  // gate: slab 0 of each stage
+    const uint8_t *sg = a.s13 + st0 * kStageSBytes + row * 4;
+    const auto src = row_pair_src(
+        wg, wg + kSlabBytes, sg, sg + kStageSBytes / 2,
+        [](int kb) { return (size_t)kb * kStageWBytes; },
+        [](int kb) { return (size_t)kb * kStageSBytes; });
+    RowPair ring[kGvAhead + 1];
+    prefetch_slabs(ring, src, kb0, kb1);
+    // the split's k range of the token's x row as the fp16 operand
     const int t = p / a.top_k;
     bool bad = false;
     const uint32_t *xr = reinterpret_cast<const uint32_t *>(a.x + (size_t)t * a.H + kb0 * 64);
+    uint32_t *xs = reinterpret_cast<uint32_t *>(smem + kGvActOffset);
     const int n2 = (kb1 - kb0) * 32;  // bf16 pairs of the range
-    for (int c = threadIdx.x; c < n2; c += blockDim.x) {
-        const float2 f = __half22float2(as_h2(bf16x2_to_f16x2_sat(__ldg(xr + c), bad)));
-        xs[2 * c] = f.x;
-        xs[2 * c + 1] = f.y;
-    }
+    for (int c = threadIdx.x; c < n2; c += blockDim.x)
+        xs[c] = bf16x2_to_f16x2_sat(__ldg(xr + c), bad);
+    zero_b_operand(smem);
     report_range(bad, a.err);
     __syncthreads();
-    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = tg * 4 + (wid >> 2);
-    if (r >= a.RT1) return;
-    const int row = (wid & 3) * 32 + lane;
-    const size_t st0 = ((size_t)e * a.RT1 + r) * a.KB;
-    const uint8_t *wrow = a.w13 + st0 * kStageWBytes + row * 16;
-    const uint8_t *srow = a.s13 + st0 * kStageSBytes + row * 4;
-    float g = 0.f, u = 0.f;
-    // two k blocks of loads in flight while one is computed
-    RowLoad cur = load_row(wrow + (size_t)kb0 * kStageWBytes, srow + (size_t)kb0 * kStageSBytes);
-    RowLoad nxt = cur;
-    if (kb0 + 1 < kb1)
-        nxt = load_row(wrow + (size_t)(kb0 + 1) * kStageWBytes,
-                       srow + (size_t)(kb0 + 1) * kStageSBytes);
-#pragma unroll 1
-    for (int kb = kb0; kb < kb1; ++kb) {
-        RowLoad nn = nxt;
-        if (kb + 2 < kb1)
-            nn = load_row(wrow + (size_t)(kb + 2) * kStageWBytes,
-                          srow + (size_t)(kb + 2) * kStageSBytes);
-        const float *x = xs + (kb - kb0) * 64;
-        uint32_t v[32];
-        dequant<FMT>(cur.a_lo, cur.a_hi, cur.sa, a.dq, v);  // gate row
-        g = dot64(v, x, g);
-        dequant<FMT>(cur.b_lo, cur.b_hi, cur.sb, a.dq, v);  // up row
-        u = dot64(v, x, u);
-        cur = nxt;
-        nxt = nn;
+    const bool diag = (lane >> 2) == (lane & 3);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    reduce_slabs<FMT>(d, ring, src, kb0, kb1, diag ? smem + kGvActOffset : smem, diag, a.dq);
+    // D[g][n] / D[g + 8][n] are lane 4g + n's gate / up sums: lanes with
+    // lane % 4 < 2 hold n = 2 (lane % 4) and the next one
+    if ((lane & 3) < 2) {
+        const int src = (lane >> 2) * 4 + (lane & 3) * 2;  // the first of the two lanes
+        const int feat = r * kSlabRows + wid * 32 + src;
+        float *gu = a.gu + ((size_t)s * a.P + p) * 2 * a.I;
+        *reinterpret_cast<float2 *>(gu + feat) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(gu + a.I + feat) = make_float2(d[2], d[3]);
     }
-    float *gu = a.gu + ((size_t)s * a.P + p) * 2 * a.I;
-    const int feat = r * kSlabRows + row;
-    gu[feat] = g;
-    gu[a.I + feat] = u;
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(const GemvArgs a) {
-    extern __shared__ float av[];  // the split's k range of the intermediate (fp16 values)
-    const int tgroups = (a.RT2 + 3) / 4;
-    const int per_pair = a.SB * tgroups;
-    const int p = blockIdx.x / per_pair;
-    const int s = (blockIdx.x % per_pair) / tgroups, tg = blockIdx.x % tgroups;
-    const int ks0 = s * a.KS2s;
-    const int ks1 = (ks0 + a.KS2s < a.KS2) ? ks0 + a.KS2s : a.KS2;
-    if (p >= a.P || ks0 >= ks1) return;
+__global__ void __launch_bounds__(kGvThreads, kGvMinCtas) gemv_down_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tiles2 = (a.RT2 + 1) / 2;  // 256-row CTA tiles
+    const int p = blockIdx.x % a.P;
+    const int q = (blockIdx.x / a.P) % tiles2;
+    const int s = blockIdx.x / (a.P * tiles2);
+    const int kb0 = s * a.KB2s;
+    const int kb1 = (kb0 + a.KB2s < a.KB2) ? kb0 + a.KB2s : a.KB2;
+    if (s >= a.SB || kb0 >= kb1) return;
     const int e = a.ids[p];  // a call input: readable before the wait
     if (e < 0 || e >= a.E) return;
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = 2 * q + (wid >> 1);  // the warp's 128-row tile
+    const bool rows_in = r < a.RT2;
+    const int row = (wid & 1) * 32 + lane;  // rows row and row + 64 of the tile's slabs
+    const size_t st0 = ((size_t)e * a.RT2 + (rows_in ? r : 0)) * (a.KB2 / 2);
+    const uint8_t *w = a.w2 + st0 * kStageWBytes + row * 16;
+    const uint8_t *sc = a.s2 + st0 * kStageSBytes + row * 4;
+    // 64-k block kb is slab kb % 2 of stage kb / 2
+    const auto src = row_pair_src(
+        w, w + 64 * 16, sc, sc + 64 * 4,
+        [](int kb) { return (size_t)(kb >> 1) * kStageWBytes + (kb & 1) * kSlabBytes; },
+        [](int kb) { return (size_t)(kb >> 1) * kStageSBytes + (kb & 1) * (kStageSBytes / 2); });
+    RowPair ring[kGvAhead + 1];
+    if (rows_in) prefetch_slabs(ring, src, kb0, kb1);  // weights: call inputs, before the wait
     pdl_wait();  // the gate/up partials and the zeroed output
+    // the split's k range of the intermediate: fp16 SiLU(g) * u of the summed partials
     bool bad = false;
-    const int n = (ks1 - ks0) * 2 * kSlabK;
-    for (int c = threadIdx.x; c < n; c += blockDim.x) {
-        const int i = ks0 * 2 * kSlabK + c;
-        const float *gp = a.gu + (size_t)p * 2 * a.I + i;
-        const size_t split = (size_t)a.P * 2 * a.I;
-        float gs = 0.f, us = 0.f;
-        for (int sa0 = 0; sa0 < a.SA; sa0 += 8) {  // eight splits' loads at a time
-            float gv[8], uv[8];
+    uint32_t *as = reinterpret_cast<uint32_t *>(smem + kGvActOffset);
+    const int n2 = (kb1 - kb0) * 32;  // fp16 pairs of the range
+    const size_t split = (size_t)a.P * 2 * a.I;
+    for (int c = threadIdx.x; c < n2; c += blockDim.x) {
+        const float *gp = a.gu + (size_t)p * 2 * a.I + kb0 * 64 + 2 * c;
+        float2 gs = make_float2(0.f, 0.f), us = make_float2(0.f, 0.f);
+        for (int sa0 = 0; sa0 < a.SA; sa0 += 4) {  // four splits' loads at a time
+            float2 gv[4], uv[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const bool in = sa0 + q < a.SA;
-                gv[q] = in ? __ldcg(gp + (sa0 + q) * split) : 0.f;
-                uv[q] = in ? __ldcg(gp + (sa0 + q) * split + a.I) : 0.f;
+            for (int j = 0; j < 4; ++j) {
+                const bool in = sa0 + j < a.SA;
+                const float *g = gp + (size_t)(in ? sa0 + j : 0) * split;
+                gv[j] = in ? __ldcg(reinterpret_cast<const float2 *>(g)) : make_float2(0.f, 0.f);
+                uv[j] = in ? __ldcg(reinterpret_cast<const float2 *>(g + a.I))
+                           : make_float2(0.f, 0.f);
             }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                gs += gv[q];
-                us += uv[q];
+            for (int j = 0; j < 4; ++j) {
+                gs.x += gv[j].x;
+                gs.y += gv[j].y;
+                us.x += uv[j].x;
+                us.y += uv[j].y;
             }
         }
-        av[c] = __half2float(__ushort_as_half(f16_sat(silu_mul(gs, us), bad)));
+        const uint32_t lo = f16_sat(silu_mul(gs.x, us.x), bad);
+        const uint32_t hi = f16_sat(silu_mul(gs.y, us.y), bad);
+        as[c] = lo | (hi << 16);
     }
+    zero_b_operand(smem);
     report_range(bad, a.err);
     __syncthreads();
-    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = tg * 4 + (wid >> 2);
-    if (r >= a.RT2) return;
-    const int row = (wid & 3) * 32 + lane;
-    const size_t st0 = ((size_t)e * a.RT2 + r) * a.KS2;
-    const uint8_t *wrow = a.w2 + st0 * kStageWBytes + row * 16;
-    const uint8_t *srow = a.s2 + st0 * kStageSBytes + row * 4;
-    float y = 0.f;
-    RowLoad cur = load_row(wrow + (size_t)ks0 * kStageWBytes, srow + (size_t)ks0 * kStageSBytes);
-    RowLoad nxt = cur;
-    if (ks0 + 1 < ks1)
-        nxt = load_row(wrow + (size_t)(ks0 + 1) * kStageWBytes,
-                       srow + (size_t)(ks0 + 1) * kStageSBytes);
-#pragma unroll 1
-    for (int ks = ks0; ks < ks1; ++ks) {
-        RowLoad nn = nxt;
-        if (ks + 2 < ks1)
-            nn = load_row(wrow + (size_t)(ks + 2) * kStageWBytes,
-                          srow + (size_t)(ks + 2) * kStageSBytes);
-        const float *x = av + (ks - ks0) * 2 * kSlabK;
-        uint32_t v[32];
-        dequant<FMT>(cur.a_lo, cur.a_hi, cur.sa, a.dq, v);  // k block 2 ks
-        y = dot64(v, x, y);
-        dequant<FMT>(cur.b_lo, cur.b_hi, cur.sb, a.dq, v);  // k block 2 ks + 1
-        y = dot64(v, x + kSlabK, y);
-        cur = nxt;
-        nxt = nn;
+    if (!rows_in) return;
+    const bool diag = (lane >> 2) == (lane & 3);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    reduce_slabs<FMT>(d, ring, src, kb0, kb1, diag ? smem + kGvActOffset : smem, diag, a.dq);
+    if ((lane & 3) < 2) {
+        const int src = (lane >> 2) * 4 + (lane & 3) * 2;
+        const int o = r * kSlabRows + (wid & 1) * 32 + src;  // output rows o, o + 1 (+ 64)
+        const float tw = a.topk_weights[p];
+        float *y = a.out + (size_t)(p / a.top_k) * a.H;
+        atomicAdd(reinterpret_cast<float2 *>(y + o), make_float2(tw * d[0], tw * d[1]));
+        atomicAdd(reinterpret_cast<float2 *>(y + o + 64), make_float2(tw * d[2], tw * d[3]));
     }
-    const int t = p / a.top_k;
-    atomicAdd(a.out + (size_t)t * a.H + r * kSlabRows + row, a.topk_weights[p] * y);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const GemvArgs &a, int step, cudaStream_t s, int *launches) {
     if (step == 1) {  // gate/up: a plain launch (it overwrites the workspace partials)
-        const int ga = a.P * a.SA * ((a.RT1 + 3) / 4);
-        const size_t sma = (size_t)a.KBs * 64 * sizeof(float);
+        const int ga = a.P * a.RT1 * a.SA;
+        const size_t sma = kGvActOffset + (size_t)a.KBs * 64 * 2;
         if (sma > 48 * 1024) return cudaErrorInvalidValue;
         if (a.fmt == 1)
             gemv_gate_up_kernel<1><<<ga, kGvThreads, sma, s>>>(a);
@@ -246,8 +326,8 @@ cudaError_t launch_gemv(const GemvArgs &a, int step, cudaStream_t s, int *launch
         if (e == cudaSuccess && launches) *launches += 1;
         return e;
     }
-    const int gb = a.P * a.SB * ((a.RT2 + 3) / 4);
-    const size_t smb = (size_t)a.KS2s * 2 * kSlabK * sizeof(float);
+    const int gb = a.P * ((a.RT2 + 1) / 2) * a.SB;
+    const size_t smb = kGvActOffset + (size_t)a.KB2s * 64 * 2;
     if (smb > 48 * 1024) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = pdl_config((unsigned)gb, kGvThreads, smb, s);
     cudaLaunchAttribute attr;

@@ -138,31 +138,6 @@ struct GemmParams {
     DequantConsts dq;
 };
 
-// kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine; kind 3:
-// both in one persistent launch (the fused decode kernel: gather, gate/up, then
-// down, blocks of at most 128 rows).  The tensor maps cover the B operand rows in
-// bucketed order, 64-column x block_m-row boxes, 128-byte swizzle: tmap_x the fp16
-// x rows (gate/up), tmap_a the fp16 intermediate (down); a kind uses its own.
-// The small-batch path (gemv.cu): the expert MLP as matrix-vector products
-// on the CUDA cores, one routed pair at a time.
-struct GemvArgs {
-    const uint16_t *x;          // [M][H] bf16 bits
-    const int32_t *ids;         // [P] expert of each (token, slot) pair
-    const float *topk_weights;  // [P]
-    const uint8_t *w13, *s13, *w2, *s2;  // packed weights and scales
-    float *gu;                  // [SA][P][2][I] gate / up partial sums per k split
-    float *out;                 // [M][H] fp32 accumulator, zeroed by the gate/up kernel
-    size_t out_n16;             // its size in float4s
-    uint32_t *err;              // error words (flags, dropped pairs)
-    int M, top_k, P, E, H, I;
-    int RT1, KB, SA, KBs;       // gate/up: row tiles (I / 128), 64-k blocks, k splits, per split
-    int RT2, KS2, SB, KS2s;     // down: row tiles (H / 128), 128-k stages, k splits, per split
-    int fmt;                    // 0 INT4, 1 MXFP4
-    DequantConsts dq;
-};
-// step 1: the gate/up kernel; step 2: the down kernel (programmatic dependent launch)
-cudaError_t launch_gemv(const GemvArgs &a, int step, cudaStream_t s, int *launches);
-
 // The INT4 dequantisation constants (see dequant_row).
 inline DequantConsts int4_dequant_consts() {
     DequantConsts d;
@@ -172,6 +147,11 @@ inline DequantConsts int4_dequant_consts() {
     return d;
 }
 
+// kind 1: gate/up GEMM + SwiGLU; kind 2: down GEMM + weighted combine; kind 3:
+// both in one persistent launch (the fused decode kernel: gather, gate/up, then
+// down, blocks of at most 128 rows).  The tensor maps cover the B operand rows in
+// bucketed order, 64-column x block_m-row boxes, 128-byte swizzle: tmap_x the fp16
+// x rows (gate/up), tmap_a the fp16 intermediate (down); a kind uses its own.
 cudaError_t launch_gemm(int kind, const GemmParams &p, const CUtensorMap *tmap_x,
                         const CUtensorMap *tmap_a, int grid, cudaStream_t s, int *launches);
 // Fills the ring depths and shared-memory layout of p for the given kind.
