@@ -307,19 +307,22 @@ def run_reference(args, cfg, Ms, world, rank):
 def roofline_of(recs, w13_b, w2_b, top_k, H, I, hbm_peak, tc_peak, peak_src, workload):
     """Roofline position of the dominant kernel over profiled calls: of the fused
     decode kernel (both GEMMs in one launch, where the forward ran it), the
-    gate/up GEMM and the down GEMM (where it ran them separately), the one with
-    the largest share of the per-kernel event time, over the calls that ran it.
+    gate/up GEMM and the down GEMM (where it ran them separately) and the two
+    small-batch matrix-vector kernels (where it ran those), the one with the
+    largest share of the per-kernel event time, over the calls that ran it.
     Algorithmic bytes (touched experts x packed weights + scales) or FLOPs
     (2 x pairs x the kernel's weights) per launch over its CUDA-event duration,
     whichever bound is the slower at the peaks."""
-    mult = {"fused": 3, "gate_up": 2, "down": 1}
-    wbytes = {"fused": w13_b + w2_b, "gate_up": w13_b, "down": w2_b}
+    mult = {"fused": 3, "gate_up": 2, "down": 1, "gemv_gate_up": 2, "gemv_down": 1}
+    wbytes = {"fused": w13_b + w2_b, "gate_up": w13_b, "down": w2_b, "gemv_gate_up": w13_b,
+              "gemv_down": w2_b}
 
     def launches(kernel):  # (ms, record) of every launch of the kernel
         if kernel == "fused":
             return [(r["stages"][1], r) for r in recs if r["fused"]]
-        col = 1 if kernel == "gate_up" else 2
-        return [(r["stages"][col], r) for r in recs if not r["fused"]]
+        gemv = kernel.startswith("gemv_")
+        col = 1 if kernel.endswith("gate_up") else 2
+        return [(r["stages"][col], r) for r in recs if not r["fused"] and r["gemv"] == gemv]
 
     dominant = max(mult, key=lambda k: sum(ms for ms, _ in launches(k)))
     lr = launches(dominant)

@@ -203,16 +203,16 @@ def test_ep_row_kernels_check_arguments_on_the_host():
 
 def test_launch_plans():
     """Which forwards run which plan (host logic; the measured crossovers): the
-    small-batch kernels up to 64 pairs and 1.2 pairs per expected touched
+    small-batch kernels up to 128 pairs and 1.2 pairs per expected touched
     expert, or up to 256 pairs when all experts fit in half the L2; the fused
     decode kernel up to 512 pairs in blocks of up to 128 rows; the separate
     kernels beyond."""
     k26 = ops.Shape.of(384, 8, 7168, 2048)
-    Ms = (1, 8, 9, 64, 65, 90, 1024)
-    # 8 of 384 experts per token: 64 pairs touch about 59.4 experts (1.08 per)
-    assert [ops.moe_int4_gemv(M, k26) for M in Ms] == [True, True] + [False] * 5
-    assert [ops.moe_int4_fused(M, k26) for M in Ms] == [False, False, True, True, False, False,
-                                                        False]
+    Ms = (1, 8, 9, 16, 17, 64, 65, 90, 1024)
+    # 8 of 384 experts per token: 128 pairs touch about 109.7 experts (1.17 per)
+    assert [ops.moe_int4_gemv(M, k26) for M in Ms] == [True] * 4 + [False] * 5
+    assert [ops.moe_int4_fused(M, k26) for M in Ms] == [False] * 4 + [True, True, False, False,
+                                                                      False]
     mid = ops.Shape.of(64, 6, 4096, 1408)
     # M = 4: 24 pairs on about 20.8 experts (1.15); M = 5: 30 on 24.9 (1.20+)
     assert [ops.moe_int4_gemv(M, mid) for M in (1, 4, 5, 32)] == [True, True, False, False]

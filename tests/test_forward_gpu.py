@@ -99,6 +99,7 @@ GEMV = [
     (8, 1, 2048, 512, 7, 43),     # top-1
     (48, 8, 2048, 1024, 2, 44),   # 16 pairs over 170 MB of experts: the re-read rule
     (8, 2, 256, 128, 128, 46),    # 256 pairs on 8 experts (L2-resident): the pair limit
+    (512, 8, 512, 256, 12, 47),   # 96 pairs over 113 MB of experts (1.09 per touched)
 ]
 
 

@@ -28,14 +28,19 @@ constexpr int kSingleBlockAlignMax = 4096;
 // gather kernel copies the rows faster than the fused kernel's gather share.
 constexpr int kFusedMaxPairs = 512;
 // The small-batch matrix-vector kernels stream each routed pair's expert on its
-// own, so they run where that re-reads little: at most 64 pairs and at most
+// own, so they run where that re-reads little: at most 128 pairs and at most
 // 1.2 pairs per expert the routing is expected to touch (uniform routing), or
 // at most 256 pairs when all experts together fit in half the L2, where a
 // re-read is an L2 hit.  Same-box A/B against the tensor-core plans (us):
-// K2.6 M = 1 47.8 / 69.3, M = 8 285 / 313; mid-size M = 1 24.2 / 34.4, M = 4
-// 54.9 / 74.4, but M = 16 (1.8 pairs per touched expert) 174 / 133; the tiny
-// shape M = 128 12.9 / 106.
-constexpr int kGemvMaxPairs = 64;
+// K2.6 M = 1 47.7 / 69.3, M = 8 285 / 313, M = 9 312 / 357, M = 16 521 / 569;
+// mid-size M = 1 24.2 / 34.4, M = 4 54.9 / 74.4, but M = 16 (1.8 pairs per
+// touched expert) 179 / 133 and K2.6 M = 32 (1.35) 1078 / 933; the tiny shape
+// M = 128 12.9 / 106.  Grouping an expert's pairs so that they share the
+// weight loads (up to four per CTA, a leader CTA per group found by a search
+// over the routing) measured slower at every size: 377 / 324 us at K2.6
+// M = 9, 208 / 157 at mid-size M = 32; most groups hold one pair there, and the
+// search and the second MMA set cost more than the re-reads.
+constexpr int kGemvMaxPairs = 128;
 constexpr double kGemvMaxRereads = 1.2;
 constexpr int kGemvMaxPairsL2 = 256;
 constexpr double kGemvL2Bytes = 64.0 * (1 << 20);
