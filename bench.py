@@ -307,22 +307,27 @@ def run_reference(args, cfg, Ms, world, rank):
 def roofline_of(recs, w13_b, w2_b, top_k, H, I, hbm_peak, tc_peak, peak_src, workload):
     """Roofline position of the dominant kernel over profiled calls: of the fused
     decode kernel (both GEMMs in one launch, where the forward ran it), the
-    gate/up GEMM and the down GEMM (where it ran them separately) and the two
-    small-batch matrix-vector kernels (where it ran those), the one with the
+    gate/up GEMM and the down GEMM or the per-block down kernel (where it ran
+    them separately) and the two small-batch matrix-vector kernels (where it
+    ran those), the one with the
     largest share of the per-kernel event time, over the calls that ran it.
     Algorithmic bytes (touched experts x packed weights + scales) or FLOPs
     (2 x pairs x the kernel's weights) per launch over its CUDA-event duration,
     whichever bound is the slower at the peaks."""
-    mult = {"fused": 3, "gate_up": 2, "down": 1, "gemv_gate_up": 2, "gemv_down": 1}
-    wbytes = {"fused": w13_b + w2_b, "gate_up": w13_b, "down": w2_b, "gemv_gate_up": w13_b,
-              "gemv_down": w2_b}
+    mult = {"fused": 3, "gate_up": 2, "down": 1, "block_down": 1, "gemv_gate_up": 2,
+            "gemv_down": 1}
+    wbytes = {"fused": w13_b + w2_b, "gate_up": w13_b, "down": w2_b, "block_down": w2_b,
+              "gemv_gate_up": w13_b, "gemv_down": w2_b}
 
     def launches(kernel):  # (ms, record) of every launch of the kernel
         if kernel == "fused":
             return [(r["stages"][1], r) for r in recs if r["fused"]]
         gemv = kernel.startswith("gemv_")
         col = 1 if kernel.endswith("gate_up") else 2
-        return [(r["stages"][col], r) for r in recs if not r["fused"] and r["gemv"] == gemv]
+        rs = [r for r in recs if not r["fused"] and r["gemv"] == gemv]
+        if kernel in ("down", "block_down"):  # the separate plan's two down kernels
+            rs = [r for r in rs if r["block_down"] == (kernel == "block_down")]
+        return [(r["stages"][col], r) for r in rs]
 
     dominant = max(mult, key=lambda k: sum(ms for ms, _ in launches(k)))
     lr = launches(dominant)
@@ -406,7 +411,8 @@ class Workload:
             rec.append({"M": M, "ms": ev0.elapsed_time(ev1), "stages": stages,
                         "touched": n_touched, "launches": launches,
                         "fused": ops.moe_int4_fused(M, shape),
-                        "gemv": ops.moe_int4_gemv(M, shape)})
+                        "gemv": ops.moe_int4_gemv(M, shape),
+                        "block_down": ops.moe_int4_block_down(M, shape)})
 
     def profiled(self, steps, first, stream):
         """The same calls again with CUDA events between the kernels, on the
@@ -438,6 +444,7 @@ class Workload:
             st = np.mean([r["stages"] for r in prec if r["M"] == M], axis=0)
             fused = all(r["fused"] for r in rs)
             gemv = all(r["gemv"] for r in rs)
+            block_down = all(r["block_down"] for r in rs)
             out[str(M)] = {
                 "us_per_call": t_med, "us_mean": statistics.mean(us), "calls": len(us),
                 "tokens_per_s": M / (t_med / 1e6),
@@ -450,7 +457,8 @@ class Workload:
                 "ideal_us": {"hbm": t_hbm, "tensor": t_tc},
                 "bound": "hbm" if t_hbm >= t_tc else "tensor",
                 "roofline_frac": max(t_hbm, t_tc) / t_med,
-                "kernels": "gemv" if gemv else ("fused" if fused else "separate"),
+                "kernels": "gemv" if gemv else ("fused" if fused else (
+                    "separate, block down" if block_down else "separate")),
                 "stage_us": ({"route": st[0] * 1e3, "gate_up": st[1] * 1e3, "down": st[2] * 1e3,
                               "finalize": st[3] * 1e3} if gemv else
                              {"align": st[0] * 1e3, "fused": st[1] * 1e3, "finalize": st[3] * 1e3}

@@ -94,7 +94,7 @@ enum {
                                 tensor-core kernels even where the fused decode kernel or
                                 the small-batch path applies (same results) */
 #define MOE_FLAG_NO_GEMV 0x2 /* keep to the tensor-core kernels (fused where it applies)
-                                where the small-batch matrix-vector path would run */
+                                where the matrix-vector kernels would run */
 
 /* Layer shape.  Supported: 1 <= E <= 1024, 1 <= top_k <= min(E, 32),
  * hidden % 128 == 0, inter % 128 == 0, group == 32, weight_format one of
@@ -272,6 +272,11 @@ int moe_int4_fused(int M, const moe_int4_shape *shape);
  * per-pair matrix-vector products; see moe_int4_forward), 0 otherwise. */
 int moe_int4_gemv(int M, const moe_int4_shape *shape);
 
+/* 1 if a forward of M tokens runs the separate plan with its down step as
+ * per-block matrix-vector work (routing blocks of at most 16 rows; see
+ * moe_int4_forward), 0 otherwise. */
+int moe_int4_block_down(int M, const moe_int4_shape *shape);
+
 /*
  * moe_int4_workspace_layout: byte offsets inside the workspace of a forward of
  * M tokens, for inspecting a finished call: offsets[0] error words (uint32 flags,
@@ -311,7 +316,9 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
  * tensor-core kernel that gathers x, runs the gate/up GEMM and then the down
  * GEMM (its CTAs hand work to each other through counters in the workspace,
  * with bounded waits; it expects to get every SM within about two seconds);
- * otherwise a gather kernel and one kernel per GEMM.  All plans form the same fp16 weights and intermediates and
+ * otherwise a gather kernel and one kernel per GEMM, where at routing blocks of
+ * at most 16 rows the down step streams each block's expert once and reduces it
+ * against the block's rows as matrix-vector work.  All plans form the same fp16 weights and intermediates and
  * accumulate in fp32; they differ only in summation order.  bf16 output adds a
  * conversion kernel.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,

@@ -227,3 +227,9 @@ def test_launch_plans():
     assert not ops.moe_int4_fused(512, ops.Shape.of(3, 1, 256, 128))  # 512 pairs, block 192
     unfused = ops.Shape.of(384, 8, 7168, 2048, flags=ops.MOE_FLAG_UNFUSED)
     assert not ops.moe_int4_fused(1, unfused) and not ops.moe_int4_gemv(1, unfused)
+    # the separate plan's down step as per-block work at 16-row blocks only
+    assert [ops.moe_int4_block_down(M, k26) for M in (1, 64, 65, 90, 256)] == [
+        False, False, True, True, False]
+    assert not ops.moe_int4_block_down(90, unfused)
+    assert not ops.moe_int4_block_down(90, ops.Shape.of(384, 8, 7168, 2048,
+                                                        flags=ops.MOE_FLAG_NO_GEMV))

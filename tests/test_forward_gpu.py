@@ -113,6 +113,32 @@ def test_small_batch_kernels_match_oracle(E, k, H, I, M, seed):
     print(assert_parity(got, ref, f"gemv E{E} k{k} H{H} I{I} M{M}"))
 
 
+# the separate plan's per-block down step: blocks of 16 rows with about two real
+# rows each, odd down row-tile counts, and skewed routing whose fullest blocks
+# need two passes of eight rows
+BLOCK_DOWN = [
+    (384, 8, 256, 128, 90, 50, "uniform"),
+    (384, 8, 384, 256, 80, 51, "uniform"),   # three down row tiles: a half CTA tile
+    (384, 8, 512, 256, 120, 52, "skewed"),  # up to 12 rows on one expert
+]
+
+
+@pytest.mark.parametrize("E,k,H,I,M,seed,routing", BLOCK_DOWN)
+def test_block_down_matches_oracle_and_tensor_path(E, k, H, I, M, seed, routing):
+    ops = _ops()
+    w, pw, t = setup(E, k, H, I, M, seed, routing)
+    assert ops.moe_int4_block_down(M, pw.shape) and ops.moe_int4_block_m(M, pw.shape) == 16
+    got = gpu_forward(pw, t)
+    ref = oracle_out(w, t)
+    print(assert_parity(got, ref, f"block down E{E} H{H} I{I} M{M} {routing}"))
+    if routing == "skewed":  # some block holds more than eight real rows
+        assert np.bincount(t["topk_ids"].ravel(), minlength=E).max() > 8
+    b = gpu_forward(with_flags(pw, ops.MOE_FLAG_NO_GEMV), t)
+    assert not ops.moe_int4_block_down(M, with_flags(pw, ops.MOE_FLAG_NO_GEMV).shape)
+    rms = float(np.sqrt(np.mean(b.astype(np.float64) ** 2)))
+    assert np.abs(got.astype(np.float64) - b).max() <= 1e-3 * rms
+
+
 def test_small_batch_kernels_match_the_tensor_path_closely():
     """Both paths form the same fp16 weights and intermediates and sum exact
     products in fp32, so they differ only by summation order: far below the

@@ -41,6 +41,14 @@ constexpr int kFusedMaxPairs = 512;
 // M = 9, 208 / 157 at mid-size M = 32; most groups hold one pair there, and the
 // search and the second MMA set cost more than the re-reads.
 constexpr int kGemvMaxPairs = 128;
+// The separate plan's down step runs as per-block matrix-vector work (one pass
+// over the expert's down rows per routing block) at blocks of up to this many
+// rows.
+// Same-box A/B against the down GEMM (us per call): K2.6 M = 65 1 372 / 1 431,
+// M = 90 1 548 / 1 593; at 32-row blocks verify M = 256 2 149 / 1 885, so not
+// there.  Its CTAs (4 warps, 8 block rows per pass) run 4 per SM.
+constexpr int kBlockDownMaxRows = 16;
+constexpr int kBlockDownSlots = 152 * 4;
 constexpr double kGemvMaxRereads = 1.2;
 constexpr int kGemvMaxPairsL2 = 256;
 constexpr double kGemvL2Bytes = 64.0 * (1 << 20);
@@ -99,6 +107,8 @@ struct Plan {
     bool fused;  // the fused decode kernel (gather + gate/up + down in one launch)
     bool gemv;   // the small-batch matrix-vector kernels
     int SA, KBs, SB, KB2s;  // their k splits in 64-k blocks (gate/up over H, down over I)
+    bool block_down;        // the separate plan's down step as per-block matrix-vector work
+    int bd_SB, bd_KB2s;     // its k splits
     size_t cap, blocks_cap, tiles1_cap;
     size_t off_err, off_npp, off_sorted, off_expert, off_chunk, off_pos, off_cnt, off_partial, off_a,
         off_x16, off_acc, off_gu, off_io_x, off_io_ids, off_io_w, off_io_out, total, total_io;
@@ -132,29 +142,42 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
                         : p.P <= kGemvMaxPairs && p.P <= kGemvMaxRereads * touched);
     }
     p.fused = !p.gemv && !(sh->flags & MOE_FLAG_UNFUSED) && p.P <= kFusedMaxPairs && p.BM <= 128;
-    if (p.gemv) {
+    p.block_down = !p.gemv && !p.fused &&
+                   !(sh->flags & (MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) &&
+                   p.BM <= kBlockDownMaxRows;
+    if (p.gemv || p.block_down) {
         // (splits, 64-k blocks per split) of n blocks over `base` CTAs per split:
         // the fewest waves x (blocks per CTA + fixed cost), fewer splits on ties
-        auto splits = [&](int base, int n, int max_per) {
+        auto splits = [&](int base, int n, int max_per, int slots) {
             int best_sp = 1, best_per = n;
             long long best = -1;
             for (int sp = 1; sp <= n && sp <= 64; ++sp) {
                 const int per = (n + sp - 1) / sp;
                 if (per > max_per) continue;
                 const int used = (n + per - 1) / per;
-                const long long waves = ((long long)base * used + kGemvSlots - 1) / kGemvSlots;
+                const long long waves = ((long long)base * used + slots - 1) / slots;
                 const long long cost = waves * (per + kGemvCtaCost);
                 if (best < 0 || cost < best) best = cost, best_sp = used, best_per = per;
             }
             return std::make_pair(best_sp, best_per);
         };
-        // at most 256 blocks per split (32 KB of fp16 activations)
-        const auto a = splits(p.P * p.RT1, p.H / 64, 256);
-        const auto b = splits(p.P * ((p.RT2 + 1) / 2), p.I / 64, 256);
-        p.SA = a.first;
-        p.KBs = a.second;
-        p.SB = b.first;
-        p.KB2s = b.second;
+        if (p.gemv) {
+            // at most 256 blocks per split (32 KB of fp16 activations)
+            const auto a = splits(p.P * p.RT1, p.H / 64, 256, kGemvSlots);
+            const auto b = splits(p.P * ((p.RT2 + 1) / 2), p.I / 64, 256, kGemvSlots);
+            p.SA = a.first;
+            p.KBs = a.second;
+            p.SB = b.first;
+            p.KB2s = b.second;
+        } else {
+            // about one routing block per touched expert; at most 32 blocks per
+            // split (eight intermediate rows of 4 KB)
+            const double miss = std::pow(1.0 - (double)p.k / p.E, (double)p.M);
+            const int blocks = (int)std::ceil(p.E * (1.0 - miss));
+            const auto b = splits(blocks * ((p.RT2 + 1) / 2), p.I / 64, 32, kBlockDownSlots);
+            p.bd_SB = b.first;
+            p.bd_KB2s = b.second;
+        }
     }
     size_t o = 0;
     p.off_err = o; o += 256;
@@ -351,6 +374,11 @@ size_t moe_int4_workspace_bytes(int M, const moe_int4_shape *shape, int flags) {
 int moe_int4_fused(int M, const moe_int4_shape *shape) {
     if (check_shape(shape) != MOE_OK || M < 1 || M > (1 << 20)) return 0;
     return make_plan(M, shape).fused ? 1 : 0;
+}
+
+int moe_int4_block_down(int M, const moe_int4_shape *shape) {
+    if (check_shape(shape) != MOE_OK || M < 1 || M > (1 << 20)) return 0;
+    return make_plan(M, shape).block_down ? 1 : 0;
 }
 
 int moe_int4_gemv(int M, const moe_int4_shape *shape) {
@@ -595,11 +623,38 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
         if (launch_gemm(1, g1, &tmap_x, &tmap_a, grid, s, &launches) != cudaSuccess)
             return MOE_ERR_CUDA;
         prof_record(2, s);
-        GemmParams g2 = g;
-        g2.skip_stage = -1;
-        if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
-        if (launch_gemm(2, g2, &tmap_x, &tmap_a, grid, s, &launches) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (pl.block_down) {
+            BlockDownArgs bd{};
+            bd.sorted_ids = sorted;
+            bd.expert_ids = expert;
+            bd.num_post_pad = npp;
+            bd.a_out = a_buf;
+            bd.topk_weights = topk_weights;
+            bd.w2 = reinterpret_cast<const uint8_t *>(w2_packed);
+            bd.s2 = reinterpret_cast<const uint8_t *>(w2_scales);
+            bd.out = acc;
+            bd.err = err;
+            bd.P = pl.P;
+            bd.E = pl.E;
+            bd.H = pl.H;
+            bd.I = pl.I;
+            bd.top_k = pl.k;
+            bd.block_m = pl.BM;
+            bd.blocks_cap = (int)pl.blocks_cap;
+            bd.RT2 = pl.RT2;
+            bd.KB2 = pl.I / 64;
+            bd.SB = pl.bd_SB;
+            bd.KB2s = pl.bd_KB2s;
+            bd.fmt = shape->weight_format;
+            bd.dq = int4_dequant_consts();
+            if (launch_block_down(bd, s, &launches) != cudaSuccess) return MOE_ERR_CUDA;
+        } else {
+            GemmParams g2 = g;
+            g2.skip_stage = -1;
+            if (!plan_gemm_smem(2, g2)) return MOE_ERR_SHAPE;
+            if (launch_gemm(2, g2, &tmap_x, &tmap_a, grid, s, &launches) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
         prof_record(3, s);
     }
 

@@ -311,6 +311,172 @@ __global__ void __launch_bounds__(kGvThreads, kGvMinCtas) gemv_down_kernel(const
     }
 }
 
+// ---------------------------------------------------------------- block down --
+// The separate plan's down step at short routing blocks (16 or 32 rows): per
+// align block, a CTA streams 256 of the expert's down rows over its k split once
+// and reduces them against the block's real rows of the gate/up intermediate,
+// up to kBdRows at a time: MMA q takes rows 2q (result columns 0..3) and 2q + 1
+// (columns 4..7) of the pass, through the same block-diagonal operand as above.
+#ifndef GV_BD_ROWS
+#define GV_BD_ROWS 8
+#endif
+#ifndef GV_BD_MIN_CTAS
+#define GV_BD_MIN_CTAS 4
+#endif
+constexpr int kBdRows = GV_BD_ROWS;          // block rows per pass (two per MMA)
+constexpr int kBdMinCtas = GV_BD_MIN_CTAS;   // resident CTAs per SM (registers)
+
+// One slab against NQ row pairs of a pass.
+template <int NQ>
+__device__ __forceinline__ void slab_mma_rows(float (&d)[NQ][4], const uint32_t (&v0)[32],
+                                              const uint32_t (&v1)[32],
+                                              const uint8_t *const (&xk)[NQ]) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const uint4 xb = *reinterpret_cast<const uint4 *>(xk[q] + 16 * w);
+            mma_f16_16816(d[q], v0[4 * w], v1[4 * w], v0[4 * w + 1], v1[4 * w + 1], xb.x, xb.y);
+            mma_f16_16816(d[q], v0[4 * w + 2], v1[4 * w + 2], v0[4 * w + 3], v1[4 * w + 3], xb.z,
+                          xb.w);
+        }
+    }
+}
+
+// The k loop of one warp against a pass's rows (act[q]: this lane's source for
+// MMA q, slab kb0 first, or null for the zeros).
+template <int FMT, int NQ, class Src>
+__device__ __forceinline__ void reduce_rows(float (&d)[NQ][4], RowPair (&ring)[kGvAhead + 1],
+                                            const Src &src, int kb0, int kb1,
+                                            const uint8_t *const (&act)[NQ],
+                                            const uint8_t *zeros, const DequantConsts &dq) {
+#pragma unroll 1
+    for (int kb = kb0; kb < kb1; ++kb) {
+        if (kb + kGvAhead < kb1) ring[kGvAhead] = src.load(kb + kGvAhead);
+        uint32_t v0[32], v1[32];
+        dequant<FMT>(ring[0].lo0, ring[0].hi0, ring[0].s0, dq, v0);
+        dequant<FMT>(ring[0].lo1, ring[0].hi1, ring[0].s1, dq, v1);
+        const uint8_t *xk[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) xk[q] = act[q] ? act[q] + (size_t)(kb - kb0) * 128 : zeros;
+        slab_mma_rows<NQ>(d, v0, v1, xk);
+#pragma unroll
+        for (int i = 0; i < kGvAhead; ++i) ring[i] = ring[i + 1];
+    }
+}
+
+// One pass over nr <= 2 NQ rows of a block: the k loop, then routing weight x
+// result into each row's token.  o is the lane's first output row.
+template <int FMT, int NQ, class Src>
+__device__ __forceinline__ void block_pass(const BlockDownArgs &a, RowPair (&ring)[kGvAhead + 1],
+                                           const Src &src, int kb0, int kb1, uint8_t *smem,
+                                           int span, const int *row_p, int nr, int o, int lane) {
+    const int g = lane >> 2, j4 = lane & 3;
+    const int slot = (g == j4) ? 0 : (g == j4 + 4) ? 1 : -1;
+    const uint8_t *act[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        const int m = 2 * q + slot;
+        act[q] = (slot >= 0 && m < nr) ? smem + kGvActOffset + (size_t)m * span : nullptr;
+    }
+    float d[NQ][4] = {};
+    reduce_rows<FMT, NQ>(d, ring, src, kb0, kb1, act, smem, a.dq);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        const int m = 2 * q + (j4 >> 1);
+        if (m >= nr) continue;
+        const int pm = row_p[m];
+        const float tw = a.topk_weights[pm];
+        float *y = a.out + (size_t)(pm / a.top_k) * a.H;  // output rows o, o + 1 (and + 64)
+        atomicAdd(reinterpret_cast<float2 *>(y + o), make_float2(tw * d[q][0], tw * d[q][1]));
+        atomicAdd(reinterpret_cast<float2 *>(y + o + 64), make_float2(tw * d[q][2], tw * d[q][3]));
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kGvThreads, kBdMinCtas) block_down_kernel(const BlockDownArgs a) {
+    constexpr int NQ = kBdRows / 2;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tiles2 = (a.RT2 + 1) / 2;  // 256-row CTA tiles
+    const int b = blockIdx.x % a.blocks_cap;
+    const int tq = (blockIdx.x / a.blocks_cap) % tiles2;
+    const int s = blockIdx.x / (a.blocks_cap * tiles2);
+    const int kb0 = s * a.KB2s;
+    const int kb1 = (kb0 + a.KB2s < a.KB2) ? kb0 + a.KB2s : a.KB2;
+    if (s >= a.SB || kb0 >= kb1) return;
+    // The routing buffers: the align kernel has completed before any CTA of
+    // this grid starts (the gate/up GEMM's predecessors wait for it before they
+    // launch their dependents), so they are read before the wait, through L2.
+    const int npp = __ldcg(a.num_post_pad);
+    if (b * a.block_m >= npp) return;
+    const int e = __ldcg(a.expert_ids + b);
+    if (e < 0 || e >= a.E) return;
+    const int span = a.KB2s * 128;
+    int *row_j = reinterpret_cast<int *>(smem + kGvActOffset + kBdRows * span);  // bucketed row
+    int *row_p = row_j + 32;                                                       // its pair
+    int *row_n = row_p + 32;
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (wid == 0) {  // the block's real rows (block_m <= 32), in bucketed order
+        const int j = b * a.block_m + lane;
+        const int p = lane < a.block_m ? __ldcg(a.sorted_ids + j) : a.P;
+        const bool real = p >= 0 && p < a.P;
+        const uint32_t m = __ballot_sync(0xffffffffu, real);
+        if (real) {
+            const int pos = __popc(m & ((1u << lane) - 1u));
+            row_j[pos] = j;
+            row_p[pos] = p;
+        }
+        if (lane == 0) *row_n = __popc(m);
+    }
+    const int r = 2 * tq + (wid >> 1);  // the warp's 128-row tile
+    const bool rows_in = r < a.RT2;
+    const int row = (wid & 1) * 32 + lane;  // rows row and row + 64 of the tile's slabs
+    const size_t st0 = ((size_t)e * a.RT2 + (rows_in ? r : 0)) * (a.KB2 / 2);
+    const uint8_t *w = a.w2 + st0 * kStageWBytes + row * 16;
+    const uint8_t *sc = a.s2 + st0 * kStageSBytes + row * 4;
+    const auto src = row_pair_src(
+        w, w + 64 * 16, sc, sc + 64 * 4,
+        [](int kb) { return (size_t)(kb >> 1) * kStageWBytes + (kb & 1) * kSlabBytes; },
+        [](int kb) { return (size_t)(kb >> 1) * kStageSBytes + (kb & 1) * (kStageSBytes / 2); });
+    RowPair ring[kGvAhead + 1];
+    if (rows_in) prefetch_slabs(ring, src, kb0, kb1);  // weights: call inputs, before the wait
+    zero_b_operand(smem);
+    pdl_wait();  // the intermediate and the zeroed accumulator
+    __syncthreads();
+    const int n = *row_n;
+    const int o = r * kSlabRows + (wid & 1) * 32 + (lane >> 2) * 4 + (lane & 1) * 2;
+    for (int c0 = 0; c0 < n; c0 += kBdRows) {
+        const int nr = (n - c0 < kBdRows) ? n - c0 : kBdRows;
+        // the pass's intermediate rows over the split's k range
+        const int n16 = (kb1 - kb0) * 8;  // 16-byte pieces per row
+        for (int c = threadIdx.x; c < nr * n16; c += blockDim.x) {
+            const int m = c / n16, k16 = c - m * n16;
+            const uint4 *ar = reinterpret_cast<const uint4 *>(
+                a.a_out + (size_t)row_j[c0 + m] * a.I + kb0 * 64);
+            reinterpret_cast<uint4 *>(smem + kGvActOffset + (size_t)m * span)[k16] =
+                __ldcg(ar + k16);
+        }
+        __syncthreads();
+        if (rows_in) {
+            if (c0 > 0) prefetch_slabs(ring, src, kb0, kb1);  // a further pass re-streams
+            // one variant per row-pair count: the MMAs stay unconditional
+            const int nq = (nr + 1) / 2;
+            if (nq == 1 || kBdRows <= 2)
+                block_pass<FMT, 1>(a, ring, src, kb0, kb1, smem, span, row_p + c0, nr, o, lane);
+            else if (nq == 2 || kBdRows <= 4)
+                block_pass<FMT, (kBdRows >= 4 ? 2 : 1)>(a, ring, src, kb0, kb1, smem, span,
+                                                        row_p + c0, nr, o, lane);
+            else if (nq == 3 || kBdRows <= 6)
+                block_pass<FMT, (kBdRows >= 6 ? 3 : 1)>(a, ring, src, kb0, kb1, smem, span,
+                                                        row_p + c0, nr, o, lane);
+            else
+                block_pass<FMT, (kBdRows >= 8 ? 4 : 1)>(a, ring, src, kb0, kb1, smem, span,
+                                                        row_p + c0, nr, o, lane);
+        }
+        __syncthreads();  // the staged rows are read before the next pass overwrites them
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(const GemvArgs &a, int step, cudaStream_t s, int *launches) {
@@ -335,6 +501,23 @@ cudaError_t launch_gemv(const GemvArgs &a, int step, cudaStream_t s, int *launch
     cfg.numAttrs = pdl_attr(attr);
     const cudaError_t e = (a.fmt == 1) ? cudaLaunchKernelEx(&cfg, gemv_down_kernel<1>, a)
                                        : cudaLaunchKernelEx(&cfg, gemv_down_kernel<0>, a);
+    if (e != cudaSuccess) return e;
+    if (launches) *launches += 1;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_down(const BlockDownArgs &a, cudaStream_t s, int *launches) {
+    static_assert(kBdRows == 2 || kBdRows == 4 || kBdRows == 6 || kBdRows == 8, "rows per pass");
+    if (a.block_m > 32 || a.blocks_cap <= 0) return cudaErrorInvalidValue;
+    const int grid = a.blocks_cap * ((a.RT2 + 1) / 2) * a.SB;
+    const size_t smem = kGvActOffset + (size_t)kBdRows * a.KB2s * 128 + 96 * sizeof(int);
+    if (smem > 48 * 1024) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = pdl_config((unsigned)grid, kGvThreads, smem, s);
+    cudaLaunchAttribute attr;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl_attr(attr);
+    const cudaError_t e = (a.fmt == 1) ? cudaLaunchKernelEx(&cfg, block_down_kernel<1>, a)
+                                       : cudaLaunchKernelEx(&cfg, block_down_kernel<0>, a);
     if (e != cudaSuccess) return e;
     if (launches) *launches += 1;
     return cudaGetLastError();

@@ -27,4 +27,24 @@ struct GemvArgs {
 // step 1: the gate/up kernel; step 2: the down kernel (programmatic dependent launch)
 cudaError_t launch_gemv(const GemvArgs &a, int step, cudaStream_t s, int *launches);
 
+// The down step of the separate plan at short routing blocks, in the same
+// style: per align block, the expert's down rows are streamed once and reduced
+// against the block's real rows of the gate/up intermediate, two rows per MMA.
+struct BlockDownArgs {
+    const int32_t *sorted_ids;   // [cap] pair of each bucketed row (>= P: padding)
+    const int32_t *expert_ids;   // [blocks] expert of each block
+    const int32_t *num_post_pad; // [1] rows in use (a multiple of block_m)
+    const uint16_t *a_out;       // [cap][I] fp16 intermediate, bucketed order
+    const float *topk_weights;   // [P]
+    const uint8_t *w2, *s2;      // packed down weights and scales
+    float *out;                  // [M][H] fp32 accumulator (zeroed by the gate/up GEMM)
+    uint32_t *err;
+    int P, E, H, I, top_k, block_m, blocks_cap;
+    int RT2, KB2, SB, KB2s;      // row tiles (H / 128), 64-k blocks, k splits, per split
+    int fmt;
+    DequantConsts dq;
+};
+// Programmatic dependent launch after the gate/up GEMM.
+cudaError_t launch_block_down(const BlockDownArgs &a, cudaStream_t s, int *launches);
+
 }  // namespace moe

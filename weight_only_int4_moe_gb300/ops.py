@@ -33,6 +33,7 @@ EXPORTED = [
     "moe_int4_packed_bytes", "moe_int4_packed_scale_bytes", "moe_int4_pack", "moe_mxfp4_pack",
     "moe_align_capacity", "moe_align_scratch_bytes", "moe_align",
     "moe_int4_workspace_bytes", "moe_int4_block_m", "moe_int4_fused", "moe_int4_gemv",
+    "moe_int4_block_down",
     "moe_int4_workspace_layout",
     "moe_int4_forward",
     "moe_int4_forward_host", "moe_int4_get_errors", "moe_int4_clear_errors",
@@ -94,6 +95,7 @@ def load_library(build_if_missing: bool = True):
             "moe_int4_workspace_bytes": ([i, sp, i], sz),
             "moe_int4_fused": ([i, sp], i),
             "moe_int4_gemv": ([i, sp], i),
+            "moe_int4_block_down": ([i, sp], i),
             "moe_int4_block_m": ([i, sp], i),
             "moe_int4_workspace_layout": ([i, sp, p], i),
             "moe_int4_forward": ([p] * 8 + [i, sp, p, sz, p], i),
@@ -267,6 +269,12 @@ def moe_int4_fused(M: int, shape: Shape) -> bool:
     """Whether a forward of M tokens runs the fused decode kernel (the gather
     and both GEMMs in one launch)."""
     return load_library().moe_int4_fused(M, ctypes.byref(shape)) == 1
+
+
+def moe_int4_block_down(M: int, shape: Shape) -> bool:
+    """Whether a forward of M tokens runs the separate plan's down step as
+    per-block matrix-vector work."""
+    return load_library().moe_int4_block_down(M, ctypes.byref(shape)) == 1
 
 
 def moe_int4_gemv(M: int, shape: Shape) -> bool:
