@@ -312,13 +312,14 @@ int moe_int4_workspace_layout(int M, const moe_int4_shape *shape, size_t *offset
  * matrix-vector kernels, gate/up + SwiGLU and then down + combine, each routed
  * pair reading its token's row and its expert's packed weights directly (no
  * align; a shared expert is read once per pair).  Otherwise the align kernel,
- * then, for routings of at most 512 pairs (decode batches), one persistent
- * tensor-core kernel that gathers x, runs the gate/up GEMM and then the down
- * GEMM (its CTAs hand work to each other through counters in the workspace,
- * with bounded waits; it expects to get every SM within about two seconds);
- * otherwise a gather kernel and one kernel per GEMM, where at routing blocks of
- * at most 16 rows the down step streams each block's expert once and reduces it
- * against the block's rows as matrix-vector work.  All plans form the same fp16 weights and intermediates and
+ * then either a gather kernel and one kernel per GEMM, where at routing blocks
+ * of at most 16 rows the down step streams each block's expert once and reduces
+ * it against the block's rows as matrix-vector work; or, for routings of at
+ * most 512 pairs whose blocks hold more than about 2.5 rows per expert (or with
+ * MOE_FLAG_NO_GEMV), one persistent tensor-core kernel that gathers x, runs the
+ * gate/up GEMM and then the down GEMM (its CTAs hand work to each other through
+ * counters in the workspace, with bounded waits; it expects to get every SM
+ * within about two seconds).  All plans form the same fp16 weights and intermediates and
  * accumulate in fp32; they differ only in summation order.  bf16 output adds a
  * conversion kernel.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,

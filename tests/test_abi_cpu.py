@@ -211,13 +211,17 @@ def test_launch_plans():
     Ms = (1, 8, 9, 16, 17, 64, 65, 90, 1024)
     # 8 of 384 experts per token: 128 pairs touch about 109.7 experts (1.17 per)
     assert [ops.moe_int4_gemv(M, k26) for M in Ms] == [True] * 4 + [False] * 5
-    assert [ops.moe_int4_fused(M, k26) for M in Ms] == [False] * 4 + [True, True, False, False,
-                                                                      False]
+    # the fused decode kernel gives way to the separate plan with the per-block
+    # down kernel where blocks hold at most 2.5 rows per expected touched expert
+    assert not any(ops.moe_int4_fused(M, k26) for M in Ms)
+    assert [ops.moe_int4_block_down(M, k26) for M in Ms] == [False] * 4 + [True] * 4 + [False]
     mid = ops.Shape.of(64, 6, 4096, 1408)
     # M = 4: 24 pairs on about 20.8 experts (1.15); M = 5: 30 on 24.9 (1.20+)
     assert [ops.moe_int4_gemv(M, mid) for M in (1, 4, 5, 32)] == [True, True, False, False]
     assert [ops.moe_int4_fused(M, mid) for M in (1, 32, 128, 2048, 8192)] == [False, True, False,
                                                                               False, False]
+    # mid-size M = 16: 96 pairs on about 50.8 experts (1.89); M = 32: 3.13
+    assert [ops.moe_int4_block_down(M, mid) for M in (5, 16, 32)] == [True, True, False]
     no_gemv = ops.Shape.of(64, 6, 4096, 1408, flags=ops.MOE_FLAG_NO_GEMV)
     assert ops.moe_int4_fused(1, no_gemv) and not ops.moe_int4_gemv(1, no_gemv)
     tiny = ops.Shape.of(8, 2, 256, 128)  # 8 experts of 55 KB: L2-resident
@@ -227,9 +231,9 @@ def test_launch_plans():
     assert not ops.moe_int4_fused(512, ops.Shape.of(3, 1, 256, 128))  # 512 pairs, block 192
     unfused = ops.Shape.of(384, 8, 7168, 2048, flags=ops.MOE_FLAG_UNFUSED)
     assert not ops.moe_int4_fused(1, unfused) and not ops.moe_int4_gemv(1, unfused)
-    # the separate plan's down step as per-block work at 16-row blocks only
-    assert [ops.moe_int4_block_down(M, k26) for M in (1, 64, 65, 90, 256)] == [
-        False, False, True, True, False]
+    # the per-block down kernel at 16-row blocks only, and never under either flag
+    assert not ops.moe_int4_block_down(256, k26)
     assert not ops.moe_int4_block_down(90, unfused)
-    assert not ops.moe_int4_block_down(90, ops.Shape.of(384, 8, 7168, 2048,
-                                                        flags=ops.MOE_FLAG_NO_GEMV))
+    k26_tc = ops.Shape.of(384, 8, 7168, 2048, flags=ops.MOE_FLAG_NO_GEMV)
+    assert not ops.moe_int4_block_down(90, k26_tc)
+    assert [ops.moe_int4_fused(M, k26_tc) for M in (1, 9, 64, 65)] == [True, True, True, False]

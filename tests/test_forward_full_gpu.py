@@ -106,3 +106,18 @@ def test_k26_separate_kernels(k26, workload, M):
     assert ops.moe_int4_fused(M, pw.shape) or ops.moe_int4_gemv(M, pw.shape)
     assert not ops.moe_int4_fused(M, b.shape) and not ops.moe_int4_gemv(M, b.shape)
     print(_check(w, b, inputs.WORKLOADS[workload], M))
+
+
+@pytest.mark.parametrize("M", [9, 64])
+def test_k26_fused_decode_kernel(k26, M):
+    """The fused decode kernel at the full K2.6 size (MOE_FLAG_NO_GEMV: at these
+    sizes the default plan runs the small-batch kernels or the separate plan
+    with the per-block down kernel)."""
+    ops = _ops()
+    w, pw = k26
+    b = copy.copy(pw)
+    sh = pw.shape
+    b.shape = ops.Shape.of(sh.E, sh.top_k, sh.hidden, sh.inter, sh.out_dtype, sh.weight_format,
+                           ops.MOE_FLAG_NO_GEMV)
+    assert not ops.moe_int4_fused(M, pw.shape) and ops.moe_int4_fused(M, b.shape)
+    print(_check(w, b, inputs.WORKLOADS["k26_decode"], M))

@@ -48,6 +48,12 @@ constexpr int kGemvMaxPairs = 128;
 // M = 90 1 548 / 1 593; at 32-row blocks verify M = 256 2 149 / 1 885, so not
 // there.  Its CTAs (4 warps, 8 block rows per pass) run 4 per SM.
 constexpr int kBlockDownMaxRows = 16;
+// Below kFusedMaxPairs the separate plan with this down step replaces the
+// fused decode kernel at up to this many pairs per expected touched expert
+// (same-box A/B, us: K2.6 M = 17 571 / 598, M = 32 894 / 956, M = 64 1 345 /
+// 1 435; mid-size M = 8 94 / 102, M = 16 132 / 134; but mid-size M = 32, 3.1
+// rows per expert, 166 / 157).
+constexpr double kBlockDownMaxRowsPerExpert = 2.5;
 constexpr int kBlockDownSlots = 152 * 4;
 constexpr double kGemvMaxRereads = 1.2;
 constexpr int kGemvMaxPairsL2 = 256;
@@ -131,20 +137,24 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
     p.cap = (size_t)p.P + touched * (size_t)(p.BM - 1);
     p.blocks_cap = p.cap / p.BM + 1;
     p.tiles1_cap = p.blocks_cap * p.RT1;
+    // expected touched experts: each token picks top_k distinct of E
+    const double exp_touched = p.E * (1.0 - std::pow(1.0 - (double)p.k / p.E, (double)p.M));
     {
-        // expected touched experts: each token picks top_k distinct of E
-        const double miss = std::pow(1.0 - (double)p.k / p.E, (double)p.M);
-        const double touched = p.E * (1.0 - miss);
         const double expert_bytes = 3.0 * p.H * p.I * (0.5 + 2.0 / 32);  // weights + scales
         const bool in_l2 = p.E * expert_bytes <= kGemvL2Bytes;
         p.gemv = !(sh->flags & (MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) &&
                  (in_l2 ? p.P <= kGemvMaxPairsL2
-                        : p.P <= kGemvMaxPairs && p.P <= kGemvMaxRereads * touched);
+                        : p.P <= kGemvMaxPairs && p.P <= kGemvMaxRereads * exp_touched);
     }
-    p.fused = !p.gemv && !(sh->flags & MOE_FLAG_UNFUSED) && p.P <= kFusedMaxPairs && p.BM <= 128;
-    p.block_down = !p.gemv && !p.fused &&
-                   !(sh->flags & (MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) &&
-                   p.BM <= kBlockDownMaxRows;
+    // The per-block down kernel where blocks are short; below the fused kernel's
+    // pair limit only where they hold few rows, since with fuller blocks the
+    // fused kernel's single launch wins.
+    const bool block_down_ok = !p.gemv && !(sh->flags & (MOE_FLAG_UNFUSED | MOE_FLAG_NO_GEMV)) &&
+                               p.BM <= kBlockDownMaxRows;
+    const bool few_rows = p.P <= kBlockDownMaxRowsPerExpert * exp_touched;
+    p.fused = !p.gemv && !(sh->flags & MOE_FLAG_UNFUSED) && p.P <= kFusedMaxPairs &&
+              p.BM <= 128 && !(block_down_ok && few_rows);
+    p.block_down = block_down_ok && !p.fused;
     if (p.gemv || p.block_down) {
         // (splits, 64-k blocks per split) of n blocks over `base` CTAs per split:
         // the fewest waves x (blocks per CTA + fixed cost), fewer splits on ties
