@@ -28,6 +28,7 @@ CASES = [
     (64, 6, 512, 256, 700, "skewed"),      # multi-block align, skewed routing
     (8, 2, 512, 256, 1000, "uniform"),     # wide 192
     (128, 8, 1024, 512, 200, "uniform"),   # round-robin waves then the split part
+    (384, 8, 256, 128, 90, "uniform"),     # 16, separate plan: the per-block down kernel
 ]
 
 
@@ -49,7 +50,8 @@ def run_case(E, k, H, I, M, routing, seed, flags=0):
                                 t["topk_weights"])
     m = assert_parity(out.cpu().numpy(), ref, f"E{E} M{M}")
     plan = "small-batch" if ops.moe_int4_gemv(M, pw.shape) else (
-        f"block_m={ops.moe_int4_block_m(M, pw.shape)}")
+        f"block_m={ops.moe_int4_block_m(M, pw.shape)}" +
+        (", per-block down" if ops.moe_int4_block_down(M, pw.shape) else ""))
     print(f"E={E} k={k} H={H} I={I} M={M} {plan} "
           f"max/rms={m['max_over_rms']:.2e} rel_l1={m['rel_l1']:.2e}", flush=True)
     return w, pw
@@ -131,12 +133,13 @@ def main():
     assert ops.debug_bounds(), "run with MOE_INT4_DEBUG_BOUNDS=1"
     ops.load_library()
     assert ops.library_path() == build.DEBUG_LIB
-    # every case through the tensor-core kernels, and through the small-batch
-    # kernels where the default plan picks them
+    # every case through the tensor-core kernels, and through the matrix-vector
+    # kernels (small-batch or per-block down) where the default plan picks them
     for i, case in enumerate(CASES):
         run_case(*case, seed=i, flags=ops.MOE_FLAG_NO_GEMV)
         E, k, H, I, M, _ = case
-        if ops.moe_int4_gemv(M, ops.Shape.of(E, k, H, I)):
+        sh = ops.Shape.of(E, k, H, I)
+        if ops.moe_int4_gemv(M, sh) or ops.moe_int4_block_down(M, sh):
             run_case(*case, seed=i)
     for flags in (ops.MOE_FLAG_NO_GEMV, 0):
         run_invalid_ids(flags)

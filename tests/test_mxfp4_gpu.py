@@ -65,6 +65,7 @@ SHAPES = [
     (64, 6, 512, 256, 700, 4),    # multi-block align
     (8, 2, 512, 256, 1000, 5),    # wide 192
     (4, 2, 384, 256, 300, 6),     # wide 192, three down row tiles
+    (384, 8, 256, 128, 90, 7),    # default plan: separate, per-block down kernel
 ]
 
 

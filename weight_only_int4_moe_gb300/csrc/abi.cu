@@ -651,6 +651,7 @@ int forward_impl(const uint16_t *x, const void *w13_packed, const void *w13_scal
             bd.top_k = pl.k;
             bd.block_m = pl.BM;
             bd.blocks_cap = (int)pl.blocks_cap;
+            bd.cap = g.cap;
             bd.RT2 = pl.RT2;
             bd.KB2 = pl.I / 64;
             bd.SB = pl.bd_SB;

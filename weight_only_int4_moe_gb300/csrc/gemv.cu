@@ -407,10 +407,12 @@ __global__ void __launch_bounds__(kGvThreads, kBdMinCtas) block_down_kernel(cons
     // The routing buffers: the align kernel has completed before any CTA of
     // this grid starts (the gate/up GEMM's predecessors wait for it before they
     // launch their dependents), so they are read before the wait, through L2.
-    const int npp = __ldcg(a.num_post_pad);
+    // (Debug-bounds builds record an out-of-range value and skip the block.)
+    int npp = __ldcg(a.num_post_pad);
+    if (!bounds_ok(npp >= 0 && npp <= a.cap && npp % a.block_m == 0, a.err)) npp = 0;
     if (b * a.block_m >= npp) return;
     const int e = __ldcg(a.expert_ids + b);
-    if (e < 0 || e >= a.E) return;
+    if (!bounds_ok(e >= 0 && e < a.E, a.err) || e < 0 || e >= a.E) return;
     const int span = a.KB2s * 128;
     int *row_j = reinterpret_cast<int *>(smem + kGvActOffset + kBdRows * span);  // bucketed row
     int *row_p = row_j + 32;                                                       // its pair
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(kGvThreads, kBdMinCtas) block_down_kernel(cons
     if (wid == 0) {  // the block's real rows (block_m <= 32), in bucketed order
         const int j = b * a.block_m + lane;
         const int p = lane < a.block_m ? __ldcg(a.sorted_ids + j) : a.P;
-        const bool real = p >= 0 && p < a.P;
+        const bool real = bounds_ok(p >= 0, a.err) && p >= 0 && p < a.P;  // >= P: padding
         const uint32_t m = __ballot_sync(0xffffffffu, real);
         if (real) {
             const int pos = __popc(m & ((1u << lane) - 1u));

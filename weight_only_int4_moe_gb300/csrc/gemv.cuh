@@ -40,6 +40,7 @@ struct BlockDownArgs {
     float *out;                  // [M][H] fp32 accumulator (zeroed by the gate/up GEMM)
     uint32_t *err;
     int P, E, H, I, top_k, block_m, blocks_cap;
+    int cap;                     // rows of sorted_ids and a_out
     int RT2, KB2, SB, KB2s;      // row tiles (H / 128), 64-k blocks, k splits, per split
     int fmt;
     DequantConsts dq;
