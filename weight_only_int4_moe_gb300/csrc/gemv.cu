@@ -32,8 +32,12 @@
 //    range, forms the fp16 intermediate SiLU(g) * u (saturating, as the GEMM
 //    epilogue does), and adds routing weight x result into the token's fp32
 //    output row with float2 atomics.
-// The k splits are chosen per call (moe_int4_forward) so the grid is about one
-// wave of small CTAs over the SMs.
+//  * Per-block down kernel (the separate plan's down step at routing blocks of
+//    at most 16 rows): CTA (k split, 256 output rows, align block); the block's
+//    real rows of the gate/up intermediate take the activation's place, two rows
+//    per MMA (columns 0..3 and 4..7).
+// The k splits are chosen per call (moe_int4_forward): the grid of the small-
+// batch kernels is about one wave of small CTAs over the SMs.
 #include <cuda_fp16.h>
 
 #include "dequant.cuh"
@@ -46,14 +50,11 @@ namespace {
 
 constexpr int kGvWarps = 4;
 constexpr int kGvThreads = 32 * kGvWarps;
-#ifndef GV_AHEAD
-#define GV_AHEAD 1
-#endif
-#ifndef GV_MIN_CTAS
-#define GV_MIN_CTAS 6
-#endif
-constexpr int kGvAhead = GV_AHEAD;      // slabs of weight loads in flight per warp
-constexpr int kGvMinCtas = GV_MIN_CTAS;  // resident CTAs per SM the register budget allows
+// One slab of loads in flight per warp ahead of the one being reduced, and six
+// resident CTAs per SM (80 registers per thread): two slabs at five CTAs, or
+// rings of 2-4 slabs in shared memory, measured slower.
+constexpr int kGvAhead = 1;
+constexpr int kGvMinCtas = 6;
 // Shared memory of both kernels: 128 bytes of zeros (the B operand of the
 // off-diagonal lanes), 64 bytes of padding so that the zeros and the
 // activation rows sit in different banks, then the split's activation in fp16.
@@ -312,19 +313,16 @@ __global__ void __launch_bounds__(kGvThreads, kGvMinCtas) gemv_down_kernel(const
 }
 
 // ---------------------------------------------------------------- block down --
-// The separate plan's down step at short routing blocks (16 or 32 rows): per
+// The separate plan's down step at short routing blocks (up to 32 rows; the plan
+// uses it at 16, where it measured faster than the down GEMM): per
 // align block, a CTA streams 256 of the expert's down rows over its k split once
 // and reduces them against the block's real rows of the gate/up intermediate,
 // up to kBdRows at a time: MMA q takes rows 2q (result columns 0..3) and 2q + 1
 // (columns 4..7) of the pass, through the same block-diagonal operand as above.
-#ifndef GV_BD_ROWS
-#define GV_BD_ROWS 8
-#endif
-#ifndef GV_BD_MIN_CTAS
-#define GV_BD_MIN_CTAS 4
-#endif
-constexpr int kBdRows = GV_BD_ROWS;          // block rows per pass (two per MMA)
-constexpr int kBdMinCtas = GV_BD_MIN_CTAS;   // resident CTAs per SM (registers)
+// Block rows per pass (two per MMA) and resident CTAs per SM (111 registers
+// per thread); four rows at five CTAs ran alike, two at six were slower.
+constexpr int kBdRows = 8;
+constexpr int kBdMinCtas = 4;
 
 // One slab against NQ row pairs of a pass.
 template <int NQ>
