@@ -52,6 +52,7 @@ def _capture(fn):
     (16, 4, 384, 256, 37, "uniform", "tensor"),      # ragged M, single-block align
     (64, 6, 512, 256, 700, "skewed", "default"),     # multi-block align, skewed routing
     (8, 2, 512, 256, 1000, "uniform", "default"),    # wide blocks of 192 rows
+    (384, 8, 256, 128, 90, "uniform", "default"),    # 16-row blocks: the per-block down kernel
 ])
 def test_forward_graph_replays_new_inputs(E, k, H, I, M, routing, plan):
     import torch
