@@ -41,20 +41,6 @@ constexpr int kFusedMaxPairs = 512;
 // M = 9, 208 / 157 at mid-size M = 32; most groups hold one pair there, and the
 // search and the second MMA set cost more than the re-reads.
 constexpr int kGemvMaxPairs = 128;
-// The separate plan's down step runs as per-block matrix-vector work (one pass
-// over the expert's down rows per routing block) at blocks of up to this many
-// rows.
-// Same-box A/B against the down GEMM (us per call): K2.6 M = 65 1 372 / 1 431,
-// M = 90 1 548 / 1 593; at 32-row blocks verify M = 256 2 149 / 1 885, so not
-// there.  Its CTAs (4 warps, 8 block rows per pass) run 4 per SM.
-constexpr int kBlockDownMaxRows = 16;
-// Below kFusedMaxPairs the separate plan with this down step replaces the
-// fused decode kernel at up to this many pairs per expected touched expert
-// (same-box A/B, us: K2.6 M = 17 571 / 598, M = 32 894 / 956, M = 64 1 345 /
-// 1 435; mid-size M = 8 94 / 102, M = 16 132 / 134; but mid-size M = 32, 3.1
-// rows per expert, 166 / 157).
-constexpr double kBlockDownMaxRowsPerExpert = 2.5;
-constexpr int kBlockDownSlots = 152 * 4;
 constexpr double kGemvMaxRereads = 1.2;
 constexpr int kGemvMaxPairsL2 = 256;
 constexpr double kGemvL2Bytes = 64.0 * (1 << 20);
@@ -63,6 +49,19 @@ constexpr double kGemvL2Bytes = 64.0 * (1 << 20);
 // units of one 64-k block of its loop.
 constexpr int kGemvSlots = 152 * 6;
 constexpr int kGemvCtaCost = 2;
+// The separate plan's down step runs as per-block matrix-vector work (one pass
+// over the expert's down rows per routing block) at blocks of up to this many
+// rows.  Same-box A/B against the down GEMM (us per call): K2.6 M = 65 1 372 /
+// 1 431, M = 90 1 548 / 1 593; at 32-row blocks verify M = 256 2 149 / 1 885,
+// so not there.  Its CTAs (4 warps, 8 block rows per pass) run 4 per SM.
+constexpr int kBlockDownMaxRows = 16;
+constexpr int kBlockDownSlots = 152 * 4;
+// Below kFusedMaxPairs the separate plan with this down step replaces the
+// fused decode kernel at up to this many pairs per expected touched expert
+// (same-box A/B, us: K2.6 M = 17 571 / 598, M = 32 894 / 956, M = 64 1 345 /
+// 1 435; mid-size M = 8 94 / 102, M = 16 132 / 134; but mid-size M = 32, 3.1
+// rows per expert, 166 / 157).
+constexpr double kBlockDownMaxRowsPerExpert = 2.5;
 constexpr int kAlignChunk = 1024;
 
 thread_local int g_last_launches = 0;
