@@ -181,8 +181,7 @@ Plan make_plan(int M, const moe_int4_shape *sh) {
         } else {
             // about one routing block per touched expert; at most 32 blocks per
             // split (eight intermediate rows of 4 KB)
-            const double miss = std::pow(1.0 - (double)p.k / p.E, (double)p.M);
-            const int blocks = (int)std::ceil(p.E * (1.0 - miss));
+            const int blocks = (int)std::ceil(exp_touched);
             const auto b = splits(blocks * ((p.RT2 + 1) / 2), p.I / 64, 32, kBlockDownSlots);
             p.bd_SB = b.first;
             p.bd_KB2s = b.second;
